@@ -1,0 +1,70 @@
+"""Pure-Python brute force of paged decode attention for tiny inputs (TEST INFRASTRUCTURE ONLY).
+
+A second implementation, independent of ``pa_oracle.c``: it decodes stored
+bits with ``struct`` (binary16 via the 'e' format, bfloat16 by padding to a
+binary32), builds each sequence's contiguous key and value lists by walking the
+block table token by token, and evaluates softmax(scale * q k^T) v with Python
+floats (IEEE double) and ``math.exp``.
+
+Source: "PagedAttention 详解：缓存的存储结构", sections "Block Table" and
+"软件地址翻译" (token i lives at offset i % B of block block_tables[s][i // B]);
+"vLLM 核心工程深度剖析", section "3.1 Kernel 签名与分块策略" (the scaled
+softmax and the value-weighted sum).
+"""
+from __future__ import annotations
+
+import math
+import struct
+
+
+def _decode(bits_or_value, dtype: str) -> float:
+    if dtype == "f32":
+        return float(bits_or_value)
+    if dtype == "f16":
+        return struct.unpack("<e", struct.pack("<H", int(bits_or_value)))[0]
+    return struct.unpack("<f", struct.pack("<I", int(bits_or_value) << 16))[0]
+
+
+def _flat_values(arr, dtype: str) -> list[float]:
+    """Python floats of an array given as float32 values, float16 values or bf16 bit patterns."""
+    if dtype == "f16":
+        return [_decode(int(b), "f16") for b in arr.reshape(-1).view("uint16")]
+    return [_decode(x, dtype) for x in arr.reshape(-1).tolist()]
+
+
+def paged_attention(q, k_cache, v_cache, block_tables, seq_lens, *, dtype: str, num_kv_heads: int,
+                    block_size: int, scale: float) -> list:
+    """Nested lists out[s][h][d]; cache layout [blocks][kv_heads][block_size][head_size]."""
+    N, Hq, D = q.shape
+    G = Hq // num_kv_heads
+    qf = _flat_values(q, dtype)
+    kf = _flat_values(k_cache, dtype)
+    vf = _flat_values(v_cache, dtype)
+
+    def row(cache, blk, head, slot):
+        base = ((blk * num_kv_heads + head) * block_size + slot) * D
+        return cache[base:base + D]
+
+    out = []
+    for s in range(N):
+        L = int(seq_lens[s])
+        per_head = []
+        for h in range(Hq):
+            hkv = h // G
+            qv = qf[(s * Hq + h) * D:(s * Hq + h + 1) * D]
+            keys, values = [], []
+            for i in range(L):
+                blk = int(block_tables[s][i // block_size])
+                off = i % block_size
+                keys.append(row(kf, blk, hkv, off))
+                values.append(row(vf, blk, hkv, off))
+            if L == 0:
+                per_head.append([0.0] * D)
+                continue
+            scores = [scale * sum(a * b for a, b in zip(qv, k)) for k in keys]
+            mx = max(scores)
+            ex = [math.exp(x - mx) for x in scores]
+            den = sum(ex)
+            per_head.append([sum(e * v[d] for e, v in zip(ex, values)) / den for d in range(D)])
+        out.append(per_head)
+    return out
