@@ -1,0 +1,480 @@
+"""Benchmark of the paged decode step on GB300.
+
+One step = every row of the hot path over one batch: the copy-on-write block
+copies (workloads that have them), the slot-mapping append of the step's new
+tokens, and paged decode attention (block-table gather, K/V streaming, QK^T,
+online softmax, PV and, for long contexts, the partition merge).
+
+Prints ONE JSON line (rank 0).  ``value`` = KV GB/s: algorithmic K+V bytes the
+attention reads per step, summed over ranks, divided by the device time of a
+step (max over ranks).  Default workload: MHA fp16 decode (64 seqs, lens
+U[128, 2048], 32 heads, D = 128, B = 16, pool 8192, one append per seq).
+
+--impl reference times the CPU fp64 evaluation (the test oracle) on the host
+cores instead, on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s (fraction of GB300 HBM peak) and decode tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0
+WORKLOAD_DESC = {
+    "mha_f16": "MHA fp16 decode: 64 seqs, seq_lens U[128,2048], 32 q = 32 kv heads, D 128, B 16, pool 8192 shuffled, "
+               "one reshape_and_cache append per seq, then attention",
+    "gqa_bf16": "GQA bf16 decode: 128 seqs, 64 q / 8 kv heads, D 128, B 32, lognormal(ln 1200, 0.6) lens in "
+                "[64, 4096], pool 1.2x needed, shuffled",
+    "shared_prefix_f16": "shared-prefix fp16: 16 prompts x 8 branches, 1024-token shared prefix, suffix U[1,256], "
+                         "32 heads, D 128, B 16; 128 CoW block copies + suffix appends, then attention",
+    "long_bf16_b16": "long bf16 split-KV: 8 seqs x 32768 tokens, 32 q / 8 kv heads, D 128, B 16, 512-token partitions",
+    "long_bf16_b32": "long bf16 split-KV: 8 seqs x 32768 tokens, 32 q / 8 kv heads, D 128, B 32, 512-token partitions",
+    "long_bf16_b64": "long bf16 split-KV: 8 seqs x 32768 tokens, 32 q / 8 kv heads, D 128, B 64, 512-token partitions",
+}
+TORCH_DT = {"f32": "float32", "f16": "float16", "bf16": "bfloat16"}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return None
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_32_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu summary,
+    valid only while the kernel sources are unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(workload)
+    if not entry or entry.get("source_sha") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the GPU works."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        inside = [p for (t, p) in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        if not inside:  # the timed region was shorter than the sampling period: nearest sample
+            mid = 0.5 * (t0 + t1)
+            inside = [min(self.samples, key=lambda tp: abs(tp[0] - mid))[1]]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside),
+                "power_w_max": max((num(p[3]) or 0.0) for p in inside)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def all_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------------- GPU arm
+class DeviceStep:
+    """All device buffers of one workload and the library calls of one step."""
+
+    def __init__(self, w: W.Workload, device):
+        import torch
+        import paged_kv_cache_32_gb300 as pa
+        self.pa, self.w, self.dev = pa, w, device
+        tdt = getattr(torch, TORCH_DT[w.dtype])
+        self.k, self.v = W.device_caches(w, device)
+        self.desc = pa.cache_desc(self.k)
+
+        def t(a, dtype=None):
+            if a is None:
+                return None
+            if w.dtype == "bf16" and dtype is None and a.dtype == np.uint16:
+                return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+            return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        self.q = t(w.q)
+        self.tables = t(w.block_tables)
+        self.lens = t(w.seq_lens)
+        self.pairs = t(w.copy_pairs) if w.copy_pairs is not None and len(w.copy_pairs) else None
+        self.slots = t(w.slot_mapping) if w.slot_mapping is not None and len(w.slot_mapping) else None
+        self.nk = t(w.new_key) if self.slots is not None else None
+        self.nv = t(w.new_value) if self.slots is not None else None
+        self.out = torch.empty_like(self.q)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.part = pa.pa_decode_partition_size(w.max_blocks_per_seq, self.desc, w.partition_size)
+        need = pa.pa_decode_workspace_size(w.num_seqs, w.num_q_heads, w.max_blocks_per_seq, self.desc,
+                                           w.partition_size)
+        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        self.ws_bytes = need
+        self.pmax = 1 if need == 0 else -(-w.max_blocks_per_seq * w.block_size // self.part)
+        assert tdt == self.q.dtype
+
+    def launches_per_step(self) -> int:
+        return (self.pairs is not None) + (self.slots is not None) + 1 + (self.pmax > 1)
+
+    def writes(self, stream):
+        if self.pairs is not None:
+            self.pa.pa_copy_blocks(self.k, self.v, self.pairs, err_flag=self.err, stream=stream, desc=self.desc)
+        if self.slots is not None:
+            self.pa.pa_reshape_and_cache(self.k, self.v, self.nk, self.nv, self.slots, err_flag=self.err,
+                                         stream=stream, desc=self.desc)
+
+    def decode(self, stream, q=None, tables=None, lens=None, out=None):
+        self.pa.pa_decode(self.out if out is None else out, self.q if q is None else q, self.k, self.v,
+                          self.tables if tables is None else tables, self.lens if lens is None else lens,
+                          self.w.scale, partition_size=self.w.partition_size, workspace=self.ws,
+                          err_flag=self.err, stream=stream, desc=self.desc)
+
+    def decode_bytes(self) -> int:
+        """Algorithmic HBM bytes of one pa_decode call: K+V of every token, q in,
+        out, table entries, and the split-KV partial results (written then read)."""
+        w = self.w
+        eb = W.ELEM_BYTES[w.dtype]
+        b = w.kv_bytes() + 2 * w.num_seqs * w.num_q_heads * w.head_size * eb
+        b += int(np.sum(-(-w.seq_lens.astype(np.int64) // w.block_size))) * 4 + w.num_seqs * 4
+        if self.pmax > 1:
+            nparts = -(-w.seq_lens.astype(np.int64) // self.part)
+            multi = nparts[nparts > 1]
+            b += 2 * int(multi.sum()) * w.num_q_heads * (w.head_size + 2) * 4
+        return b
+
+
+def time_device(ds: DeviceStep, steps: int, warmup: int, world: int):
+    import torch
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            ds.writes(stream)
+            ds.decode(stream)
+        stream.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.time()
+        for i in range(steps):
+            ev[i][0].record(stream)
+            ds.writes(stream)
+            ev[i][1].record(stream)
+            ds.decode(stream)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        barrier(world)
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    decode_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)]
+    write_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)]
+    return total_ms / steps, decode_ms, write_ms, (t0, t1)
+
+
+def time_e2e(ds: DeviceStep, steps: int, warmup: int, world: int):
+    """Same step through the public API with the step's inputs copied from pinned
+    host memory and the output copied back, inside the timed region."""
+    import torch
+    w = ds.w
+    host = {}
+
+    def pin(name, tens):
+        if tens is not None:
+            host[name] = tens.detach().cpu().pin_memory()
+    pin("q", ds.q), pin("tables", ds.tables), pin("lens", ds.lens)
+    pin("slots", ds.slots), pin("nk", ds.nk), pin("nv", ds.nv), pin("pairs", ds.pairs)
+    out_host = torch.empty(ds.out.shape, dtype=ds.out.dtype).pin_memory()
+    dev = {k: torch.empty_like(v, device=ds.dev) for k, v in host.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    stream = torch.cuda.Stream()
+
+    def one():
+        for k, v in host.items():
+            dev[k].copy_(v, non_blocking=True)
+        if ds.pairs is not None:
+            ds.pa.pa_copy_blocks(ds.k, ds.v, dev["pairs"], err_flag=ds.err, stream=stream, desc=ds.desc)
+        if ds.slots is not None:
+            ds.pa.pa_reshape_and_cache(ds.k, ds.v, dev["nk"], dev["nv"], dev["slots"], err_flag=ds.err,
+                                       stream=stream, desc=ds.desc)
+        ds.decode(stream, q=dev["q"], tables=dev["tables"], lens=dev["lens"])
+        out_host.copy_(ds.out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            one()
+        stream.synchronize()
+        barrier(world)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(steps):
+            one()
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    return start.elapsed_time(end) / steps, h2d, d2h
+
+
+def cpu_baseline(w_meta: W.Workload, budget_s: float = 12.0):
+    """The oracle as it stands, on the host cores, over a bounded sample of the
+    workload (whole sequences, in order), repeated until the budget is used."""
+    import oracle as O
+    threads = O.max_threads()
+    n = w_meta.num_seqs
+    take = list(range(min(n, 16)))
+    sample = W.host_sample(w_meta, take)
+    kw = dict(dtype=sample.dtype, num_kv_heads=sample.num_kv_heads, block_size=sample.block_size)
+    reps, t_total = 0, 0.0
+    while t_total < budget_s and reps < 50:
+        k, v = sample.k_cache.copy(), sample.v_cache.copy()
+        t0 = time.perf_counter()
+        W.apply_writes_host(sample, k, v,
+                            lambda kk, vv, pairs: O.copy_blocks(kk, vv, pairs, head_size=sample.head_size, **kw),
+                            lambda kk, vv, nk, nv, sl: O.reshape_and_cache(kk, vv, nk, nv, sl, **kw))
+        O.paged_attention(sample.q, k, v, sample.block_tables, sample.seq_lens, scale=sample.scale,
+                          threads=threads, **kw)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    gbs = reps * sample.kv_bytes() / t_total / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(take)} of {n} sequences ({int(sample.seq_lens.sum())} tokens) x {reps} repetitions, "
+                      f"{t_total:.1f} s wall, OpenMP over (seq, q head)",
+            "tokens_per_s": reps * len(take) / t_total}
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import paged_kv_cache_32_gb300 as pa
+    pa.build()
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    w = W.WORKLOADS[args.workload](materialize=False)
+    ds = DeviceStep(w, device)
+    sampler = ClockSampler(local)
+    sampler.start()
+    ms_step, decode_ms, write_ms, (t0, t1) = time_device(ds, args.steps, args.warmup, world)
+    ms_step = all_max(ms_step, world)
+    dec_ms = statistics.mean(decode_ms)
+    e2e_ms, h2d, d2h = time_e2e(ds, args.steps, args.warmup, world)
+    e2e_ms = all_max(e2e_ms, world)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+    err = int(ds.err.item())
+    if err:
+        raise RuntimeError(f"device error flag {err}")
+
+    kv = w.kv_bytes()
+    value = world * kv / (ms_step * 1e-3) / 1e9
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs") if peaks else None
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or FALLBACK_HBM_GBS
+    dbytes = ds.decode_bytes()
+    achieved = dbytes / (dec_ms * 1e-3) / 1e9
+    traffic = ncu_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded; K/V pools drawn N(0,1) on device)",
+        "config": {"workload": args.workload, "description": WORKLOAD_DESC.get(args.workload, args.workload),
+                   "num_seqs": w.num_seqs, "tokens": int(w.seq_lens.sum()), "kv_bytes_per_step": kv,
+                   "partition_size": ds.part, "l2": "inputs larger than L2 (K/V working set "
+                   f"{kv / 1e9:.2f} GB vs 0.13 GB L2); no flush", "parallelism": f"replicas x{world}"},
+        "tokens_per_s": round(world * w.num_seqs / (ms_step * 1e-3), 1),
+        "roofline": {"bound": "hbm", "kernel": "pa_decode (decode_tc_kernel + merge_kernel when split)",
+                     "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_src, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": dbytes, "launch_ms": round(dec_ms, 5),
+                     "nominal_peak": NOMINAL_HBM_GBS},
+        "writes_ms": round(statistics.mean(write_ms), 5),
+        "e2e": {"value": round(world * kv / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": ds.launches_per_step() * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_extra and world == 1:
+        line["other_workloads"] = {}
+        for name in args.extra:
+            if name == args.workload:
+                continue
+            wx = W.WORKLOADS[name](materialize=False)
+            dx = DeviceStep(wx, device)
+            msx, dmx, _, _ = time_device(dx, max(5, args.steps), args.warmup, 1)
+            dm = statistics.mean(dmx)
+            ab = dx.decode_bytes()
+            line["other_workloads"][name] = {
+                "kv_gbs_step": round(wx.kv_bytes() / (msx * 1e-3) / 1e9, 1), "ms_per_step": round(msx, 5),
+                "decode_ms": round(dm, 5), "decode_achieved_gbs": round(ab / (dm * 1e-3) / 1e9, 1),
+                "decode_frac": round(ab / (dm * 1e-3) / 1e9 / peak, 4), "tokens_per_s": round(wx.num_seqs / (msx * 1e-3), 1)}
+            if name == "shared_prefix_f16":
+                line["other_workloads"][name]["unique_kv_bytes"] = wx.unique_kv_bytes()
+            del dx
+            torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, world, rank):
+    """CPU fp64 evaluation (the oracle) of the same step on bounded samples."""
+    if rank != 0:
+        return
+    import oracle as O
+    w = W.WORKLOADS[args.workload](materialize=False)
+    threads = O.max_threads()
+    n_take = min(w.num_seqs, 4)
+    samples = [W.host_sample(w, [(i * n_take + j) % w.num_seqs for j in range(n_take)], seed=i)
+               for i in range(max(1, min(args.steps, 8)))]
+    kw = lambda s: dict(dtype=s.dtype, num_kv_heads=s.num_kv_heads, block_size=s.block_size)
+
+    def step(s):
+        k, v = s.k_cache.copy(), s.v_cache.copy()
+        W.apply_writes_host(s, k, v,
+                            lambda kk, vv, pairs: O.copy_blocks(kk, vv, pairs, head_size=s.head_size, **kw(s)),
+                            lambda kk, vv, nk, nv, sl: O.reshape_and_cache(kk, vv, nk, nv, sl, **kw(s)))
+        O.paged_attention(s.q, k, v, s.block_tables, s.seq_lens, scale=s.scale, threads=threads, **kw(s))
+    for i in range(args.warmup):
+        step(samples[i % len(samples)])
+    t0 = time.perf_counter()
+    kv = 0
+    for i in range(args.steps):
+        s = samples[i % len(samples)]
+        step(s)
+        kv += s.kv_bytes()
+    dt = time.perf_counter() - t0
+    value = kv / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)",
+            "config": {"workload": args.workload, "description": WORKLOAD_DESC.get(args.workload, args.workload),
+                       "sample_seqs_per_step": n_take},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{n_take} of {w.num_seqs} sequences per step, CPU fp64 oracle"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mha_f16", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--extra", nargs="*", default=["gqa_bf16", "long_bf16_b16", "long_bf16_b32", "long_bf16_b64",
+                                                   "shared_prefix_f16"])
+    ap.add_argument("--no-extra", action="store_true", help="time only the headline workload")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,160 @@
+/*
+ * pa.h - C ABI of the paged decode-attention library (libpa.so) for GB300 (sm_103a).
+ *
+ * The library implements the decode hot path of PagedAttention: single-query
+ * attention over a KV cache held in fixed-size physical blocks reached through
+ * per-sequence block tables, the slot-mapping append that writes new K/V into
+ * the cache, and the whole-block copy used by copy-on-write.
+ *
+ * Sources (page title, section):
+ *  [P1] "PagedAttention 详解：缓存的存储结构" - "Block Table", "软件地址翻译"
+ *       (software address translation), "写入新 K/V" (writing new K/V).
+ *  [P2] "PagedAttention 笔记" - "写时复制是正确性的边界" (copy-on-write).
+ *  [P3] "vLLM 核心工程深度剖析" - "3.1 Kernel 签名与分块策略" (kernel signature),
+ *       "4.1 Beam Search 中的 CoW" (block-level copy).
+ *  [P4] "PagedAttention是什麼？" - "PagedAttention Kernel在做什麼？" (grid over
+ *       sequence, head and partition; partition reduction for long contexts).
+ *
+ * Conventions shared by every call
+ *  - All data pointers are DEVICE pointers owned by the caller.  The library
+ *    allocates no memory and keeps no state between calls except a lazily
+ *    resolved driver entry point and per-kernel launch attributes.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Every call is asynchronous on that stream.
+ *  - Cache layout (both K and V): [num_blocks][num_kv_heads][block_size][head_size],
+ *    dense, element type `dtype`.  One (block, kv head) is one contiguous run of
+ *    block_size * head_size elements.
+ *  - Return value: PA_OK, or a PA_ERR_* code for an argument error detected on
+ *    the host, in which case NOTHING is launched; PA_ERR_CUDA if a launch failed.
+ *  - Data errors (a bad block ID or slot inside device arrays) are detected on
+ *    the device.  The offending item is skipped (never read or written out of
+ *    bounds); if `err_flag` is non-NULL the first error code (PA_DEVERR_*) is
+ *    stored there with an atomic compare-and-swap from 0.  `err_flag` is a
+ *    device int32 the caller zeroes.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+
+/* Shape of one layer's KV cache pair. */
+typedef struct {
+  int32_t num_blocks;   /* physical blocks in the pool */
+  int32_t block_size;   /* tokens per block B: f16/bf16 need a multiple of 16 (<= 256); f32 any B >= 1 */
+  int32_t num_kv_heads; /* Hkv */
+  int32_t head_size;    /* D: 64 or 128 */
+  int32_t dtype;        /* pa_dtype of the cache, of q/out and of new key/value */
+} pa_cache_desc;
+
+/* Host-side status codes. */
+enum {
+  PA_OK = 0,
+  PA_ERR_NULL_POINTER = 1, /* a required pointer is NULL */
+  PA_ERR_UNSUPPORTED = 2,  /* dtype / head_size / block_size combination not built */
+  PA_ERR_INVALID_ARG = 3,  /* negative size, Hq % Hkv != 0, bad partition size, ... */
+  PA_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than pa_decode_workspace_size() */
+  PA_ERR_MISALIGNED = 5,   /* a pointer is not aligned as documented */
+  PA_ERR_CUDA = 6,         /* a CUDA runtime call or kernel launch failed */
+  PA_ERR_TOO_LARGE = 7     /* sizes exceed the index ranges the kernels use */
+};
+
+/* Device-side data error codes written to *err_flag. */
+enum {
+  PA_DEVERR_NONE = 0,
+  PA_DEVERR_BLOCK_ID = 1, /* a block_tables entry outside [0, num_blocks) */
+  PA_DEVERR_SLOT = 2,     /* a slot_mapping entry >= num_blocks * block_size */
+  PA_DEVERR_PAIR = 3,     /* a copy pair with an ID outside [0, num_blocks) */
+  PA_DEVERR_TIMEOUT = 4   /* a bounded wait on an asynchronous copy expired */
+};
+
+/*
+ * pa_decode - one decode step of paged attention for one layer.
+ *   [P3 "3.1"] signature: out/q [num_seqs, num_heads, head_size], block_tables
+ *   [num_seqs, max_blocks_per_seq], context lengths, scale.
+ *   [P1 "软件地址翻译"] token i of sequence s lives at offset i % B of block
+ *   block_tables[s][i / B].
+ *
+ *   out[s][h][:] = sum_i softmax_i(scale * q[s][h] . k_i) * v_i over the
+ *   seq_lens[s] tokens of sequence s, where k_i, v_i are the K/V rows of kv head
+ *   h / (num_q_heads / num_kv_heads) (consecutive query heads share a kv head).
+ *   Accumulation is in fp32; out is rounded to `dtype` round-to-nearest-even.
+ *   seq_lens[s] == 0 writes a zero row.  Table entries at or beyond
+ *   ceil(seq_lens[s] / B) are never read.
+ *
+ *   out          [num_seqs][num_q_heads][head_size] of dtype (written)
+ *   q            [num_seqs][num_q_heads][head_size] of dtype, 4-byte aligned
+ *   k_cache, v_cache  cache pair (layout above), 16-byte aligned
+ *   block_tables int32 [num_seqs][max_blocks_per_seq], row-major
+ *   seq_lens     int32 [num_seqs]; each <= max_blocks_per_seq * block_size (not checked
+ *                on the device beyond the table width: longer values are clamped)
+ *   scale        softmax scale (usually 1/sqrt(head_size))
+ *   partition_size  0 = library default; else tokens per partition, a multiple of
+ *                block_size (f16/bf16: also of 32 when block_size >= 32).  Sequences longer
+ *                than one partition are split across CTAs and merged with a
+ *                log-sum-exp reduction [P4 "PagedAttention Kernel在做什麼？"].
+ *   workspace    device scratch of at least pa_decode_workspace_size(...) bytes,
+ *                256-byte aligned; may be NULL when that size is 0.
+ *   err_flag     nullable device int32 (see above).
+ */
+int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+              const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
+              const pa_cache_desc* cache, float scale, int32_t partition_size, void* workspace,
+              size_t workspace_bytes, int32_t* err_flag, void* stream);
+
+/* Partition size pa_decode uses for these arguments (resolves 0 to the default);
+ * returns a value >= max_blocks_per_seq * block_size when no split happens, or a
+ * negative PA_ERR_* code for invalid arguments. */
+int32_t pa_decode_partition_size(int32_t max_blocks_per_seq, const pa_cache_desc* cache, int32_t partition_size);
+
+/* Bytes of workspace pa_decode needs: num_seqs * num_q_heads * P_max * (head_size + 2)
+ * * 4 (fp32 partial outputs, maxima and sums), P_max = ceil(max_blocks_per_seq *
+ * block_size / partition); 0 when no sequence can span two partitions.  Returns 0
+ * for invalid arguments as well (pa_decode then reports the argument error). */
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                const pa_cache_desc* cache, int32_t partition_size);
+
+/*
+ * pa_reshape_and_cache - append new tokens' K/V through slot_mapping.
+ *   [P1 "写入新 K/V"] slot = block_id * B + offset; the kernel decodes
+ *   block_id = slot / B, offset = slot % B and stores key[t][h][:] and
+ *   value[t][h][:] at (block_id, h, offset) of k_cache / v_cache.
+ *   A negative slot marks a padding token and is skipped.
+ *
+ *   key, value   [num_tokens][num_kv_heads][head_size] of dtype, dense, 16-byte aligned
+ *   slot_mapping int64 [num_tokens]
+ *   Slots must be distinct (two tokens with one slot race; either may win).
+ */
+int pa_reshape_and_cache(void* k_cache, void* v_cache, const void* key, const void* value,
+                         const int64_t* slot_mapping, int32_t num_tokens, const pa_cache_desc* cache,
+                         int32_t* err_flag, void* stream);
+
+/*
+ * pa_copy_blocks - the copy step of copy-on-write [P2 "写时复制是正确性的边界";
+ *   P3 "4.1"]: for every pair, the whole physical block dst of both caches
+ *   (all kv heads, all slots) becomes a copy of block src.
+ *
+ *   block_pairs  int32 [num_pairs][2] = (src, dst)
+ *   Precondition: no dst appears twice and no dst is also a src (the pairs are
+ *   copied concurrently).  A pair with src == dst is a no-op.
+ */
+int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pairs, int32_t num_pairs,
+                   const pa_cache_desc* cache, int32_t* err_flag, void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* pa_status_string(int status);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,189 @@
+"""paged_kv_cache_32_gb300 - paged decode attention for GB300 (sm_103a).
+
+Thin Python binding of the C ABI in ``include/pa.h`` (``libpa.so``), with the
+same entry-point names.  It only marshals arguments: torch tensors provide
+device memory and the current CUDA stream; every step of the computation runs
+in the library's CUDA kernels.  There is no CPU or PyTorch fallback: if the
+library has not been built, every entry point raises.
+
+Cache layout expected by every call: K and V are each a dense tensor
+[num_blocks, num_kv_heads, block_size, head_size] of float32, float16 or
+bfloat16 on the GPU.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+PA_F32, PA_F16, PA_BF16 = 0, 1, 2
+PA_OK = 0
+PA_DEVERR = {0: "none", 1: "block id out of range", 2: "slot out of range", 3: "copy pair id out of range",
+             4: "wait on an asynchronous copy timed out"}
+
+EXPORTED = ("pa_decode", "pa_decode_partition_size", "pa_decode_workspace_size", "pa_reshape_and_cache",
+            "pa_copy_blocks", "pa_status_string", "pa_version")
+
+
+class pa_cache_desc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_size", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libpa.so.  Raises if it has not been built (no fallback)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_build.LIB):
+            raise ImportError(f"libpa.so is not built ({_build.LIB}); run paged_kv_cache_32_gb300.build.build()")
+        L = ctypes.CDLL(_build.LIB)
+        vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        desc_p = ctypes.POINTER(pa_cache_desc)
+        L.pa_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, desc_p, ctypes.c_float, i32, vp, sz, vp, vp]
+        L.pa_decode.restype = ctypes.c_int
+        L.pa_decode_partition_size.argtypes = [i32, desc_p, i32]
+        L.pa_decode_partition_size.restype = i32
+        L.pa_decode_workspace_size.argtypes = [i32, i32, i32, desc_p, i32]
+        L.pa_decode_workspace_size.restype = sz
+        L.pa_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i32, desc_p, vp, vp]
+        L.pa_reshape_and_cache.restype = ctypes.c_int
+        L.pa_copy_blocks.argtypes = [vp, vp, vp, i32, desc_p, vp, vp]
+        L.pa_copy_blocks.restype = ctypes.c_int
+        L.pa_status_string.argtypes = [ctypes.c_int]
+        L.pa_status_string.restype = ctypes.c_char_p
+        L.pa_version.argtypes = []
+        L.pa_version.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def build(force: bool = False) -> str:
+    """Compile libpa.so in-tree for sm_103a (see build.py)."""
+    global _lib
+    path = _build.build(force=force)
+    _lib = None
+    return path
+
+
+def status_string(status: int) -> str:
+    return lib().pa_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return lib().pa_version()
+
+
+# ---------------------------------------------------------------- marshalling helpers
+def _dtype_code(t) -> int:
+    import torch
+    codes = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
+    if t.dtype not in codes:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return codes[t.dtype]
+
+
+def cache_desc(k_cache) -> pa_cache_desc:
+    """Descriptor of a [num_blocks, num_kv_heads, block_size, head_size] cache tensor."""
+    if k_cache.dim() != 4:
+        raise ValueError("cache must be [num_blocks, num_kv_heads, block_size, head_size]")
+    nb, hkv, bs, d = (int(x) for x in k_cache.shape)
+    return pa_cache_desc(nb, bs, hkv, d, _dtype_code(k_cache))
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+def _dense(t, name: str):
+    if t is not None and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    return int(getattr(stream, "cuda_stream", stream))
+
+
+def _check(status: int, where: str) -> None:
+    if status != PA_OK:
+        raise PaError(status, where)
+
+
+# ---------------------------------------------------------------- entry points
+def pa_decode_partition_size(max_blocks_per_seq: int, desc: pa_cache_desc, partition_size: int = 0) -> int:
+    r = lib().pa_decode_partition_size(int(max_blocks_per_seq), ctypes.byref(desc), int(partition_size))
+    if r < 0:
+        raise PaError(-r, "pa_decode_partition_size")
+    return r
+
+
+def pa_decode_workspace_size(num_seqs: int, num_q_heads: int, max_blocks_per_seq: int, desc: pa_cache_desc,
+                             partition_size: int = 0) -> int:
+    return int(lib().pa_decode_workspace_size(int(num_seqs), int(num_q_heads), int(max_blocks_per_seq),
+                                              ctypes.byref(desc), int(partition_size)))
+
+
+def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale: float, partition_size: int = 0,
+              workspace=None, err_flag=None, stream=None, desc: pa_cache_desc | None = None) -> None:
+    """out[s, h] = softmax(scale * q[s, h] K_s^T) V_s over seq_lens[s] paged tokens.
+
+    out, q: [num_seqs, num_q_heads, head_size] (cache dtype); block_tables: int32
+    [num_seqs, max_blocks_per_seq]; seq_lens: int32 [num_seqs].  ``workspace`` is a
+    uint8 device tensor of at least pa_decode_workspace_size(...) bytes; when None
+    and one is needed, it is allocated with torch.
+    """
+    desc = desc or cache_desc(k_cache)
+    for t, n in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (block_tables, "block_tables"), (seq_lens, "seq_lens")):
+        _dense(t, n)
+    num_seqs, num_q_heads = int(q.shape[0]), int(q.shape[1])
+    max_blocks = int(block_tables.shape[1]) if block_tables.dim() == 2 else 0
+    need = pa_decode_workspace_size(num_seqs, num_q_heads, max_blocks, desc, partition_size)
+    if workspace is None and need > 0:
+        import torch
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    status = lib().pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(seq_lens),
+                             num_seqs, num_q_heads, max_blocks, ctypes.byref(desc), float(scale),
+                             int(partition_size), _ptr(workspace), ws_bytes, _ptr(err_flag), _stream(stream))
+    _check(status, "pa_decode")
+
+
+def pa_reshape_and_cache(k_cache, v_cache, key, value, slot_mapping, err_flag=None, stream=None,
+                         desc: pa_cache_desc | None = None) -> None:
+    """Write key/value [num_tokens, num_kv_heads, head_size] into the slots of slot_mapping (int64)."""
+    desc = desc or cache_desc(k_cache)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (key, "key"), (value, "value"),
+                 (slot_mapping, "slot_mapping")):
+        _dense(t, n)
+    status = lib().pa_reshape_and_cache(_ptr(k_cache), _ptr(v_cache), _ptr(key), _ptr(value), _ptr(slot_mapping),
+                                        int(slot_mapping.shape[0]), ctypes.byref(desc), _ptr(err_flag),
+                                        _stream(stream))
+    _check(status, "pa_reshape_and_cache")
+
+
+def pa_copy_blocks(k_cache, v_cache, block_pairs, err_flag=None, stream=None, desc: pa_cache_desc | None = None) -> None:
+    """For each (src, dst) row of block_pairs (int32 [n, 2]) copy whole block src to dst in both caches."""
+    desc = desc or cache_desc(k_cache)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (block_pairs, "block_pairs")):
+        _dense(t, n)
+    status = lib().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(block_pairs), int(block_pairs.shape[0]),
+                                  ctypes.byref(desc), _ptr(err_flag), _stream(stream))
+    _check(status, "pa_copy_blocks")

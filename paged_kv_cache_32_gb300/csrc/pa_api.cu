@@ -1,0 +1,231 @@
+// pa_api.cu - the C ABI of libpa: argument validation, tensor-map set-up and
+// dispatch to the kernels.  Every host-side check runs before any CUDA call,
+// so an argument error launches nothing (and needs no GPU to be reported).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <math.h>
+#include <mutex>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+constexpr int32_t kDefaultPartition = 512;  // tokens per partition when the caller passes 0
+constexpr int64_t kInt32Max = 2147483647;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int elem_bytes(int32_t dtype) { return dtype == PA_F32 ? 4 : 2; }
+
+// Shape checks common to every call.
+int check_cache(const pa_cache_desc* c) {
+  if (c == nullptr) return PA_ERR_NULL_POINTER;
+  if (c->dtype != PA_F32 && c->dtype != PA_F16 && c->dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (c->num_blocks < 0 || c->block_size <= 0 || c->num_kv_heads <= 0 || c->head_size <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (c->head_size != 64 && c->head_size != 128) return PA_ERR_UNSUPPORTED;
+  if (c->dtype != PA_F32 && (c->block_size % 16 != 0 || c->block_size > 256)) return PA_ERR_UNSUPPORTED;
+  // row index (block * Hkv + head) * B + slot must fit the kernels' int32 arithmetic
+  if ((int64_t)c->num_blocks * c->num_kv_heads * c->block_size > kInt32Max) return PA_ERR_TOO_LARGE;
+  return PA_OK;
+}
+
+// Resolved partition size, or a negative status.
+int32_t resolve_partition(int32_t max_blocks_per_seq, const pa_cache_desc* c, int32_t requested) {
+  const int rc = check_cache(c);
+  if (rc != PA_OK) return -rc;
+  if (max_blocks_per_seq < 0 || requested < 0) return -PA_ERR_INVALID_ARG;
+  const int64_t max_len = (int64_t)max_blocks_per_seq * c->block_size;
+  if (max_len > kInt32Max) return -PA_ERR_TOO_LARGE;
+  int64_t part = requested;
+  if (part == 0) {
+    part = kDefaultPartition;
+    if (part % c->block_size != 0) part = ((part + c->block_size - 1) / c->block_size) * c->block_size;
+  } else if (part % c->block_size != 0) {
+    return -PA_ERR_INVALID_ARG;
+  }
+  if (part >= max_len) part = max_len > 0 ? max_len : c->block_size;  // no split needed
+  return (int32_t)part;
+}
+
+int32_t num_partitions(int32_t max_blocks_per_seq, int32_t block_size, int32_t part) {
+  const int64_t max_len = (int64_t)max_blocks_per_seq * block_size;
+  return max_len <= part ? 1 : (int32_t)((max_len + part - 1) / part);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D view of a cache: rows = num_blocks * Hkv * B, columns = D elements;
+// box = 64 columns (128 bytes, swizzled) x `slab` rows.
+bool encode_cache_map(CUtensorMap* map, const void* base, const pa_cache_desc* c, int slab) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)c->head_size, (cuuint64_t)c->num_blocks * c->num_kv_heads * c->block_size};
+  cuuint64_t strides[1] = {(cuuint64_t)c->head_size * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)slab};
+  cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      c->dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_version(void) { return 100; }
+
+const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case PA_ERR_UNSUPPORTED: return "unsupported dtype / head_size / block_size";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_WORKSPACE: return "workspace missing or too small";
+    case PA_ERR_MISALIGNED: return "pointer misaligned";
+    case PA_ERR_CUDA: return "CUDA error";
+    case PA_ERR_TOO_LARGE: return "sizes exceed the supported index range";
+    default: return "unknown status";
+  }
+}
+
+int32_t pa_decode_partition_size(int32_t max_blocks_per_seq, const pa_cache_desc* cache, int32_t partition_size) {
+  return resolve_partition(max_blocks_per_seq, cache, partition_size);
+}
+
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                const pa_cache_desc* cache, int32_t partition_size) {
+  const int32_t part = resolve_partition(max_blocks_per_seq, cache, partition_size);
+  if (part <= 0 || num_seqs < 0 || num_q_heads <= 0) return 0;
+  const int32_t pmax = num_partitions(max_blocks_per_seq, cache->block_size, part);
+  if (pmax <= 1) return 0;
+  const size_t rows = (size_t)num_seqs * num_q_heads * pmax;
+  const size_t o_bytes = rows * cache->head_size * sizeof(float);
+  const size_t o_padded = (o_bytes + 255) / 256 * 256;
+  return o_padded + rows * 2 * sizeof(float);
+}
+
+int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+              const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
+              const pa_cache_desc* cache, float scale, int32_t partition_size, void* workspace,
+              size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  int rc = check_cache(cache);
+  if (rc != PA_OK) return rc;
+  if (num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq < 0) return PA_ERR_INVALID_ARG;
+  if (num_q_heads % cache->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+  if (!(scale == scale) || isinf(scale)) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (out == nullptr || q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr)
+    return PA_ERR_NULL_POINTER;
+  if (block_tables == nullptr && max_blocks_per_seq > 0) return PA_ERR_NULL_POINTER;
+  const int32_t part = resolve_partition(max_blocks_per_seq, cache, partition_size);
+  if (part < 0) return -part;
+  const int32_t pmax = num_partitions(max_blocks_per_seq, cache->block_size, part);
+  const size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, max_blocks_per_seq, cache, partition_size);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PA_ERR_WORKSPACE;
+  if (need > 0 && !aligned(workspace, 256)) return PA_ERR_MISALIGNED;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 4) || !aligned(out, 4)) return PA_ERR_MISALIGNED;
+  const int G = num_q_heads / cache->num_kv_heads;
+  const int head_groups = (G + 7) / 8;
+  const long long grid = (long long)num_seqs * cache->num_kv_heads * head_groups * pmax;
+  if (grid > kInt32Max || (long long)num_seqs * num_q_heads > kInt32Max) return PA_ERR_TOO_LARGE;
+
+  pa::DecodeParams p;
+  p.out = out;
+  p.q = q;
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.ws_o = nullptr;
+  p.ws_ml = nullptr;
+  if (need > 0) {
+    const size_t rows = (size_t)num_seqs * num_q_heads * pmax;
+    const size_t o_padded = (rows * cache->head_size * sizeof(float) + 255) / 256 * 256;
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_padded);
+  }
+  p.err_flag = err_flag;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = cache->num_kv_heads;
+  p.head_groups = head_groups;
+  p.max_blocks = max_blocks_per_seq;
+  p.block_size = cache->block_size;
+  p.num_blocks = cache->num_blocks;
+  p.partition_size = part;
+  p.pmax = pmax;
+  p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (cache->dtype == PA_F32) {
+    e = pa::launch_decode_f32(cache->head_size, static_cast<const float*>(k_cache),
+                              static_cast<const float*>(v_cache), p, st);
+  } else {
+    CUtensorMap tk, tv;
+    const int slab = pa::tc_slab_tokens(cache->block_size);
+    if (!encode_cache_map(&tk, k_cache, cache, slab) || !encode_cache_map(&tv, v_cache, cache, slab))
+      return PA_ERR_CUDA;
+    e = pa::launch_decode_tc(cache->dtype, cache->head_size, cache->block_size, tk, tv, p, st);
+  }
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (pmax > 1) {
+    e = pa::launch_merge(cache->dtype, cache->head_size, p, st);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+int pa_reshape_and_cache(void* k_cache, void* v_cache, const void* key, const void* value,
+                         const int64_t* slot_mapping, int32_t num_tokens, const pa_cache_desc* cache,
+                         int32_t* err_flag, void* stream) {
+  int rc = check_cache(cache);
+  if (rc != PA_OK) return rc;
+  if (num_tokens < 0) return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (k_cache == nullptr || v_cache == nullptr || key == nullptr || value == nullptr || slot_mapping == nullptr)
+    return PA_ERR_NULL_POINTER;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(key, 16) || !aligned(value, 16) ||
+      !aligned(slot_mapping, 8))
+    return PA_ERR_MISALIGNED;
+  const int32_t row_bytes = cache->head_size * elem_bytes(cache->dtype);
+  cudaError_t e = pa::launch_reshape_and_cache(k_cache, v_cache, key, value, slot_mapping, num_tokens,
+                                               cache->num_blocks, cache->block_size, cache->num_kv_heads, row_bytes,
+                                               err_flag, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pairs, int32_t num_pairs,
+                   const pa_cache_desc* cache, int32_t* err_flag, void* stream) {
+  int rc = check_cache(cache);
+  if (rc != PA_OK) return rc;
+  if (num_pairs < 0) return PA_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PA_OK;
+  if (k_cache == nullptr || v_cache == nullptr || block_pairs == nullptr) return PA_ERR_NULL_POINTER;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(block_pairs, 4)) return PA_ERR_MISALIGNED;
+  const int64_t block_bytes =
+      (int64_t)cache->num_kv_heads * cache->block_size * cache->head_size * elem_bytes(cache->dtype);
+  const int64_t pieces = (block_bytes + 16383) / 16384;
+  if (pieces * num_pairs > kInt32Max) return PA_ERR_TOO_LARGE;
+  cudaError_t e = pa::launch_copy_blocks(k_cache, v_cache, block_pairs, num_pairs, cache->num_blocks, block_bytes,
+                                         err_flag, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // extern "C"

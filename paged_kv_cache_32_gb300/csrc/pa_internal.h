@@ -1,0 +1,46 @@
+// pa_internal.h - launch parameters and kernel launchers shared by the
+// translation units of libpa (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+// Parameters of one decode launch (and of its partition merge).
+struct DecodeParams {
+  void* out;                  // [N][Hq][D] of the cache dtype
+  const void* q;              // [N][Hq][D]
+  const int32_t* block_tables;  // [N][M]
+  const int32_t* seq_lens;    // [N]
+  float* ws_o;                // [N][Hq][pmax][D] unnormalised partial outputs
+  float* ws_ml;               // [N][Hq][pmax][2] (running max in log2 units, sum)
+  int32_t* err_flag;          // nullable
+  int32_t num_seqs, num_q_heads, num_kv_heads;
+  int32_t head_groups;        // ceil(G / 8): CTAs per kv head, 8 query heads each
+  int32_t max_blocks;         // M
+  int32_t block_size;         // B
+  int32_t num_blocks;
+  int32_t partition_size;     // tokens per partition (multiple of B)
+  int32_t pmax;               // partitions per sequence in the grid
+  float scale_log2;           // scale * log2(e)
+};
+
+// Kernel launchers (return the cudaGetLastError of the launch).
+cudaError_t launch_decode_tc(int dtype, int head_size, int block_size, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_f32(int head_size, const float* k_cache, const float* v_cache, const DecodeParams& p,
+                              cudaStream_t stream);
+cudaError_t launch_merge(int dtype, int head_size, const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_reshape_and_cache(void* k_cache, void* v_cache, const void* key, const void* value,
+                                     const int64_t* slot_mapping, int32_t num_tokens, int32_t num_blocks,
+                                     int32_t block_size, int32_t num_kv_heads, int32_t row_bytes,
+                                     int32_t* err_flag, cudaStream_t stream);
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int32_t num_pairs,
+                               int32_t num_blocks, int64_t block_bytes, int32_t* err_flag, cudaStream_t stream);
+
+// Slab (TMA tile height in tokens) used by the tensor-core decode for a block size.
+inline int tc_slab_tokens(int block_size) { return block_size % 32 == 0 ? 32 : 16; }
+
+}  // namespace pa

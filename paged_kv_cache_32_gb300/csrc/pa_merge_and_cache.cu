@@ -1,0 +1,182 @@
+// pa_merge_and_cache.cu - the partition merge of long-context decode, the
+// slot-mapping append and the copy-on-write block copy.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "pa.h"
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+// ---------------------------------------------------------------------------
+// Partition merge ("PagedAttention是什麼？", section "PagedAttention Kernel在做
+// 什麼？": long contexts use a partition reduction).  Partition p of a
+// sequence left m_p (max score, log2 units), l_p = sum 2^(s_i - m_p) and the
+// unnormalised o_p = sum 2^(s_i - m_p) v_i.  With m* = max_p m_p and
+// w_p = 2^(m_p - m*):  out = sum_p w_p o_p / sum_p w_p l_p.
+// One CTA of D threads per (sequence, query head); thread d owns output dim d.
+// ---------------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(D) merge_kernel(const DecodeParams p) {
+  constexpr int CHUNK = 256;
+  __shared__ float s_w[CHUNK];
+  __shared__ float s_lw[CHUNK];
+  __shared__ float s_red[D / 32];
+
+  const int sh = blockIdx.x;
+  const int s = sh / p.num_q_heads;
+  int L = p.seq_lens[s];
+  L = max(0, min(L, p.max_blocks * p.block_size));
+  const int nparts = (L + p.partition_size - 1) / p.partition_size;
+  if (nparts <= 1) return;  // written directly by the decode kernel
+  const float* ml = p.ws_ml + (size_t)sh * p.pmax * 2;
+  const float* os = p.ws_o + (size_t)sh * p.pmax * D;
+  const int tid = threadIdx.x;
+
+  float mx = -INFINITY;
+  for (int i = tid; i < nparts; i += D) mx = fmaxf(mx, ml[2 * i]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if ((tid & 31) == 0) s_red[tid >> 5] = mx;
+  __syncthreads();
+  float mstar = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < D / 32; ++w) mstar = fmaxf(mstar, s_red[w]);
+
+  float acc = 0.f, lsum = 0.f;
+  for (int base = 0; base < nparts; base += CHUNK) {
+    const int n = min(CHUNK, nparts - base);
+    __syncthreads();
+    for (int i = tid; i < n; i += D) {
+      const float mi = ml[2 * (base + i)];
+      const float w = (mi == -INFINITY || mstar == -INFINITY) ? 0.f : fast_exp2(mi - mstar);
+      s_w[i] = w;
+      s_lw[i] = w * ml[2 * (base + i) + 1];
+    }
+    __syncthreads();
+    for (int i = 0; i < n; ++i) {
+      acc = fmaf(s_w[i], os[(size_t)(base + i) * D + tid], acc);
+      lsum += s_lw[i];
+    }
+  }
+  T* out = reinterpret_cast<T*>(p.out);
+  out[(size_t)sh * D + tid] = from_float<T>(lsum > 0.f ? acc / lsum : 0.f);
+}
+
+cudaError_t launch_merge(int dtype, int head_size, const DecodeParams& p, cudaStream_t stream) {
+  const long long grid = (long long)p.num_seqs * p.num_q_heads;
+  if (grid == 0) return cudaSuccess;
+#define PA_MERGE(T, DD) merge_kernel<T, DD><<<(unsigned)grid, DD, 0, stream>>>(p)
+  if (dtype == PA_F32 && head_size == 64) PA_MERGE(float, 64);
+  else if (dtype == PA_F32 && head_size == 128) PA_MERGE(float, 128);
+  else if (dtype == PA_F16 && head_size == 64) PA_MERGE(__half, 64);
+  else if (dtype == PA_F16 && head_size == 128) PA_MERGE(__half, 128);
+  else if (dtype == PA_BF16 && head_size == 64) PA_MERGE(__nv_bfloat16, 64);
+  else if (dtype == PA_BF16 && head_size == 128) PA_MERGE(__nv_bfloat16, 128);
+  else return cudaErrorInvalidValue;
+#undef PA_MERGE
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Slot-mapping append ("PagedAttention 详解：缓存的存储结构", section "写入新
+// K/V"): block = slot / B, offset = slot % B; the token's [Hkv][D] key and
+// value rows go to (block, h, offset) of each cache.  One CTA per token, each
+// thread moving 16-byte vectors; negative slots are padding and skipped.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128)
+    reshape_and_cache_kernel(uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
+                             const uint8_t* __restrict__ key, const uint8_t* __restrict__ value,
+                             const int64_t* __restrict__ slot_mapping, int32_t num_blocks, int32_t block_size,
+                             int32_t num_kv_heads, int32_t row_bytes, int32_t* err_flag) {
+  const int t = blockIdx.x;
+  const int64_t slot = slot_mapping[t];
+  if (slot < 0) return;
+  const int64_t block = slot / block_size;
+  const int64_t off = slot % block_size;
+  if (block >= num_blocks) {
+    if (threadIdx.x == 0) report_error(err_flag, PA_DEVERR_SLOT);
+    return;
+  }
+  const int vec_per_row = row_bytes / 16;
+  const int total = num_kv_heads * vec_per_row;
+  const size_t src_base = (size_t)t * num_kv_heads * row_bytes;
+  for (int i = threadIdx.x; i < total; i += blockDim.x) {
+    const int h = i / vec_per_row;
+    const int c = i % vec_per_row;
+    const size_t src = src_base + (size_t)h * row_bytes + (size_t)c * 16;
+    const size_t dst = (((size_t)block * num_kv_heads + h) * block_size + off) * row_bytes + (size_t)c * 16;
+    const uint4 kx = __ldg(reinterpret_cast<const uint4*>(key + src));
+    const uint4 vx = __ldg(reinterpret_cast<const uint4*>(value + src));
+    *reinterpret_cast<uint4*>(k_cache + dst) = kx;
+    *reinterpret_cast<uint4*>(v_cache + dst) = vx;
+  }
+}
+
+cudaError_t launch_reshape_and_cache(void* k_cache, void* v_cache, const void* key, const void* value,
+                                     const int64_t* slot_mapping, int32_t num_tokens, int32_t num_blocks,
+                                     int32_t block_size, int32_t num_kv_heads, int32_t row_bytes,
+                                     int32_t* err_flag, cudaStream_t stream) {
+  if (num_tokens == 0) return cudaSuccess;
+  reshape_and_cache_kernel<<<num_tokens, 128, 0, stream>>>(
+      static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), static_cast<const uint8_t*>(key),
+      static_cast<const uint8_t*>(value), slot_mapping, num_blocks, block_size, num_kv_heads, row_bytes, err_flag);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Block copy for copy-on-write ("PagedAttention 笔记", section "写时复制是
+// 正确性的边界"; "vLLM 核心工程深度剖析", section "4.1 Beam Search 中的 CoW"):
+// block dst of a cache becomes a copy of block src.  Grid: x = pair * pieces
+// + piece, y = cache (K, V); each CTA moves one 16 KB piece with 16-byte
+// vectors, four loads in flight per thread.
+// ---------------------------------------------------------------------------
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;
+constexpr int kCopyPiece = kCopyThreads * kCopyUnroll * 16;
+
+__global__ void __launch_bounds__(kCopyThreads)
+    copy_blocks_kernel(uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
+                       const int32_t* __restrict__ pairs, int32_t num_blocks, int64_t block_bytes,
+                       int32_t pieces, int32_t* err_flag) {
+  const int pair = blockIdx.x / pieces;
+  const int piece = blockIdx.x % pieces;
+  const int32_t src = pairs[2 * pair];
+  const int32_t dst = pairs[2 * pair + 1];
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (threadIdx.x == 0 && piece == 0 && blockIdx.y == 0) report_error(err_flag, PA_DEVERR_PAIR);
+    return;
+  }
+  if (src == dst) return;
+  uint8_t* cache = blockIdx.y == 0 ? k_cache : v_cache;
+  const uint8_t* from = cache + (size_t)src * block_bytes;
+  uint8_t* to = cache + (size_t)dst * block_bytes;
+  const int64_t begin = (int64_t)piece * kCopyPiece;
+  uint4 r[kCopyUnroll];
+#pragma unroll
+  for (int u = 0; u < kCopyUnroll; ++u) {
+    const int64_t off = begin + ((int64_t)u * kCopyThreads + threadIdx.x) * 16;
+    if (off < block_bytes) r[u] = __ldg(reinterpret_cast<const uint4*>(from + off));
+  }
+#pragma unroll
+  for (int u = 0; u < kCopyUnroll; ++u) {
+    const int64_t off = begin + ((int64_t)u * kCopyThreads + threadIdx.x) * 16;
+    if (off < block_bytes) *reinterpret_cast<uint4*>(to + off) = r[u];
+  }
+}
+
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int32_t num_pairs,
+                               int32_t num_blocks, int64_t block_bytes, int32_t* err_flag, cudaStream_t stream) {
+  if (num_pairs == 0) return cudaSuccess;
+  const int32_t pieces = (int32_t)((block_bytes + kCopyPiece - 1) / kCopyPiece);
+  dim3 grid((unsigned)((int64_t)pieces * num_pairs), 2);
+  copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(static_cast<uint8_t*>(k_cache),
+                                                        static_cast<uint8_t*>(v_cache), pairs, num_blocks,
+                                                        block_bytes, pieces, err_flag);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,97 @@
+"""Test-side glue: run a workload step through the CUDA library and through the oracle.
+
+The two sides receive the same host arrays from ``workloads``; nothing the GPU
+computes is ever fed to the oracle.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle as O
+import workloads as W
+
+TOL = {"f32": 1e-5, "f16": 3e-3, "bf16": 3e-3}
+
+
+def to_torch(a: np.ndarray, dtype: str, device="cuda"):
+    import torch
+    if dtype == "bf16":
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(a))
+    return t.to(device)
+
+
+def to_numpy_storage(t, dtype: str) -> np.ndarray:
+    import torch
+    t = t.detach().cpu().contiguous()
+    if dtype == "bf16":
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def out_f64(t) -> np.ndarray:
+    return t.detach().float().cpu().double().numpy()
+
+
+class GpuStep:
+    """Device copies of a workload's inputs plus the calls of one decode step."""
+
+    def __init__(self, w: W.Workload, device="cuda"):
+        import torch
+        import paged_kv_cache_32_gb300 as pa
+        self.w, self.pa = w, pa
+        self.k = to_torch(w.k_cache, w.dtype, device)
+        self.v = to_torch(w.v_cache, w.dtype, device)
+        self.q = to_torch(w.q, w.dtype, device)
+        self.tables = torch.from_numpy(w.block_tables).to(device)
+        self.lens = torch.from_numpy(w.seq_lens).to(device)
+        self.out = torch.empty_like(self.q)
+        self.pairs = torch.from_numpy(w.copy_pairs).to(device) if w.copy_pairs is not None else None
+        self.slots = torch.from_numpy(w.slot_mapping).to(device) if w.slot_mapping is not None else None
+        self.nk = to_torch(w.new_key, w.dtype, device) if w.new_key is not None else None
+        self.nv = to_torch(w.new_value, w.dtype, device) if w.new_value is not None else None
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.desc = pa.cache_desc(self.k)
+        need = pa.pa_decode_workspace_size(w.num_seqs, w.num_q_heads, w.max_blocks_per_seq, self.desc,
+                                           w.partition_size)
+        self.ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+
+    def writes(self, stream=None):
+        if self.pairs is not None and len(self.pairs):
+            self.pa.pa_copy_blocks(self.k, self.v, self.pairs, err_flag=self.err, stream=stream, desc=self.desc)
+        if self.slots is not None and len(self.slots):
+            self.pa.pa_reshape_and_cache(self.k, self.v, self.nk, self.nv, self.slots, err_flag=self.err,
+                                         stream=stream, desc=self.desc)
+
+    def decode(self, stream=None, partition_size=None):
+        part = self.w.partition_size if partition_size is None else partition_size
+        ws = self.ws
+        if partition_size is not None:
+            import torch
+            need = self.pa.pa_decode_workspace_size(self.w.num_seqs, self.w.num_q_heads, self.w.max_blocks_per_seq,
+                                                    self.desc, part)
+            if need > ws.numel():
+                ws = torch.empty(need, dtype=torch.uint8, device=self.q.device)
+        self.pa.pa_decode(self.out, self.q, self.k, self.v, self.tables, self.lens, self.w.scale,
+                          partition_size=part, workspace=ws, err_flag=self.err, stream=stream, desc=self.desc)
+
+    def step(self, stream=None):
+        self.writes(stream)
+        self.decode(stream)
+
+
+def oracle_step(w: W.Workload, threads: int = 0):
+    """Host pools after the step's writes, and the fp64 attention output."""
+    k, v = w.k_cache.copy(), w.v_cache.copy()
+    kw = dict(dtype=w.dtype, num_kv_heads=w.num_kv_heads, block_size=w.block_size)
+    W.apply_writes_host(
+        w, k, v,
+        lambda kk, vv, pairs: O.copy_blocks(kk, vv, pairs, head_size=w.head_size, **kw),
+        lambda kk, vv, nk, nv, slots: O.reshape_and_cache(kk, vv, nk, nv, slots, **kw))
+    out = O.paged_attention(w.q, k, v, w.block_tables, w.seq_lens, scale=w.scale, threads=threads, **kw)
+    return k, v, out
+
+
+def max_abs_err(gpu_out, ref: np.ndarray) -> float:
+    return float(np.max(np.abs(out_f64(gpu_out) - ref))) if ref.size else 0.0

@@ -1,0 +1,114 @@
+"""The C ABI without a GPU: the library builds, loads, exports every declared
+symbol, and rejects invalid arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_32_gb300 as pa
+
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pa.build()
+    return pa.lib()
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names.update(re.findall(r"\b(pa_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert {"pa_decode", "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_workspace_size"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(pa.EXPORTED) <= set(names)
+
+
+def test_version_and_status_strings(lib):
+    assert pa.version() >= 100
+    for code in range(8):
+        assert pa.status_string(code)
+    assert pa.status_string(999) == "unknown status"
+
+
+def desc(nb=16, bs=16, hkv=2, d=128, dtype=pa.PA_F16):
+    return pa.pa_cache_desc(nb, bs, hkv, d, dtype)
+
+
+FAKE = 0x10000  # never dereferenced: every call below is rejected before any CUDA call
+
+
+def call_decode(lib, d, out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, sl=FAKE, n=2, hq=4, m=4, scale=0.1, part=0,
+                ws=None, ws_bytes=0):
+    return lib.pa_decode(out, q, k, v, bt, sl, n, hq, m, ctypes.byref(d), scale, part, ws, ws_bytes, None, None)
+
+
+def test_decode_argument_errors(lib):
+    assert call_decode(lib, desc(d=96)) == 2                         # head_size unsupported
+    assert call_decode(lib, desc(dtype=7)) == 2                      # dtype unsupported
+    assert call_decode(lib, desc(bs=8)) == 2                         # f16 needs B % 16 == 0
+    assert call_decode(lib, desc(), hq=3) == 3                       # Hq % Hkv != 0
+    assert call_decode(lib, desc(), n=-1) == 3
+    assert call_decode(lib, desc(), scale=float("nan")) == 3
+    assert call_decode(lib, desc(), out=None) == 1
+    assert call_decode(lib, desc(), bt=None) == 1
+    assert call_decode(lib, desc(), part=24) == 3                    # not a multiple of B
+    assert call_decode(lib, desc(), m=100) == 4                      # split needs a workspace
+    assert call_decode(lib, desc(), m=100, ws=FAKE, ws_bytes=16) == 4
+    assert call_decode(lib, desc(), k=FAKE + 2) == 5                 # TMA needs 16-byte aligned caches
+    assert call_decode(lib, desc(nb=1 << 30, hkv=8)) == 7            # row index overflows int32
+    assert call_decode(lib, desc(), n=0, out=None) == 0              # nothing to do, nothing launched
+
+
+def test_partition_and_workspace_sizes(lib):
+    d = desc(nb=16384, bs=16, hkv=8, d=128, dtype=pa.PA_BF16)
+    assert pa.pa_decode_partition_size(2048, d, 0) == 512
+    assert pa.pa_decode_partition_size(2048, d, 1024) == 1024
+    assert pa.pa_decode_partition_size(16, d, 0) == 256              # whole context fits: no split
+    with pytest.raises(pa.PaError):
+        pa.pa_decode_partition_size(2048, d, 100)
+    # 8 seqs x 32 heads x 64 partitions x (128 + 2) floats
+    rows = 8 * 32 * 64
+    assert pa.pa_decode_workspace_size(8, 32, 2048, d, 512) == rows * 128 * 4 + rows * 2 * 4
+    assert pa.pa_decode_workspace_size(8, 32, 16, d, 0) == 0
+
+
+def test_write_argument_errors(lib):
+    d = desc()
+    assert lib.pa_reshape_and_cache(FAKE, FAKE, FAKE, FAKE, FAKE, -1, ctypes.byref(d), None, None) == 3
+    assert lib.pa_reshape_and_cache(FAKE, FAKE, FAKE, FAKE, FAKE, 0, ctypes.byref(d), None, None) == 0
+    assert lib.pa_reshape_and_cache(FAKE, FAKE, None, FAKE, FAKE, 4, ctypes.byref(d), None, None) == 1
+    assert lib.pa_reshape_and_cache(FAKE, FAKE, FAKE + 8, FAKE, FAKE, 4, ctypes.byref(d), None, None) == 5
+    assert lib.pa_copy_blocks(FAKE, FAKE, None, 3, ctypes.byref(d), None, None) == 1
+    assert lib.pa_copy_blocks(FAKE, FAKE, FAKE, 0, ctypes.byref(d), None, None) == 0
+    assert lib.pa_copy_blocks(FAKE, FAKE, FAKE, -2, ctypes.byref(d), None, None) == 3
+    assert lib.pa_copy_blocks(FAKE, FAKE, FAKE, 3, None, None, None) == 1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch):
+    monkeypatch.setattr(pa._build, "LIB", "/nonexistent/libpa.so")
+    monkeypatch.setattr(pa, "_lib", None)
+    with pytest.raises(ImportError):
+        pa.lib()
+
+
+def test_product_package_never_touches_the_oracle():
+    pkg = os.path.join(ROOT, "paged_kv_cache_32_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "oracle" not in text.lower(), fn
+                assert "pa_oracle" not in text and "pao_" not in text, fn

@@ -1,0 +1,162 @@
+"""CUDA library vs the CPU fp64 oracle, element by element (needs a GB300).
+
+Attention: max abs error <= 1e-5 (fp32) / 3e-3 (fp16, bf16) against fp64.
+Slot writes and block copies: bit-exact over the whole pool (untouched bytes
+included).  Unused slots and unreferenced blocks hold NaN, so any read past a
+sequence's end or through a wrong block ID poisons the output.
+"""
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+from harness import TOL, GpuStep, max_abs_err, oracle_step, out_f64, to_numpy_storage
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import paged_kv_cache_32_gb300 as pa
+    pa.build()
+    return pa
+
+
+def check_step(w: W.Workload, threads: int = 0, partition_size=None):
+    import torch
+    g = GpuStep(w)
+    g.writes()
+    g.decode(partition_size=partition_size)
+    torch.cuda.synchronize()
+    k_ref, v_ref, ref = oracle_step(w, threads)
+    assert int(g.err.item()) == 0
+    assert np.array_equal(to_numpy_storage(g.k, w.dtype).view(np.uint8), k_ref.view(np.uint8))
+    assert np.array_equal(to_numpy_storage(g.v, w.dtype).view(np.uint8), v_ref.view(np.uint8))
+    got = out_f64(g.out)
+    assert not np.isnan(got).any()
+    err = float(np.max(np.abs(got - ref))) if ref.size else 0.0
+    assert err <= TOL[w.dtype], f"{w.name}: max abs err {err}"
+    return err, g
+
+
+# ---------------------------------------------------------------- the five workloads at full size
+def test_tiny_f32():
+    check_step(W.tiny_f32())
+
+
+def test_mha_f16_with_append():
+    err, _ = check_step(W.mha_f16())
+    print("mha_f16 max abs err", err)
+
+
+def test_gqa_bf16():
+    w = W.gqa_bf16()
+    err, g = check_step(w)
+    # the bf16 tolerance needs |out| well below 1 (half an ulp at [1, 2) is 3.9e-3)
+    assert float(np.max(np.abs(out_f64(g.out)))) < 0.75
+
+
+def test_shared_prefix_f16_cow_and_append():
+    check_step(W.shared_prefix_f16())
+
+
+@pytest.mark.parametrize("block_size", [16, 32, 64])
+def test_long_bf16_split(block_size):
+    check_step(W.long_bf16(block_size))
+
+
+# ---------------------------------------------------------------- small cases: tiles, ragged tails, edge cases
+SMALL = [
+    # dtype, Hq, Hkv, D, B, lens
+    ("f16", 8, 8, 128, 16, [1, 15, 16, 17, 31, 32, 33, 100]),
+    ("bf16", 16, 2, 128, 32, [1, 31, 32, 33, 64, 65, 300]),
+    ("bf16", 32, 8, 128, 64, [63, 64, 65, 127, 129, 700]),
+    ("f16", 16, 1, 64, 16, [5, 16, 250, 513]),        # G = 16: two head groups per kv head
+    ("bf16", 12, 4, 64, 32, [0, 1, 2, 40, 1000]),     # G = 3, an empty sequence
+    ("f16", 4, 4, 64, 48, [47, 48, 49, 200]),          # B = 48: 16-token slabs, 3 per block
+    ("f32", 8, 2, 128, 16, [1, 16, 17, 90, 600]),
+    ("f32", 4, 4, 64, 8, [1, 7, 8, 9, 64]),           # fp32 takes any block size
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"{c[0]}-Hq{c[1]}-Hkv{c[2]}-D{c[3]}-B{c[4]}")
+@pytest.mark.parametrize("partition", [0, "one_block", "big"])
+def test_small_cases(case, partition):
+    dtype, Hq, Hkv, D, B, lens = case
+    w = W.build_decode("small", seed=zlib.crc32(repr(case).encode()) % 10000, dtype=dtype, seq_lens=lens, num_q_heads=Hq, num_kv_heads=Hkv,
+                       head_size=D, block_size=B, pool_factor=1.3, append_last=True)
+    part = {0: 0, "one_block": B, "big": 8 * max(B, 32)}[partition]
+    check_step(w, partition_size=part)
+
+
+def test_permuted_block_ids_bit_identical():
+    """Relabelling physical blocks leaves the GPU output bit-identical."""
+    import torch
+    w = W.gqa_bf16(num_seqs=16, hi=1500)
+    g1 = GpuStep(w)
+    g1.decode()
+    perm = np.random.default_rng(3).permutation(w.num_blocks)
+    k = np.empty_like(w.k_cache); k[perm] = w.k_cache
+    v = np.empty_like(w.v_cache); v[perm] = w.v_cache
+    w2 = W.Workload(**{**w.__dict__, "k_cache": k, "v_cache": v,
+                       "block_tables": perm[w.block_tables].astype(np.int32)})
+    g2 = GpuStep(w2)
+    g2.decode()
+    torch.cuda.synchronize()
+    assert torch.equal(g1.out, g2.out)
+
+
+def test_bad_block_id_sets_flag_and_stays_in_bounds():
+    import torch
+    w = W.build_decode("bad", seed=9, dtype="f16", seq_lens=[40, 40], num_q_heads=4, num_kv_heads=4,
+                       head_size=128, block_size=16, pool_factor=1.5)
+    w.block_tables[1, 1] = w.num_blocks + 1000
+    g = GpuStep(w)
+    g.decode()
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 1
+    # sequence 0 is untouched by the bad entry
+    ref = O.paged_attention(w.q[:1], w.k_cache, w.v_cache, w.block_tables[:1], w.seq_lens[:1], dtype="f16",
+                            num_kv_heads=4, block_size=16, scale=w.scale)
+    assert max_abs_err(g.out[:1], ref) <= TOL["f16"]
+
+
+def test_bad_slot_and_pair_set_flags():
+    import torch
+    import paged_kv_cache_32_gb300 as pa
+    w = W.build_decode("badw", seed=10, dtype="bf16", seq_lens=[20], num_q_heads=2, num_kv_heads=2, head_size=64,
+                       block_size=16, pool_factor=2.0)
+    g = GpuStep(w)
+    before_k = g.k.clone()
+    slots = torch.tensor([w.num_blocks * 16 + 3], dtype=torch.int64, device="cuda")
+    key = torch.ones(1, 2, 64, dtype=torch.bfloat16, device="cuda")
+    pa.pa_reshape_and_cache(g.k, g.v, key, key.clone(), slots, err_flag=g.err)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 2 and torch.equal(before_k, g.k)
+    g.err.zero_()
+    pairs = torch.tensor([[0, w.num_blocks]], dtype=torch.int32, device="cuda")
+    pa.pa_copy_blocks(g.k, g.v, pairs, err_flag=g.err)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 3 and torch.equal(before_k, g.k)
+
+
+def test_cow_leaves_other_branches_untouched_on_gpu():
+    """After the copies and appends of the shared-prefix step, every block that was
+    neither a copy destination nor written by an append is byte-identical."""
+    import torch
+    w = W.shared_prefix_f16(num_prompts=4, branches=8, prefix_len=1020, max_suffix=40, num_blocks=1024, seed=11)
+    g = GpuStep(w)
+    g.writes()
+    torch.cuda.synchronize()
+    k = to_numpy_storage(g.k, "f16").view(np.uint16)
+    dsts = set(int(x) for x in w.copy_pairs[:, 1])
+    written = set(int(s) // 16 for s in w.slot_mapping)
+    keep = [b for b in range(w.num_blocks) if b not in dsts | written]
+    assert np.array_equal(k[keep], w.k_cache.view(np.uint16)[keep])
+    # 1020 = 63 * 16 + 12: the copied block is partial and the first suffix tokens land in the copy
+    assert dsts & written

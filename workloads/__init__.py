@@ -161,8 +161,8 @@ class Workload:
     num_blocks: int
     scale: float
     q: np.ndarray                      # [N, Hq, D]
-    k_cache: np.ndarray                # [num_blocks, Hkv, B, D], state before the step's writes
-    v_cache: np.ndarray
+    k_cache: np.ndarray | None         # [num_blocks, Hkv, B, D], state before the step's writes
+    v_cache: np.ndarray | None         # (None when only the metadata was built)
     block_tables: np.ndarray           # int32 [N, M]
     seq_lens: np.ndarray               # int32 [N]
     copy_pairs: np.ndarray | None = None     # int32 [n, 2] (src, dst)
@@ -226,9 +226,11 @@ def _fill_tokens(k_cache, v_cache, rng, alloc: BlockAllocator, seq: int, t0: int
 def build_decode(name: str, *, seed: int, dtype: str, seq_lens, num_q_heads: int, num_kv_heads: int,
                  head_size: int, block_size: int, num_blocks: int | None = None, pool_factor: float = 1.2,
                  append_last: bool = False, fixed_tables: dict | None = None, shuffle: bool = True,
-                 table_width: int | None = None, partition_size: int = 0) -> Workload:
+                 table_width: int | None = None, partition_size: int = 0, materialize: bool = True) -> Workload:
     """Independent sequences.  With ``append_last`` the last token of every sequence
-    is written by the step's reshape_and_cache (its slot starts out as NaN)."""
+    is written by the step's reshape_and_cache (its slot starts out as NaN).
+    ``materialize=False`` skips the host caches (k_cache = v_cache = None): the
+    metadata, q and the new tokens are still built; see ``device_caches``."""
     rng = np.random.default_rng(seed)
     seq_lens = [int(x) for x in seq_lens]
     need = sum(-(-L // block_size) for L in seq_lens)
@@ -239,9 +241,11 @@ def build_decode(name: str, *, seed: int, dtype: str, seq_lens, num_q_heads: int
     for s, L in enumerate(seq_lens):
         alloc.allocate(s, L - 1 if (append_last and L > 0) else L, fixed=fixed_tables.get(s))
     shape = (num_blocks, num_kv_heads, block_size, head_size)
-    k_cache, v_cache = nan_array(shape, dtype), nan_array(shape, dtype)
-    for s in range(len(seq_lens)):
-        _fill_tokens(k_cache, v_cache, rng, alloc, s, 0, alloc.lens[s], dtype)
+    k_cache = v_cache = None
+    if materialize:
+        k_cache, v_cache = nan_array(shape, dtype), nan_array(shape, dtype)
+        for s in range(len(seq_lens)):
+            _fill_tokens(k_cache, v_cache, rng, alloc, s, 0, alloc.lens[s], dtype)
     slot_mapping = new_key = new_value = None
     if append_last:
         slots = []
@@ -278,14 +282,14 @@ def tiny_f32() -> Workload:
 
 
 def mha_f16(num_seqs: int = 64, max_len: int = 2048, min_len: int = 128, num_heads: int = 32,
-            num_blocks: int = 8192) -> Workload:
+            num_blocks: int = 8192, materialize: bool = True) -> Workload:
     """MHA fp16: lens uniform in [128, 2048], 32 heads, D = 128, B = 16, pool of 8192
     shuffled blocks; the step appends one token per sequence, then attends over it."""
     rng = np.random.default_rng(1001)
     lens = rng.integers(min_len, max_len, size=num_seqs, endpoint=True)
     w = build_decode("mha_f16", seed=1001, dtype="f16", seq_lens=lens, num_q_heads=num_heads,
                      num_kv_heads=num_heads, head_size=128, block_size=16, num_blocks=num_blocks,
-                     append_last=True)
+                     append_last=True, materialize=materialize)
     return w
 
 
@@ -294,18 +298,18 @@ def gqa_lens(num_seqs: int, rng: np.random.Generator, median: float = 1200.0, si
     return np.clip(np.rint(rng.lognormal(math.log(median), sigma, size=num_seqs)), lo, hi).astype(np.int64)
 
 
-def gqa_bf16(num_seqs: int = 128, hi: int = 4096) -> Workload:
+def gqa_bf16(num_seqs: int = 128, hi: int = 4096, materialize: bool = True) -> Workload:
     """GQA bf16: 128 seqs, 64 q heads / 8 kv heads, D = 128, B = 32, lens
     lognormal(ln 1200, 0.6) clamped to [64, 4096]; pool = 1.2x the blocks needed."""
     rng = np.random.default_rng(1002)
     lens = gqa_lens(num_seqs, rng, hi=hi)
     return build_decode("gqa_bf16", seed=1002, dtype="bf16", seq_lens=lens, num_q_heads=64, num_kv_heads=8,
-                        head_size=128, block_size=32, pool_factor=1.2)
+                        head_size=128, block_size=32, pool_factor=1.2, materialize=materialize)
 
 
 def shared_prefix_f16(num_prompts: int = 16, branches: int = 8, prefix_len: int = 1024,
                       max_suffix: int = 256, num_heads: int = 32, block_size: int = 16,
-                      num_blocks: int = 4096, seed: int = 1003) -> Workload:
+                      num_blocks: int = 4096, seed: int = 1003, materialize: bool = True) -> Workload:
     """Parallel sampling: each prompt's prefix blocks are shared by its branches
     (ref_count = branches).  Before appending its suffix, each branch takes a
     private copy of the last shared block (one (src, dst) copy pair per branch),
@@ -315,14 +319,17 @@ def shared_prefix_f16(num_prompts: int = 16, branches: int = 8, prefix_len: int 
     D = 128
     alloc = BlockAllocator(num_blocks, block_size, rng)
     shape = (num_blocks, num_heads, block_size, D)
-    k_cache, v_cache = nan_array(shape, "f16"), nan_array(shape, "f16")
+    k_cache = v_cache = None
+    if materialize:
+        k_cache, v_cache = nan_array(shape, "f16"), nan_array(shape, "f16")
     seqs, pairs, slots = [], [], []
     last_logical = (prefix_len - 1) // block_size
     suffix_lens = rng.integers(1, max_suffix, size=num_prompts * branches, endpoint=True)
     for p in range(num_prompts):
         root = 10_000 + p
         alloc.allocate(root, prefix_len)
-        _fill_tokens(k_cache, v_cache, rng, alloc, root, 0, prefix_len, "f16")
+        if materialize:
+            _fill_tokens(k_cache, v_cache, rng, alloc, root, 0, prefix_len, "f16")
         for b in range(branches):
             alloc.fork(root, len(seqs) + 0)
             seqs.append(len(seqs))
@@ -352,25 +359,88 @@ def shared_prefix_f16(num_prompts: int = 16, branches: int = 8, prefix_len: int 
     return w
 
 
-def long_bf16(block_size: int = 16, num_seqs: int = 8, seq_len: int = 32768, partition_size: int = 512) -> Workload:
+def long_bf16(block_size: int = 16, num_seqs: int = 8, seq_len: int = 32768, partition_size: int = 512,
+              materialize: bool = True) -> Workload:
     """Long context: 8 seqs of 32768 tokens, 32 q heads / 8 kv heads, D = 128, block
     size swept over {16, 32, 64}, pool exactly the blocks needed (shuffled), split
     into 512-token partitions merged by log-sum-exp."""
     nb = num_seqs * (-(-seq_len // block_size))
     return build_decode(f"long_bf16_b{block_size}", seed=1004, dtype="bf16", seq_lens=[seq_len] * num_seqs,
                         num_q_heads=32, num_kv_heads=8, head_size=128, block_size=block_size, num_blocks=nb,
-                        partition_size=partition_size)
+                        partition_size=partition_size, materialize=materialize)
 
 
 WORKLOADS = {
-    "tiny_f32": tiny_f32,
+    "tiny_f32": lambda materialize=True: tiny_f32(),
     "mha_f16": mha_f16,
     "gqa_bf16": gqa_bf16,
     "shared_prefix_f16": shared_prefix_f16,
-    "long_bf16_b16": lambda: long_bf16(16),
-    "long_bf16_b32": lambda: long_bf16(32),
-    "long_bf16_b64": lambda: long_bf16(64),
+    "long_bf16_b16": lambda materialize=True: long_bf16(16, materialize=materialize),
+    "long_bf16_b32": lambda materialize=True: long_bf16(32, materialize=materialize),
+    "long_bf16_b64": lambda materialize=True: long_bf16(64, materialize=materialize),
 }
+
+
+def device_caches(w: Workload, device, seed: int | None = None):
+    """K and V pools generated on the device with torch's seeded generator: every
+    slot N(0, 1) in the workload dtype (used for timing, where unused slots need no
+    poison and host generation of gigabyte pools would dominate the run)."""
+    import torch
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.dtype]
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(w.info.get("seed", 0) if seed is None else seed))
+    shape = (w.num_blocks, w.num_kv_heads, w.block_size, w.head_size)
+    out = []
+    for _ in range(2):
+        t = torch.empty(shape, dtype=tdt, device=device)
+        flat = t.view(-1)
+        step = 1 << 26
+        for i in range(0, flat.numel(), step):
+            n = min(step, flat.numel() - i)
+            flat[i:i + n] = torch.randn(n, generator=gen, device=device, dtype=torch.float32).to(tdt)
+        out.append(t)
+    return out[0], out[1]
+
+
+def host_sample(w: Workload, seqs, seed: int = 7) -> Workload:
+    """The sub-workload of sequences ``seqs`` with a compact host pool holding only
+    their blocks (freshly drawn N(0,1) values; copy pairs and appends restricted to
+    those sequences).  Used to time the CPU evaluation on a bounded sample."""
+    rng = np.random.default_rng(seed)
+    seqs = [int(s) for s in seqs]
+    B = w.block_size
+    used = []
+    for s in seqs:
+        used.extend(int(b) for b in w.block_tables[s, :-(-int(w.seq_lens[s]) // B)])
+    srcs = []
+    if w.copy_pairs is not None:
+        used_set = set(used)
+        srcs = [int(a) for a, b in w.copy_pairs if int(b) in used_set]
+        used.extend(srcs)
+    ids = sorted(set(used))
+    remap = {b: i for i, b in enumerate(ids)}
+    shape = (max(1, len(ids)), w.num_kv_heads, B, w.head_size)
+    k = normal(rng, shape, w.dtype)
+    v = normal(rng, shape, w.dtype)
+    tables = np.zeros((len(seqs), w.max_blocks_per_seq), np.int32)
+    for i, s in enumerate(seqs):
+        n = -(-int(w.seq_lens[s]) // B)
+        tables[i, :n] = [remap[int(b)] for b in w.block_tables[s, :n]]
+    pairs = None
+    if w.copy_pairs is not None:
+        pairs = np.asarray([(remap[int(a)], remap[int(b)]) for a, b in w.copy_pairs if int(b) in remap and
+                            int(a) in remap], np.int32).reshape(-1, 2)
+    slots = nk = nv = None
+    if w.slot_mapping is not None:
+        keep = [t for t, sl in enumerate(w.slot_mapping) if sl >= 0 and int(sl) // B in remap]
+        slots = np.asarray([remap[int(w.slot_mapping[t]) // B] * B + int(w.slot_mapping[t]) % B for t in keep],
+                           np.int64)
+        nk, nv = w.new_key[keep], w.new_value[keep]
+    return Workload(name=w.name + "_sample", dtype=w.dtype, num_q_heads=w.num_q_heads,
+                    num_kv_heads=w.num_kv_heads, head_size=w.head_size, block_size=B, num_blocks=shape[0],
+                    scale=w.scale, q=w.q[seqs], k_cache=k, v_cache=v, block_tables=tables,
+                    seq_lens=w.seq_lens[seqs].copy(), copy_pairs=pairs, slot_mapping=slots, new_key=nk,
+                    new_value=nv, partition_size=w.partition_size, info=dict(w.info))
 
 
 def apply_writes_host(w: Workload, k_cache: np.ndarray, v_cache: np.ndarray, copy_fn, append_fn) -> None:
