@@ -40,6 +40,12 @@ namespace pa {
 
 constexpr uint64_t kWaitLimit = 250ull * 1000 * 1000;  // 250 ms per wait
 
+// bf16 probabilities are split into a rounded part and its residual (see the value MMA)
+template <typename T>
+constexpr bool kSplitP = false;
+template <>
+constexpr bool kSplitP<__nv_bfloat16> = true;
+
 template <int D, int SB, int NW, int NS>
 struct TcShape {
   static constexpr int KSTEPS = D / 16;             // k-steps of Q K^T = m-tiles of V^T P^T
@@ -213,12 +219,21 @@ __global__ void __launch_bounds__(NW * 32)
         const float al_a = fast_exp2(m_a - mn_a), al_b = fast_exp2(m_b - mn_b);
         m_a = mn_a;
         m_b = mn_b;
-        const uint32_t x0 = Mma<T>::pack(fast_exp2(s0 - mn_a), fast_exp2(s1 - mn_b));
-        const uint32_t x1 = Mma<T>::pack(fast_exp2(s2 - mn_a), fast_exp2(s3 - mn_b));
-        // the sums use the rounded probabilities the value MMA multiplies with
-        {
-          const T* h0 = reinterpret_cast<const T*>(&x0);
-          const T* h1 = reinterpret_cast<const T*>(&x1);
+        const float p0 = fast_exp2(s0 - mn_a), p1 = fast_exp2(s1 - mn_b);
+        const float p2 = fast_exp2(s2 - mn_a), p3 = fast_exp2(s3 - mn_b);
+        const uint32_t x0 = Mma<T>::pack(p0, p1);
+        const uint32_t x1 = Mma<T>::pack(p2, p3);
+        // bf16 keeps only 8 significant bits of P; its rounding residual goes
+        // through a second MMA so P enters the value sum with ~16 bits.
+        uint32_t y0 = 0, y1 = 0;
+        const T* h0 = reinterpret_cast<const T*>(&x0);
+        const T* h1 = reinterpret_cast<const T*>(&x1);
+        if constexpr (kSplitP<T>) {
+          y0 = Mma<T>::pack(p0 - float(h0[0]), p1 - float(h0[1]));
+          y1 = Mma<T>::pack(p2 - float(h1[0]), p3 - float(h1[1]));
+          l_a = l_a * al_a + (p0 + p2);
+          l_b = l_b * al_b + (p1 + p3);
+        } else {  // fp16: the sums use the rounded probabilities the value MMA multiplies with
           l_a = l_a * al_a + (float(h0[0]) + float(h1[0]));
           l_b = l_b * al_b + (float(h0[1]) + float(h1[1]));
         }
@@ -232,6 +247,11 @@ __global__ void __launch_bounds__(NW * 32)
         // P^T fragments: (tokens 2q4, 2q4+1 | +8, +9 ; head g)
         const uint32_t pb0 = movmatrix_trans(x0);
         const uint32_t pb1 = movmatrix_trans(x1);
+        uint32_t pc0 = 0, pc1 = 0;
+        if constexpr (kSplitP<T>) {
+          pc0 = movmatrix_trans(y0);
+          pc1 = movmatrix_trans(y1);
+        }
         // ---- O^T[D x 8 heads] += V_unit^T P^T
         {
           const int row = u * 16 + (lane & 7) + (lane >> 4) * 8;
@@ -251,6 +271,7 @@ __global__ void __launch_bounds__(NW * 32)
               a3 &= mhi;
             }
             Mma<T>::run(o[i], a0, a1, a2, a3, pb0, pb1);
+            if constexpr (kSplitP<T>) Mma<T>::run(o[i], a0, a1, a2, a3, pc0, pc1);
           }
         }
       }

@@ -11,6 +11,33 @@ import oracle as O
 import workloads as W
 
 TOL = {"f32": 1e-5, "f16": 3e-3, "bf16": 3e-3}
+MANTISSA_BITS = {"f16": 10, "bf16": 7}
+
+
+def bound(ref: np.ndarray, dtype: str) -> np.ndarray:
+    """Per-element error bound against the fp64 result.
+
+    The stated tolerance (1e-5 fp32, 3e-3 fp16/bf16).  Rounding the output to a
+    16-bit type alone costs half an ulp of |out|; for bf16 that exceeds 3e-3 once
+    |out| >= 1 (half an ulp on [1, 2) is 2^-8), which very short sequences can
+    reach.  There the bound is that half ulp plus 1e-3 of arithmetic error; for
+    |out| < 1 (every output of the five benchmark workloads) it is exactly the
+    stated tolerance."""
+    tol = TOL[dtype]
+    if dtype == "f32":
+        return np.full(ref.shape, tol)
+    e = np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -14)))
+    half_ulp = 2.0 ** (e - MANTISSA_BITS[dtype] - 1)
+    return np.maximum(tol, half_ulp + 1e-3)
+
+
+def within_bound(got: np.ndarray, ref: np.ndarray, dtype: str):
+    """(ok, max abs error, worst error / bound)."""
+    if ref.size == 0:
+        return True, 0.0, 0.0
+    err = np.abs(got - ref)
+    ratio = err / bound(ref, dtype)
+    return bool(np.all(ratio <= 1.0)), float(err.max()), float(ratio.max())
 
 
 def to_torch(a: np.ndarray, dtype: str, device="cuda"):
@@ -93,5 +120,5 @@ def oracle_step(w: W.Workload, threads: int = 0):
     return k, v, out
 
 
-def max_abs_err(gpu_out, ref: np.ndarray) -> float:
+def max_abs_err(gpu_out, ref: np.ndarray) -> float:  # noqa: E302
     return float(np.max(np.abs(out_f64(gpu_out) - ref))) if ref.size else 0.0
