@@ -344,6 +344,8 @@ def run_ours(args, world, rank, local):
     device = torch.device(f"cuda:{local}")
     torch.cuda.set_device(device)
     w = W.WORKLOADS[args.workload](materialize=False)
+    if args.partition is not None:
+        w.partition_size = args.partition
     ds = DeviceStep(w, device)
     sampler = ClockSampler(local)
     sampler.start()
@@ -462,6 +464,8 @@ def main():
                                                    "shared_prefix_f16"])
     ap.add_argument("--no-extra", action="store_true", help="time only the headline workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--partition", type=int, default=None,
+                    help="tokens per split-KV partition (multiple of the block size; 0 = library default)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     world, rank, local = dist_setup()

@@ -9,24 +9,25 @@
 // reduction ("PagedAttention是什麼？", section "PagedAttention Kernel在做什麼？").
 //
 // How (GB300 design, not the pages' CUDA-core kernel):
-//  * One CTA per (sequence, kv head, group of <= 8 query heads, partition).
+//  * Work item = (sequence, kv head, group of <= 8 query heads, partition).
 //    All query heads of a GQA group share one pass over the K/V bytes.
-//  * Cache layout [blocks][kv_heads][B][D]: one (block, kv head) is one
-//    contiguous B x D tile.  Each "slab" (16 or 32 tokens of one block) of K
-//    and of V is fetched by the tensor-memory-access engine
-//    (cp.async.bulk.tensor.2d, 128-byte swizzle) straight into shared memory,
-//    completion tracked by an mbarrier; the block ID comes from the table.
-//  * Every warp owns a private ring of NS slab buffers and a private subset of
-//    the partition's slabs (round-robin), so there is no inter-warp
-//    synchronisation until the final merge of the warps' partial results.
-//  * Scores S^T[16 tokens x 8 heads] = K Q^T and the value sum
-//    O^T[D x 8 heads] += V^T P^T run on the tensor cores (mma.m16n8k16, fp32
-//    accumulate), operands read with ldmatrix from the swizzled tiles; the
-//    probability tile is moved from accumulator layout to operand layout with
-//    movmatrix.  Softmax is online (running max and sum per head, fp32).
-//  The path is bound by HBM bandwidth (1 to 8 flop per byte), so the tensor
-//  cores only keep instruction issue low; the design goal is to keep enough
-//  bulk copies in flight to saturate HBM.
+//  * Persistent CTAs (one per SM) walk a static round-robin list of items.
+//    Inside a CTA one producer warp streams "slabs" (16 tokens of one block,
+//    K and V) through a deep ring of shared-memory stages with 2-D tensor-map
+//    copies (cp.async.bulk.tensor, 128-byte swizzle), completion counted on
+//    per-stage mbarriers.  It reads the block IDs from the table a batch of 32
+//    ahead and never waits for compute except when the ring is full, and it
+//    runs on into the next item while the consumers finish the current one,
+//    so HBM sees one continuous stream per SM.
+//  * NC consumer warps take the slabs of an item round-robin.  Per 16-token
+//    slab a warp computes S^T[16 tokens x 8 heads] = K Q^T and
+//    O^T[D x 8 heads] += V^T P^T on the tensor cores (mma.m16n8k16, fp32
+//    accumulate) from ldmatrix reads of the swizzled tiles, with movmatrix
+//    turning the probability tile from accumulator into operand layout, and an
+//    online softmax (running max and sum per head, fp32).  At the end of an
+//    item the consumers merge their partial results through shared memory.
+//  The path is bound by HBM bandwidth (1 to 8 flop per byte); the tensor cores
+//  only keep the instruction count per byte low.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -46,165 +47,234 @@ constexpr bool kSplitP = false;
 template <>
 constexpr bool kSplitP<__nv_bfloat16> = true;
 
-template <int D, int SB, int NW, int NS>
-struct TcShape {
-  static constexpr int KSTEPS = D / 16;             // k-steps of Q K^T = m-tiles of V^T P^T
-  static constexpr int NBOX = D / 64;               // 128-byte (64-element) TMA boxes per row
-  static constexpr int BOX_BYTES = SB * 128;        // one box: SB rows x 128 bytes
+template <int D, int NC, int NS>
+struct Pipe {
+  static constexpr int SB = 16;                            // tokens per slab
+  static constexpr int KSTEPS = D / 16;                    // k-steps of Q K^T = m-tiles of V^T P^T
+  static constexpr int NBOX = D / 64;                      // 128-byte (64-element) TMA boxes per row
+  static constexpr int BOX_BYTES = SB * 128;               // one box: 16 rows x 128 bytes
   static constexpr int SLAB_BYTES = 2 * NBOX * BOX_BYTES;  // K boxes, then V boxes
-  static constexpr int UNITS = SB / 16;             // 16-token MMA units per slab
-  static constexpr int RING_BYTES = NS * SLAB_BYTES;  // per warp
-  static constexpr int SMEM_BYTES = NW * RING_BYTES + NW * NS * 8 + 1024;  // + barriers + alignment slack
+  static constexpr int RING_BYTES = NS * SLAB_BYTES;
+  static constexpr int MERGE_BYTES = NC * 8 * (D + 2) * 4;  // per consumer warp: O[8][D], (m, l)[8]
+  static constexpr int FULL_OFF = RING_BYTES + MERGE_BYTES;
+  static constexpr int EMPTY_OFF = FULL_OFF + NS * 8;
+  static constexpr int VALID_OFF = EMPTY_OFF + NS * 8;
+  static constexpr int ABORT_OFF = VALID_OFF + NS * 4;
+  static constexpr int SMEM_BYTES = ABORT_OFF + 16 + 1024;  // + alignment slack
+  static constexpr int THREADS = (NC + 1) * 32;
   static_assert(D % 64 == 0, "head_size must be a multiple of 64");
-  static_assert(SB == 16 || SB == 32, "slab is 16 or 32 tokens");
-  static_assert(RING_BYTES >= 8 * D * 4 + 8 * 2 * 4, "ring must hold a warp's partial result");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
-template <typename T, int D, int SB, int NW, int NS>
-__global__ void __launch_bounds__(NW * 32)
+// One work item, decoded identically by the producer and the consumers.
+struct Item {
+  int s, hkv, hq0, gcount, part;
+  int L;          // tokens of the sequence
+  int t_end;      // end of this partition
+  int j0;         // first slab (16 tokens) of the partition
+  int nslabs;
+  bool final_out;  // the sequence has a single partition: write the normalised output
+};
+
+__device__ __forceinline__ bool decode_item(const DecodeParams& p, int id, Item& it) {
+  const int per_seq = p.num_kv_heads * p.head_groups;
+  it.part = id % p.pmax;
+  const int hh = (id / p.pmax) % per_seq;
+  it.s = id / (p.pmax * per_seq);
+  it.hkv = hh / p.head_groups;
+  const int hg = hh % p.head_groups;
+  const int G = p.num_q_heads / p.num_kv_heads;
+  it.hq0 = it.hkv * G + hg * 8;
+  it.gcount = min(8, G - hg * 8);
+  int L = __ldg(p.seq_lens + it.s);
+  L = max(0, min(L, p.max_blocks * p.block_size));
+  it.L = L;
+  const int t_begin = it.part * p.partition_size;
+  if (L == 0) {  // an empty sequence: partition 0 writes a zero row
+    it.t_end = 0;
+    it.j0 = 0;
+    it.nslabs = 0;
+    it.final_out = true;
+    return it.part == 0;
+  }
+  if (t_begin >= L) return false;
+  it.t_end = min(L, t_begin + p.partition_size);
+  it.j0 = t_begin / 16;
+  it.nslabs = (it.t_end - t_begin + 15) / 16;
+  it.final_out = L <= p.partition_size;
+  return true;
+}
+
+// Wait for a barrier phase; gives up (returning false) when the CTA's abort
+// flag is set or after kWaitLimit, in which case it raises the abort flag.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t start = global_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if ((i & 63u) == 63u && global_ns() - start > kWaitLimit) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+template <typename T, int D, int NC, int NS>
+__global__ void __launch_bounds__(Pipe<D, NC, NS>::THREADS, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                      const DecodeParams p) {
-  using S = TcShape<D, SB, NW, NS>;
+  using S = Pipe<D, NC, NS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  float* merge = reinterpret_cast<float*>(smem + S::RING_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::FULL_OFF);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + S::EMPTY_OFF);
+  volatile int32_t* stage_valid = reinterpret_cast<volatile int32_t*>(smem + S::VALID_OFF);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + S::ABORT_OFF);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int g = lane >> 2;   // fragment row group
-  const int q4 = lane & 3;   // fragment column pair
-  uint8_t* ring = smem + warp * S::RING_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * S::RING_BYTES) + warp * NS;
+  const int total_items = p.num_seqs * p.num_kv_heads * p.head_groups * p.pmax;
 
-  // ---- work item: (sequence, kv head, head group, partition)
-  const int per_seq = p.num_kv_heads * p.head_groups;
-  const int part = blockIdx.x % p.pmax;
-  const int hh = (blockIdx.x / p.pmax) % per_seq;
-  const int s = blockIdx.x / (p.pmax * per_seq);
-  const int hkv = hh / p.head_groups;
-  const int hg = hh % p.head_groups;
-  const int G = p.num_q_heads / p.num_kv_heads;
-  const int hq0 = hkv * G + hg * 8;
-  const int gcount = min(8, G - hg * 8);
-  const int B = p.block_size;
-  const int P = p.partition_size;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
 
-  int L = p.seq_lens[s];
-  L = max(0, min(L, p.max_blocks * B));
-  const int t_begin = part * P;
-  if (L == 0) {
-    if (part == 0) {  // an empty sequence has a zero output
-      T* out = reinterpret_cast<T*>(p.out) + ((size_t)s * p.num_q_heads + hq0) * D;
-      for (int i = threadIdx.x; i < gcount * D; i += NW * 32) out[i] = from_float<T>(0.f);
+  if (warp == NC) {
+    // ======================= producer warp =======================
+    tma_prefetch_descriptor(&tmap_k);
+    tma_prefetch_descriptor(&tmap_v);
+    const int B = p.block_size;
+    uint32_t kk = 0;  // slabs issued by this CTA so far
+    // every decision below is taken by lane 0 and broadcast, so the warp never diverges
+    for (int id = blockIdx.x; id < total_items; id += gridDim.x) {
+      int stop = 0;
+      if (lane == 0) {
+        stop = *abort_flag;
+        if (!stop && p.err_flag != nullptr &&
+            *reinterpret_cast<volatile int32_t*>(p.err_flag) == PA_DEVERR_TIMEOUT) {
+          *abort_flag = 1;  // another CTA timed out: stop early
+          stop = 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0)) break;
+      Item it;
+      if (!decode_item(p, id, it)) continue;
+      const int32_t* table = p.block_tables + (size_t)it.s * p.max_blocks;
+      int pb_reg = -1;
+      for (int j = 0; j < it.nslabs; ++j, ++kk) {
+        if ((j & 31) == 0) {
+          const int jj = j + lane;
+          pb_reg = jj < it.nslabs ? __ldg(table + ((it.j0 + jj) * S::SB) / B) : -1;
+        }
+        const int pb = __shfl_sync(0xffffffffu, pb_reg, j & 31);
+        const int stage = kk % NS;
+        bool ok = true;
+        if (lane == 0 && kk >= (uint32_t)NS) ok = wait_phase(&empty[stage], ((kk / NS) - 1) & 1, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (lane == 0) {
+          uint64_t* bar = &full[stage];
+          const bool valid = pb >= 0 && pb < p.num_blocks;
+          stage_valid[stage] = valid;
+          if (valid) {
+            const int y = (pb * p.num_kv_heads + it.hkv) * B + ((it.j0 + j) * S::SB) % B;  // first row
+            uint8_t* dst = ring + stage * S::SLAB_BYTES;
+            mbar_arrive_expect_tx(bar, S::SLAB_BYTES);
+#pragma unroll
+            for (int b = 0; b < S::NBOX; ++b) tma_load_2d(dst + b * S::BOX_BYTES, &tmap_k, b * 64, y, bar);
+#pragma unroll
+            for (int b = 0; b < S::NBOX; ++b)
+              tma_load_2d(dst + (S::NBOX + b) * S::BOX_BYTES, &tmap_v, b * 64, y, bar);
+          } else {
+            report_error(p.err_flag, PA_DEVERR_BLOCK_ID);
+            mbar_arrive(bar);  // complete the phase without data; consumers skip the slab
+          }
+        }
+        __syncwarp();
+      }
+    }
+    if (*abort_flag) {
+      report_error(p.err_flag, PA_DEVERR_TIMEOUT);
+      // let copies already in flight land before the CTA's shared memory is released
+      if (lane == 0) {
+        volatile int32_t never = 0;
+        const uint32_t first = kk > (uint32_t)NS ? kk - NS : 0;
+        for (uint32_t k = first; k < kk; ++k) wait_phase(&full[k % NS], (k / NS) & 1, &never);
+      }
     }
     return;
   }
-  if (t_begin >= L) return;  // partition past the end of this sequence
-  // after a timed-out copy anywhere in this launch, the remaining CTAs stop early
-  if (p.err_flag != nullptr && *reinterpret_cast<volatile int32_t*>(p.err_flag) == PA_DEVERR_TIMEOUT) return;
-  const int t_end = min(L, t_begin + P);
-  const bool final_out = L <= P;  // single partition: write the normalised output directly
 
-  // ---- slabs of this partition owned by this warp: j = j0 + warp + k * NW
-  const int j0 = t_begin / SB;
-  const int j1 = (t_end + SB - 1) / SB;
-  const int n_my = (j1 - j0 - warp + NW - 1) / NW > 0 ? (j1 - j0 - warp + NW - 1) / NW : 0;
-  const int32_t* table = p.block_tables + (size_t)s * p.max_blocks;
+  // ======================= consumer warps =======================
+  const int g = lane >> 2;   // fragment row group
+  const int q4 = lane & 3;   // fragment column pair
+  const float sl2 = p.scale_log2;
+  uint32_t kk_base = 0;
+  for (int id = blockIdx.x; id < total_items; id += gridDim.x) {
+    Item it;
+    if (!decode_item(p, id, it)) continue;
+    // (no early exit here: every consumer warp must reach both barriers of every
+    // item; after an abort the waits below return at once instead)
 
-  if (lane == 0) {
-    for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
-    fence_barrier_init();
-  }
-  __syncwarp();
-
-  // ---- query fragments (B operand of S^T = K Q^T): head g, dims 16j + 2q4 (+8)
-  uint32_t qf[S::KSTEPS][2];
-  {
-    const bool real = g < gcount;
-    const uint32_t* qrow =
-        reinterpret_cast<const uint32_t*>(reinterpret_cast<const T*>(p.q) + ((size_t)s * p.num_q_heads + hq0 + g) * D);
+    // query fragments (B operand of S^T = K Q^T): head g, dims 16j + 2q4 (+8)
+    uint32_t qf[S::KSTEPS][2];
+    {
+      const bool real = g < it.gcount;
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(reinterpret_cast<const T*>(p.q) +
+                                                               ((size_t)it.s * p.num_q_heads + it.hq0 + g) * D);
 #pragma unroll
-    for (int j = 0; j < S::KSTEPS; ++j) {
-      qf[j][0] = real ? __ldg(qrow + (16 * j + 2 * q4) / 2) : 0u;
-      qf[j][1] = real ? __ldg(qrow + (16 * j + 2 * q4 + 8) / 2) : 0u;
-    }
-  }
-
-  // ---- block-table entries, fetched 32 slabs at a time across the lanes
-  int pb_batch = -1;
-  int pb_reg = -1;
-  uint32_t valid_mask = 0;  // bit stage: the slab in that stage was loaded
-  auto issue = [&](int k) {
-    const int batch = k >> 5;
-    if (batch != pb_batch) {
-      const int kk = batch * 32 + lane;
-      pb_reg = kk < n_my ? __ldg(table + ((j0 + warp + kk * NW) * SB) / B) : -1;
-      pb_batch = batch;
-    }
-    const int pb = __shfl_sync(0xffffffffu, pb_reg, k & 31);
-    const bool ok = pb >= 0 && pb < p.num_blocks;
-    const int stage = k % NS;
-    valid_mask = ok ? (valid_mask | (1u << stage)) : (valid_mask & ~(1u << stage));
-    if (lane == 0) {
-      uint64_t* bar = &bars[stage];
-      if (ok) {
-        const int j = j0 + warp + k * NW;
-        const int y = (pb * p.num_kv_heads + hkv) * B + (j * SB) % B;  // first row of the slab
-        uint8_t* dst = ring + stage * S::SLAB_BYTES;
-        mbar_arrive_expect_tx(bar, S::SLAB_BYTES);
-#pragma unroll
-        for (int b = 0; b < S::NBOX; ++b) tma_load_2d(dst + b * S::BOX_BYTES, &tmap_k, b * 64, y, bar);
-#pragma unroll
-        for (int b = 0; b < S::NBOX; ++b) tma_load_2d(dst + (S::NBOX + b) * S::BOX_BYTES, &tmap_v, b * 64, y, bar);
-      } else {
-        report_error(p.err_flag, PA_DEVERR_BLOCK_ID);
-        mbar_arrive(bar);  // complete the phase without data; the slab is skipped
+      for (int j = 0; j < S::KSTEPS; ++j) {
+        qf[j][0] = real ? __ldg(qrow + (16 * j + 2 * q4) / 2) : 0u;
+        qf[j][1] = real ? __ldg(qrow + (16 * j + 2 * q4 + 8) / 2) : 0u;
       }
     }
-  };
-
-  float o[S::KSTEPS][4];
+    float o[S::KSTEPS][4];
 #pragma unroll
-  for (int i = 0; i < S::KSTEPS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m_a = -INFINITY, m_b = -INFINITY;  // running max (log2 units) of heads 2q4, 2q4+1
-  float l_a = 0.f, l_b = 0.f;              // this lane's share of the running sums
-  const float sl2 = p.scale_log2;
+    for (int i = 0; i < S::KSTEPS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m_a = -INFINITY, m_b = -INFINITY;  // running max (log2 units) of heads 2q4, 2q4+1
+    float l_a = 0.f, l_b = 0.f;              // this lane's share of the running sums
 
-  const int prologue = n_my < NS ? n_my : NS;
-  for (int k = 0; k < prologue; ++k) issue(k);
-
-  int consumed = 0;
-  bool timed_out = false;
-  for (int k = 0; k < n_my; ++k) {
-    const int stage = k % NS;
-    if (!mbar_wait_bounded(&bars[stage], (k / NS) & 1, kWaitLimit)) {
-      timed_out = true;
-      break;
-    }
-    consumed = k + 1;
-    if ((valid_mask >> stage) & 1u) {
-      const int j = j0 + warp + k * NW;
-      const int valid = min(SB, t_end - j * SB);
-      const uint8_t* kst = ring + stage * S::SLAB_BYTES;
-      const uint8_t* vst = kst + S::NBOX * S::BOX_BYTES;
-#pragma unroll
-      for (int u = 0; u < S::UNITS; ++u) {
-        const int nvalid = valid - u * 16;
-        if (nvalid <= 0) break;
-        // ---- S^T[16 tokens x 8 heads] = K_unit Q^T
+    for (int j = warp; j < it.nslabs; j += NC) {
+      const uint32_t kk = kk_base + j;
+      const int stage = kk % NS;
+      if (!__all_sync(0xffffffffu, wait_phase(&full[stage], (kk / NS) & 1, abort_flag))) break;
+      if (stage_valid[stage]) {
+        const int nvalid = min(S::SB, it.t_end - (it.j0 + j) * S::SB);
+        const uint8_t* kst = ring + stage * S::SLAB_BYTES;
+        const uint8_t* vst = kst + S::NBOX * S::BOX_BYTES;
+        // ---- S^T[16 tokens x 8 heads] = K_slab Q^T (two accumulators: shorter dependency chain)
         float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        float sd[4] = {0.f, 0.f, 0.f, 0.f};
         {
-          const int row = u * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+          const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
           const int khalf = lane >> 4;
 #pragma unroll
           for (int jj = 0; jj < S::KSTEPS; ++jj) {
             const uint32_t addr = smem_u32(kst + (jj >> 2) * S::BOX_BYTES) + swz128(row, (jj & 3) * 2 + khalf);
             uint32_t a0, a1, a2, a3;
             ldmatrix_x4(addr, a0, a1, a2, a3);
-            Mma<T>::run(sc, a0, a1, a2, a3, qf[jj][0], qf[jj][1]);
+            if (jj & 1)
+              Mma<T>::run(sd, a0, a1, a2, a3, qf[jj][0], qf[jj][1]);
+            else
+              Mma<T>::run(sc, a0, a1, a2, a3, qf[jj][0], qf[jj][1]);
           }
         }
-        // sc: (token g, head 2q4), (token g, head 2q4+1), (token g+8, head 2q4), (token g+8, head 2q4+1)
-        float s0 = sc[0] * sl2, s1 = sc[1] * sl2, s2 = sc[2] * sl2, s3 = sc[3] * sl2;
+        // scores: (token g, head 2q4), (token g, head 2q4+1), (token g+8, head 2q4), (token g+8, head 2q4+1)
+        float s0 = (sc[0] + sd[0]) * sl2, s1 = (sc[1] + sd[1]) * sl2;
+        float s2 = (sc[2] + sd[2]) * sl2, s3 = (sc[3] + sd[3]) * sl2;
         if (nvalid < 16) {
           if (g >= nvalid) s0 = s1 = -INFINITY;
           if (g + 8 >= nvalid) s2 = s3 = -INFINITY;
@@ -252,9 +322,9 @@ __global__ void __launch_bounds__(NW * 32)
           pc0 = movmatrix_trans(y0);
           pc1 = movmatrix_trans(y1);
         }
-        // ---- O^T[D x 8 heads] += V_unit^T P^T
+        // ---- O^T[D x 8 heads] += V_slab^T P^T
         {
-          const int row = u * 16 + (lane & 7) + (lane >> 4) * 8;
+          const int row = (lane & 7) + (lane >> 4) * 8;
           const int dhalf = (lane >> 3) & 1;
 #pragma unroll
           for (int i = 0; i < S::KSTEPS; ++i) {
@@ -275,106 +345,105 @@ __global__ void __launch_bounds__(NW * 32)
           }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);  // stage free for the producer
     }
-    __syncwarp();
-    if (k + NS < n_my) issue(k + NS);
-  }
+    kk_base += it.nslabs;
 
-  if (timed_out) {
-    report_error(p.err_flag, PA_DEVERR_TIMEOUT);
-    // let copies already in flight land before this warp's buffers are reused
-    const int issued = n_my < consumed + NS ? n_my : consumed + NS;
-    for (int k = consumed; k < issued; ++k) mbar_wait_bounded(&bars[k % NS], (k / NS) & 1, kWaitLimit);
-  }
-
-  // ---- per-warp totals, then merge the warps through shared memory
+    // ---- per-warp totals into shared memory, then merge the warps
 #pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    l_a += __shfl_xor_sync(0xffffffffu, l_a, off);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, off);
-  }
-  __syncwarp();
-  float* wo = reinterpret_cast<float*>(ring);  // [8 heads][D]
-  float* wml = wo + 8 * D;                     // [8 heads][2]
-#pragma unroll
-  for (int i = 0; i < S::KSTEPS; ++i) {
-    wo[(2 * q4) * D + 16 * i + g] = o[i][0];
-    wo[(2 * q4 + 1) * D + 16 * i + g] = o[i][1];
-    wo[(2 * q4) * D + 16 * i + g + 8] = o[i][2];
-    wo[(2 * q4 + 1) * D + 16 * i + g + 8] = o[i][3];
-  }
-  if (g == 0) {
-    wml[(2 * q4) * 2] = m_a;
-    wml[(2 * q4) * 2 + 1] = l_a;
-    wml[(2 * q4 + 1) * 2] = m_b;
-    wml[(2 * q4 + 1) * 2 + 1] = l_b;
-  }
-  __syncthreads();
-
-  const size_t row0 = (size_t)s * p.num_q_heads + hq0;
-  for (int idx = threadIdx.x; idx < gcount * D; idx += NW * 32) {
-    const int gh = idx / D, d = idx % D;
-    float mstar = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      const float* wm = reinterpret_cast<const float*>(smem + w * S::RING_BYTES) + 8 * D;
-      mstar = fmaxf(mstar, wm[gh * 2]);
+    for (int off = 4; off < 32; off <<= 1) {
+      l_a += __shfl_xor_sync(0xffffffffu, l_a, off);
+      l_b += __shfl_xor_sync(0xffffffffu, l_b, off);
     }
-    float lsum = 0.f, acc = 0.f;
-    if (mstar != -INFINITY) {
+    float* wo = merge + warp * 8 * (D + 2);  // [8 heads][D], then [8 heads][2]
+    float* wml = wo + 8 * D;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float* wb = reinterpret_cast<const float*>(smem + w * S::RING_BYTES);
-        const float wt = fast_exp2(wb[8 * D + gh * 2] - mstar);
-        lsum += wt * wb[8 * D + gh * 2 + 1];
-        acc += wt * wb[gh * D + d];
+    for (int i = 0; i < S::KSTEPS; ++i) {
+      wo[(2 * q4) * D + 16 * i + g] = o[i][0];
+      wo[(2 * q4 + 1) * D + 16 * i + g] = o[i][1];
+      wo[(2 * q4) * D + 16 * i + g + 8] = o[i][2];
+      wo[(2 * q4 + 1) * D + 16 * i + g + 8] = o[i][3];
+    }
+    if (g == 0) {
+      wml[(2 * q4) * 2] = m_a;
+      wml[(2 * q4) * 2 + 1] = l_a;
+      wml[(2 * q4 + 1) * 2] = m_b;
+      wml[(2 * q4 + 1) * 2 + 1] = l_b;
+    }
+    consumer_sync(NC * 32);
+
+    const size_t row0 = (size_t)it.s * p.num_q_heads + it.hq0;
+    for (int idx = threadIdx.x; idx < it.gcount * D; idx += NC * 32) {
+      const int gh = idx / D, d = idx % D;
+      float mstar = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NC; ++w) mstar = fmaxf(mstar, merge[w * 8 * (D + 2) + 8 * D + gh * 2]);
+      float lsum = 0.f, acc = 0.f;
+      if (mstar != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < NC; ++w) {
+          const float* wb = merge + w * 8 * (D + 2);
+          const float wt = fast_exp2(wb[8 * D + gh * 2] - mstar);
+          lsum += wt * wb[8 * D + gh * 2 + 1];
+          acc += wt * wb[gh * D + d];
+        }
+      }
+      if (it.final_out) {
+        T* out = reinterpret_cast<T*>(p.out);
+        out[(row0 + gh) * D + d] = from_float<T>(lsum > 0.f ? acc / lsum : 0.f);
+      } else {
+        const size_t slot = (row0 + gh) * p.pmax + it.part;
+        p.ws_o[slot * D + d] = acc;
+        if (d == 0) {
+          p.ws_ml[slot * 2] = mstar;
+          p.ws_ml[slot * 2 + 1] = lsum;
+        }
       }
     }
-    if (final_out) {
-      T* out = reinterpret_cast<T*>(p.out);
-      out[(row0 + gh) * D + d] = from_float<T>(lsum > 0.f ? acc / lsum : 0.f);
-    } else {
-      const size_t slot = (row0 + gh) * p.pmax + part;
-      p.ws_o[slot * D + d] = acc;
-      if (d == 0) {
-        p.ws_ml[slot * 2] = mstar;
-        p.ws_ml[slot * 2 + 1] = lsum;
-      }
-    }
+    consumer_sync(NC * 32);  // merge buffer free again
   }
 }
 
 // ------------------------------------------------------------------ launch
-template <typename T, int D, int SB, int NW, int NS>
+static int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+template <typename T, int D, int NC, int NS>
 static cudaError_t launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                              cudaStream_t stream) {
-  using S = TcShape<D, SB, NW, NS>;
-  auto kernel = decode_tc_kernel<T, D, SB, NW, NS>;
+  using S = Pipe<D, NC, NS>;
+  auto kernel = decode_tc_kernel<T, D, NC, NS>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const long long grid = (long long)p.num_seqs * p.num_kv_heads * p.head_groups * p.pmax;
-  if (grid == 0) return cudaSuccess;
-  kernel<<<(unsigned)grid, NW * 32, S::SMEM_BYTES, stream>>>(tk, tv, p);
+  const long long items = (long long)p.num_seqs * p.num_kv_heads * p.head_groups * p.pmax;
+  if (items == 0) return cudaSuccess;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const unsigned grid = (unsigned)(items < sms ? items : sms);
+  kernel<<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tk, tv, p);
   return cudaGetLastError();
 }
 
-// Per-warp ring depth and warps per CTA chosen so a CTA holds about 96 KB of
-// slabs (two CTAs per SM) with every warp keeping NS - 1 slabs in flight.
+// One persistent CTA per SM: 8 consumer warps + 1 producer warp; the ring
+// takes the shared memory left after the consumers' merge buffers.
 template <typename T>
-static cudaError_t dispatch_tc(int head_size, int block_size, const CUtensorMap& tk, const CUtensorMap& tv,
-                               const DecodeParams& p, cudaStream_t stream) {
-  const int sb = tc_slab_tokens(block_size);
-  if (head_size == 128 && sb == 16) return launch_tc<T, 128, 16, 4, 3>(tk, tv, p, stream);
-  if (head_size == 128 && sb == 32) return launch_tc<T, 128, 32, 2, 3>(tk, tv, p, stream);
-  if (head_size == 64 && sb == 16) return launch_tc<T, 64, 16, 4, 4>(tk, tv, p, stream);
-  if (head_size == 64 && sb == 32) return launch_tc<T, 64, 32, 4, 3>(tk, tv, p, stream);
+static cudaError_t dispatch_tc(int head_size, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                               cudaStream_t stream) {
+  if (head_size == 128) return launch_tc<T, 128, 8, 22>(tk, tv, p, stream);
+  if (head_size == 64) return launch_tc<T, 64, 8, 48>(tk, tv, p, stream);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_decode_tc(int dtype, int head_size, int block_size, const CUtensorMap& tk, const CUtensorMap& tv,
                              const DecodeParams& p, cudaStream_t stream) {
-  if (dtype == PA_F16) return dispatch_tc<__half>(head_size, block_size, tk, tv, p, stream);
-  if (dtype == PA_BF16) return dispatch_tc<__nv_bfloat16>(head_size, block_size, tk, tv, p, stream);
+  (void)block_size;
+  if (dtype == PA_F16) return dispatch_tc<__half>(head_size, tk, tv, p, stream);
+  if (dtype == PA_BF16) return dispatch_tc<__nv_bfloat16>(head_size, tk, tv, p, stream);
   return cudaErrorInvalidValue;
 }
 
