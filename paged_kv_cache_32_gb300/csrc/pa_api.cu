@@ -179,8 +179,8 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
                               static_cast<const float*>(v_cache), p, st);
   } else {
     CUtensorMap tk, tv;
-    const int slab = pa::tc_slab_tokens(cache->block_size);
-    if (!encode_cache_map(&tk, k_cache, cache, slab) || !encode_cache_map(&tv, v_cache, cache, slab))
+    if (!encode_cache_map(&tk, k_cache, cache, pa::kTcSlabTokens) ||
+        !encode_cache_map(&tv, v_cache, cache, pa::kTcSlabTokens))
       return PA_ERR_CUDA;
     e = pa::launch_decode_tc(cache->dtype, cache->head_size, cache->block_size, tk, tv, p, st);
   }

@@ -49,7 +49,7 @@ constexpr bool kSplitP<__nv_bfloat16> = true;
 
 template <int D, int NC, int NS>
 struct Pipe {
-  static constexpr int SB = 16;                            // tokens per slab
+  static constexpr int SB = kTcSlabTokens;                 // tokens per slab (= TMA box rows)
   static constexpr int KSTEPS = D / 16;                    // k-steps of Q K^T = m-tiles of V^T P^T
   static constexpr int NBOX = D / 64;                      // 128-byte (64-element) TMA boxes per row
   static constexpr int BOX_BYTES = SB * 128;               // one box: 16 rows x 128 bytes

@@ -40,7 +40,8 @@ cudaError_t launch_reshape_and_cache(void* k_cache, void* v_cache, const void* k
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int32_t num_pairs,
                                int32_t num_blocks, int64_t block_bytes, int32_t* err_flag, cudaStream_t stream);
 
-// Slab (TMA tile height in tokens) used by the tensor-core decode for a block size.
-inline int tc_slab_tokens(int block_size) { return block_size % 32 == 0 ? 32 : 16; }
+// Slab (TMA box height in tokens) of the tensor-core decode: 16 tokens of one
+// block; the kernel's stage layout and transaction counts assume exactly this.
+constexpr int kTcSlabTokens = 16;
 
 }  // namespace pa
