@@ -89,14 +89,14 @@ enum {
  *   ceil(seq_lens[s] / B) are never read.
  *
  *   out          [num_seqs][num_q_heads][head_size] of dtype (written)
- *   q            [num_seqs][num_q_heads][head_size] of dtype, 4-byte aligned
+ *   q            [num_seqs][num_q_heads][head_size] of dtype, 16-byte aligned (f32: 4)
  *   k_cache, v_cache  cache pair (layout above), 16-byte aligned
  *   block_tables int32 [num_seqs][max_blocks_per_seq], row-major
  *   seq_lens     int32 [num_seqs]; each <= max_blocks_per_seq * block_size (not checked
  *                on the device beyond the table width: longer values are clamped)
  *   scale        softmax scale (usually 1/sqrt(head_size))
  *   partition_size  0 = library default; else tokens per partition, a multiple of
- *                block_size (f16/bf16: also of 32 when block_size >= 32).  Sequences longer
+ *                block_size.  Sequences longer
  *                than one partition are split across CTAs and merged with a
  *                log-sum-exp reduction [P4 "PagedAttention Kernel在做什麼？"].
  *   workspace    device scratch of at least pa_decode_workspace_size(...) bytes,

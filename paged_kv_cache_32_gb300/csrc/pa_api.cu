@@ -141,7 +141,10 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
   const size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, max_blocks_per_seq, cache, partition_size);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PA_ERR_WORKSPACE;
   if (need > 0 && !aligned(workspace, 256)) return PA_ERR_MISALIGNED;
-  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 4) || !aligned(out, 4)) return PA_ERR_MISALIGNED;
+  // f16/bf16: caches and q are read by bulk copies (16-byte aligned); fp32: 4-byte loads
+  const uintptr_t qalign = cache->dtype == PA_F32 ? 4 : 16;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, qalign) || !aligned(out, 4))
+    return PA_ERR_MISALIGNED;
   const int G = num_q_heads / cache->num_kv_heads;
   const int head_groups = (G + 7) / 8;
   const long long grid = (long long)num_seqs * cache->num_kv_heads * head_groups * pmax;

@@ -39,7 +39,7 @@
 
 namespace pa {
 
-constexpr uint64_t kWaitLimit = 250ull * 1000 * 1000;  // 250 ms per wait
+constexpr long long kWaitCycles = 500ll * 1000 * 1000;  // bound on one wait: ~0.25 s at 2 GHz
 
 // bf16 probabilities are split into a rounded part and its residual (see the value MMA)
 template <typename T>
@@ -55,21 +55,27 @@ struct Pipe {
   static constexpr int BOX_BYTES = SB * 128;               // one box: 16 rows x 128 bytes
   static constexpr int SLAB_BYTES = 2 * NBOX * BOX_BYTES;  // K boxes, then V boxes
   static constexpr int RING_BYTES = NS * SLAB_BYTES;
-  static constexpr int MERGE_BYTES = NC * 8 * (D + 2) * 4;  // per consumer warp: O[8][D], (m, l)[8]
-  static constexpr int FULL_OFF = RING_BYTES + MERGE_BYTES;
+  static constexpr int OROW = D + 4;                       // merge row stride (floats): conflict-free stores
+  static constexpr int WARP_MERGE = 8 * OROW + 16;         // per consumer warp: O[8][OROW], (m, l)[8]
+  static constexpr int MERGE_OFF = RING_BYTES;
+  static constexpr int Q_OFF = MERGE_OFF + NC * WARP_MERGE * 4;
+  static constexpr int Q_BYTES = 8 * D * 2;                // one item's query rows (<= 8 heads)
+  static constexpr int FULL_OFF = Q_OFF + 2 * Q_BYTES;
   static constexpr int EMPTY_OFF = FULL_OFF + NS * 8;
-  static constexpr int VALID_OFF = EMPTY_OFF + NS * 8;
-  static constexpr int ABORT_OFF = VALID_OFF + NS * 4;
+  static constexpr int QFULL_OFF = EMPTY_OFF + NS * 8;
+  static constexpr int QEMPTY_OFF = QFULL_OFF + 2 * 8;
+  static constexpr int VALID_OFF = QEMPTY_OFF + 2 * 8;
+  static constexpr int ABORT_OFF = VALID_OFF + NS * 4;     // abort flag, then a word that stays 0
   static constexpr int SMEM_BYTES = ABORT_OFF + 16 + 1024;  // + alignment slack
   static constexpr int THREADS = (NC + 1) * 32;
   static_assert(D % 64 == 0, "head_size must be a multiple of 64");
+  static_assert(Q_OFF % 16 == 0 && FULL_OFF % 8 == 0, "alignment of the q buffers and barriers");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
 // One work item, decoded identically by the producer and the consumers.
 struct Item {
   int s, hkv, hq0, gcount, part;
-  int L;          // tokens of the sequence
   int t_end;      // end of this partition
   int j0;         // first slab (16 tokens) of the partition
   int nslabs;
@@ -88,7 +94,6 @@ __device__ __forceinline__ bool decode_item(const DecodeParams& p, int id, Item&
   it.gcount = min(8, G - hg * 8);
   int L = __ldg(p.seq_lens + it.s);
   L = max(0, min(L, p.max_blocks * p.block_size));
-  it.L = L;
   const int t_begin = it.part * p.partition_size;
   if (L == 0) {  // an empty sequence: partition 0 writes a zero row
     it.t_end = 0;
@@ -99,21 +104,27 @@ __device__ __forceinline__ bool decode_item(const DecodeParams& p, int id, Item&
   }
   if (t_begin >= L) return false;
   it.t_end = min(L, t_begin + p.partition_size);
-  it.j0 = t_begin / 16;
-  it.nslabs = (it.t_end - t_begin + 15) / 16;
+  it.j0 = t_begin / kTcSlabTokens;
+  it.nslabs = (it.t_end - t_begin + kTcSlabTokens - 1) / kTcSlabTokens;
   it.final_out = L <= p.partition_size;
   return true;
 }
 
+// First item id >= `id` (stepping by `stride`) that has work; `total` if none.
+__device__ __forceinline__ int next_active(const DecodeParams& p, int id, int stride, int total, Item& it) {
+  while (id < total && !decode_item(p, id, it)) id += stride;
+  return id;
+}
+
 // Wait for a barrier phase; gives up (returning false) when the CTA's abort
-// flag is set or after kWaitLimit, in which case it raises the abort flag.
+// flag is set or after kWaitCycles SM cycles, in which case it raises the flag.
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t start = global_ns();
+  const long long start = clock64();
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if ((i & 63u) == 63u && global_ns() - start > kWaitLimit) {
+    if ((i & 15u) == 15u && clock64() - start > kWaitCycles) {
       *abort_flag = 1;
       return false;
     }
@@ -132,11 +143,15 @@ __global__ void __launch_bounds__(Pipe<D, NC, NS>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  float* merge = reinterpret_cast<float*>(smem + S::RING_BYTES);
+  float* merge = reinterpret_cast<float*>(smem + S::MERGE_OFF);
+  uint8_t* qbuf = smem + S::Q_OFF;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::FULL_OFF);
   uint64_t* empty = reinterpret_cast<uint64_t*>(smem + S::EMPTY_OFF);
+  uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + S::QFULL_OFF);
+  uint64_t* qempty = reinterpret_cast<uint64_t*>(smem + S::QEMPTY_OFF);
   volatile int32_t* stage_valid = reinterpret_cast<volatile int32_t*>(smem + S::VALID_OFF);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + S::ABORT_OFF);
+  volatile int32_t* never_flag = abort_flag + 1;  // stays 0: waits that must not be cut short
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -147,41 +162,55 @@ __global__ void __launch_bounds__(Pipe<D, NC, NS>::THREADS, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    *abort_flag = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&qfull[i], 1);
+      mbar_init(&qempty[i], NC);
+    }
+    abort_flag[0] = 0;
+    never_flag[0] = 0;
     fence_barrier_init();
   }
   __syncthreads();
 
   if (warp == NC) {
     // ======================= producer warp =======================
+    // Lane 0 issues every copy; the other lanes fetch block-table entries (32
+    // slabs per batch).  The next item's first batch is requested while the
+    // current item streams, so no dependent global load sits between items.
     tma_prefetch_descriptor(&tmap_k);
     tma_prefetch_descriptor(&tmap_v);
     const int B = p.block_size;
-    uint32_t kk = 0;  // slabs issued by this CTA so far
-    // every decision below is taken by lane 0 and broadcast, so the warp never diverges
-    for (int id = blockIdx.x; id < total_items; id += gridDim.x) {
-      int stop = 0;
+    auto table_batch = [&](const Item& it, int j) -> int {
+      const int jj = j + lane;
+      return jj < it.nslabs ? __ldg(p.block_tables + (size_t)it.s * p.max_blocks + ((it.j0 + jj) * S::SB) / B) : -1;
+    };
+    Item cur, nxt;
+    int cur_id = next_active(p, blockIdx.x, gridDim.x, total_items, cur);
+    int nxt_id = cur_id < total_items ? next_active(p, cur_id + gridDim.x, gridDim.x, total_items, nxt) : total_items;
+    int pb_cur = cur_id < total_items ? table_batch(cur, 0) : -1;
+    int pb_nxt = nxt_id < total_items ? table_batch(nxt, 0) : -1;
+    uint32_t kk = 0;      // slabs issued by this CTA so far
+    uint32_t n_item = 0;  // items started by this CTA so far
+    bool ok = true;
+    while (ok && cur_id < total_items) {
+      // ---- the item's query rows -> q buffer (n_item & 1)
       if (lane == 0) {
-        stop = *abort_flag;
-        if (!stop && p.err_flag != nullptr &&
-            *reinterpret_cast<volatile int32_t*>(p.err_flag) == PA_DEVERR_TIMEOUT) {
-          *abort_flag = 1;  // another CTA timed out: stop early
-          stop = 1;
+        const int qb = n_item & 1;
+        if (n_item >= 2) ok = wait_phase(&qempty[qb], ((n_item >> 1) - 1) & 1, abort_flag);
+        if (ok) {
+          const uint32_t bytes = cur.gcount * D * 2;
+          mbar_arrive_expect_tx(&qfull[qb], bytes);
+          bulk_load_1d(qbuf + qb * S::Q_BYTES,
+                       reinterpret_cast<const T*>(p.q) + ((size_t)cur.s * p.num_q_heads + cur.hq0) * D, bytes,
+                       &qfull[qb]);
         }
       }
-      if (__shfl_sync(0xffffffffu, stop, 0)) break;
-      Item it;
-      if (!decode_item(p, id, it)) continue;
-      const int32_t* table = p.block_tables + (size_t)it.s * p.max_blocks;
-      int pb_reg = -1;
-      for (int j = 0; j < it.nslabs; ++j, ++kk) {
-        if ((j & 31) == 0) {
-          const int jj = j + lane;
-          pb_reg = jj < it.nslabs ? __ldg(table + ((it.j0 + jj) * S::SB) / B) : -1;
-        }
-        const int pb = __shfl_sync(0xffffffffu, pb_reg, j & 31);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      // ---- the item's K/V slabs
+      for (int j = 0; ok && j < cur.nslabs; ++j, ++kk) {
+        if (j > 0 && (j & 31) == 0) pb_cur = table_batch(cur, j);
+        const int pb = __shfl_sync(0xffffffffu, pb_cur, j & 31);
         const int stage = kk % NS;
-        bool ok = true;
         if (lane == 0 && kk >= (uint32_t)NS) ok = wait_phase(&empty[stage], ((kk / NS) - 1) & 1, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
@@ -190,7 +219,7 @@ __global__ void __launch_bounds__(Pipe<D, NC, NS>::THREADS, 1)
           const bool valid = pb >= 0 && pb < p.num_blocks;
           stage_valid[stage] = valid;
           if (valid) {
-            const int y = (pb * p.num_kv_heads + it.hkv) * B + ((it.j0 + j) * S::SB) % B;  // first row
+            const int y = (pb * p.num_kv_heads + cur.hkv) * B + ((cur.j0 + j) * S::SB) % B;  // first row
             uint8_t* dst = ring + stage * S::SLAB_BYTES;
             mbar_arrive_expect_tx(bar, S::SLAB_BYTES);
 #pragma unroll
@@ -205,14 +234,24 @@ __global__ void __launch_bounds__(Pipe<D, NC, NS>::THREADS, 1)
         }
         __syncwarp();
       }
+      // ---- advance: the prefetched next item becomes current
+      ++n_item;
+      cur = nxt;
+      cur_id = nxt_id;
+      pb_cur = pb_nxt;
+      if (cur_id < total_items) {
+        nxt_id = next_active(p, cur_id + gridDim.x, gridDim.x, total_items, nxt);
+        pb_nxt = nxt_id < total_items ? table_batch(nxt, 0) : -1;
+      }
     }
-    if (*abort_flag) {
+    if (!ok) {
       report_error(p.err_flag, PA_DEVERR_TIMEOUT);
       // let copies already in flight land before the CTA's shared memory is released
       if (lane == 0) {
-        volatile int32_t never = 0;
         const uint32_t first = kk > (uint32_t)NS ? kk - NS : 0;
-        for (uint32_t k = first; k < kk; ++k) wait_phase(&full[k % NS], (k / NS) & 1, &never);
+        for (uint32_t k = first; k < kk; ++k) wait_phase(&full[k % NS], (k / NS) & 1, never_flag);
+        if (n_item >= 1) wait_phase(&qfull[(n_item - 1) & 1], ((n_item - 1) >> 1) & 1, never_flag);
+        if (n_item >= 2) wait_phase(&qfull[n_item & 1], ((n_item - 2) >> 1) & 1, never_flag);
       }
     }
     return;
@@ -223,24 +262,29 @@ __global__ void __launch_bounds__(Pipe<D, NC, NS>::THREADS, 1)
   const int q4 = lane & 3;   // fragment column pair
   const float sl2 = p.scale_log2;
   uint32_t kk_base = 0;
+  uint32_t n_item = 0;
   for (int id = blockIdx.x; id < total_items; id += gridDim.x) {
     Item it;
     if (!decode_item(p, id, it)) continue;
-    // (no early exit here: every consumer warp must reach both barriers of every
+    // (no early exit: every consumer warp must reach both barriers of every
     // item; after an abort the waits below return at once instead)
 
     // query fragments (B operand of S^T = K Q^T): head g, dims 16j + 2q4 (+8)
     uint32_t qf[S::KSTEPS][2];
     {
+      const int qb = n_item & 1;
+      __all_sync(0xffffffffu, wait_phase(&qfull[qb], (n_item >> 1) & 1, abort_flag));
       const bool real = g < it.gcount;
-      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(reinterpret_cast<const T*>(p.q) +
-                                                               ((size_t)it.s * p.num_q_heads + it.hq0 + g) * D);
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qbuf + qb * S::Q_BYTES + g * D * 2);
 #pragma unroll
       for (int j = 0; j < S::KSTEPS; ++j) {
-        qf[j][0] = real ? __ldg(qrow + (16 * j + 2 * q4) / 2) : 0u;
-        qf[j][1] = real ? __ldg(qrow + (16 * j + 2 * q4 + 8) / 2) : 0u;
+        qf[j][0] = real ? qrow[(16 * j + 2 * q4) / 2] : 0u;
+        qf[j][1] = real ? qrow[(16 * j + 2 * q4 + 8) / 2] : 0u;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&qempty[qb]);
     }
+    ++n_item;
     float o[S::KSTEPS][4];
 #pragma unroll
     for (int i = 0; i < S::KSTEPS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -296,16 +340,14 @@ __global__ void __launch_bounds__(Pipe<D, NC, NS>::THREADS, 1)
         // bf16 keeps only 8 significant bits of P; its rounding residual goes
         // through a second MMA so P enters the value sum with ~16 bits.
         uint32_t y0 = 0, y1 = 0;
-        const T* h0 = reinterpret_cast<const T*>(&x0);
-        const T* h1 = reinterpret_cast<const T*>(&x1);
         if constexpr (kSplitP<T>) {
-          y0 = Mma<T>::pack(p0 - float(h0[0]), p1 - float(h0[1]));
-          y1 = Mma<T>::pack(p2 - float(h1[0]), p3 - float(h1[1]));
+          y0 = Mma<T>::pack(p0 - Mma<T>::lo(x0), p1 - Mma<T>::hi(x0));
+          y1 = Mma<T>::pack(p2 - Mma<T>::lo(x1), p3 - Mma<T>::hi(x1));
           l_a = l_a * al_a + (p0 + p2);
           l_b = l_b * al_b + (p1 + p3);
         } else {  // fp16: the sums use the rounded probabilities the value MMA multiplies with
-          l_a = l_a * al_a + (float(h0[0]) + float(h1[0]));
-          l_b = l_b * al_b + (float(h0[1]) + float(h1[1]));
+          l_a = l_a * al_a + (Mma<T>::lo(x0) + Mma<T>::lo(x1));
+          l_b = l_b * al_b + (Mma<T>::hi(x0) + Mma<T>::hi(x1));
         }
 #pragma unroll
         for (int i = 0; i < S::KSTEPS; ++i) {
@@ -356,14 +398,14 @@ __global__ void __launch_bounds__(Pipe<D, NC, NS>::THREADS, 1)
       l_a += __shfl_xor_sync(0xffffffffu, l_a, off);
       l_b += __shfl_xor_sync(0xffffffffu, l_b, off);
     }
-    float* wo = merge + warp * 8 * (D + 2);  // [8 heads][D], then [8 heads][2]
-    float* wml = wo + 8 * D;
+    float* wo = merge + warp * S::WARP_MERGE;  // [8 heads][OROW], then [8 heads][2]
+    float* wml = wo + 8 * S::OROW;
 #pragma unroll
     for (int i = 0; i < S::KSTEPS; ++i) {
-      wo[(2 * q4) * D + 16 * i + g] = o[i][0];
-      wo[(2 * q4 + 1) * D + 16 * i + g] = o[i][1];
-      wo[(2 * q4) * D + 16 * i + g + 8] = o[i][2];
-      wo[(2 * q4 + 1) * D + 16 * i + g + 8] = o[i][3];
+      wo[(2 * q4) * S::OROW + 16 * i + g] = o[i][0];
+      wo[(2 * q4 + 1) * S::OROW + 16 * i + g] = o[i][1];
+      wo[(2 * q4) * S::OROW + 16 * i + g + 8] = o[i][2];
+      wo[(2 * q4 + 1) * S::OROW + 16 * i + g + 8] = o[i][3];
     }
     if (g == 0) {
       wml[(2 * q4) * 2] = m_a;
@@ -378,15 +420,15 @@ __global__ void __launch_bounds__(Pipe<D, NC, NS>::THREADS, 1)
       const int gh = idx / D, d = idx % D;
       float mstar = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < NC; ++w) mstar = fmaxf(mstar, merge[w * 8 * (D + 2) + 8 * D + gh * 2]);
+      for (int w = 0; w < NC; ++w) mstar = fmaxf(mstar, merge[w * S::WARP_MERGE + 8 * S::OROW + gh * 2]);
       float lsum = 0.f, acc = 0.f;
       if (mstar != -INFINITY) {
 #pragma unroll
         for (int w = 0; w < NC; ++w) {
-          const float* wb = merge + w * 8 * (D + 2);
-          const float wt = fast_exp2(wb[8 * D + gh * 2] - mstar);
-          lsum += wt * wb[8 * D + gh * 2 + 1];
-          acc += wt * wb[gh * D + d];
+          const float* wb = merge + w * S::WARP_MERGE;
+          const float wt = fast_exp2(wb[8 * S::OROW + gh * 2] - mstar);
+          lsum += wt * wb[8 * S::OROW + gh * 2 + 1];
+          acc += wt * wb[gh * S::OROW + d];
         }
       }
       if (it.final_out) {

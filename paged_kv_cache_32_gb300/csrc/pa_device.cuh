@@ -45,25 +45,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Bounded wait: returns false if the phase did not complete within `limit_ns`
-// nanoseconds of wall time (and at most 2^30 polls).
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t start = global_ns();
-  for (uint32_t i = 0; i < (1u << 30); ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u && global_ns() - start > limit_ns) return false;
-  }
-  return false;
-}
-
 // ---------------------------------------------------------------- TMA
+// 1-D bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16),
+// completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_load_1d(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(smem_dst)),
+               "l"(reinterpret_cast<uint64_t>(gmem_src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 // 2-D tiled tensor load global -> shared, completion counted on `bar` in bytes.
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, int32_t x, int32_t y, uint64_t* bar) {
   asm volatile(
@@ -116,6 +107,9 @@ struct Mma<__half> {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
   }
+  // the two halves of a packed pair, as fp32
+  static __device__ __forceinline__ float lo(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x & 0xffffu))); }
+  static __device__ __forceinline__ float hi(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x >> 16))); }
 };
 
 template <>
@@ -132,6 +126,9 @@ struct Mma<__nv_bfloat16> {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
   }
+  // bfloat16 is the upper half of a binary32: widening is a shift
+  static __device__ __forceinline__ float lo(uint32_t x) { return __uint_as_float(x << 16); }
+  static __device__ __forceinline__ float hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 };
 
 // ---------------------------------------------------------------- math
