@@ -47,7 +47,7 @@ constexpr bool kSplitP = false;
 template <>
 constexpr bool kSplitP<__nv_bfloat16> = true;
 
-template <int D, int NC, int NS>
+template <int D, int NC, int NP, int NS>
 struct Pipe {
   static constexpr int SB = kTcSlabTokens;                 // tokens per slab (= TMA box rows)
   static constexpr int KSTEPS = D / 16;                    // k-steps of Q K^T = m-tiles of V^T P^T
@@ -67,8 +67,9 @@ struct Pipe {
   static constexpr int VALID_OFF = QEMPTY_OFF + 2 * 8;
   static constexpr int ABORT_OFF = VALID_OFF + NS * 4;     // abort flag, then a word that stays 0
   static constexpr int SMEM_BYTES = ABORT_OFF + 16 + 1024;  // + alignment slack
-  static constexpr int THREADS = (NC + 1) * 32;
+  static constexpr int THREADS = (NC + NP) * 32;
   static_assert(D % 64 == 0, "head_size must be a multiple of 64");
+  static_assert(NS % NP == 0, "each producer warp owns every NP-th stage");
   static_assert(Q_OFF % 16 == 0 && FULL_OFF % 8 == 0, "alignment of the q buffers and barriers");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
@@ -135,11 +136,11 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
-template <typename T, int D, int NC, int NS>
-__global__ void __launch_bounds__(Pipe<D, NC, NS>::THREADS, 1)
+template <typename T, int D, int NC, int NP, int NS>
+__global__ void __launch_bounds__(Pipe<D, NC, NP, NS>::THREADS, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                      const DecodeParams p) {
-  using S = Pipe<D, NC, NS>;
+  using S = Pipe<D, NC, NP, NS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
@@ -172,11 +173,18 @@ __global__ void __launch_bounds__(Pipe<D, NC, NS>::THREADS, 1)
   }
   __syncthreads();
 
-  if (warp == NC) {
-    // ======================= producer warp =======================
-    // Lane 0 issues every copy; the other lanes fetch block-table entries (32
-    // slabs per batch).  The next item's first batch is requested while the
-    // current item streams, so no dependent global load sits between items.
+  if (warp >= NC) {
+    // ======================= producer warps =======================
+    // A tensor copy takes a producer thread a few hundred cycles to issue, so NP
+    // warps issue in parallel.  Producer pw owns the stages s with s % NP == pw
+    // (NS is a multiple of NP) and issues exactly the slabs kk with
+    // kk % NP == pw, in order, so every use of a stage is issued by one warp
+    // right after the previous use was released (no phase aliasing).  All
+    // producers walk the same item sequence; producer 0 also copies each item's
+    // query rows.  Lane 0 issues; the other lanes fetch block-table entries
+    // (32 slabs per batch), the next item's first batch while the current item
+    // streams, so no dependent global load sits between items.
+    const int pw = warp - NC;
     tma_prefetch_descriptor(&tmap_k);
     tma_prefetch_descriptor(&tmap_v);
     const int B = p.block_size;
@@ -194,7 +202,7 @@ __global__ void __launch_bounds__(Pipe<D, NC, NS>::THREADS, 1)
     bool ok = true;
     while (ok && cur_id < total_items) {
       // ---- the item's query rows -> q buffer (n_item & 1)
-      if (lane == 0) {
+      if (lane == 0 && pw == 0) {
         const int qb = n_item & 1;
         if (n_item >= 2) ok = wait_phase(&qempty[qb], ((n_item >> 1) - 1) & 1, abort_flag);
         if (ok) {
@@ -210,6 +218,7 @@ __global__ void __launch_bounds__(Pipe<D, NC, NS>::THREADS, 1)
       for (int j = 0; ok && j < cur.nslabs; ++j, ++kk) {
         if (j > 0 && (j & 31) == 0) pb_cur = table_batch(cur, j);
         const int pb = __shfl_sync(0xffffffffu, pb_cur, j & 31);
+        if ((int)(kk % NP) != pw) continue;  // another producer's slab
         const int stage = kk % NS;
         if (lane == 0 && kk >= (uint32_t)NS) ok = wait_phase(&empty[stage], ((kk / NS) - 1) & 1, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -249,9 +258,10 @@ __global__ void __launch_bounds__(Pipe<D, NC, NS>::THREADS, 1)
       // let copies already in flight land before the CTA's shared memory is released
       if (lane == 0) {
         const uint32_t first = kk > (uint32_t)NS ? kk - NS : 0;
-        for (uint32_t k = first; k < kk; ++k) wait_phase(&full[k % NS], (k / NS) & 1, never_flag);
-        if (n_item >= 1) wait_phase(&qfull[(n_item - 1) & 1], ((n_item - 1) >> 1) & 1, never_flag);
-        if (n_item >= 2) wait_phase(&qfull[n_item & 1], ((n_item - 2) >> 1) & 1, never_flag);
+        for (uint32_t k = first; k < kk; ++k)
+          if ((int)(k % NP) == pw) wait_phase(&full[k % NS], (k / NS) & 1, never_flag);
+        if (pw == 0 && n_item >= 1) wait_phase(&qfull[(n_item - 1) & 1], ((n_item - 1) >> 1) & 1, never_flag);
+        if (pw == 0 && n_item >= 2) wait_phase(&qfull[n_item & 1], ((n_item - 2) >> 1) & 1, never_flag);
       }
     }
     return;
@@ -455,11 +465,11 @@ static int sm_count() {
   return n;
 }
 
-template <typename T, int D, int NC, int NS>
+template <typename T, int D, int NC, int NP, int NS>
 static cudaError_t launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                              cudaStream_t stream) {
-  using S = Pipe<D, NC, NS>;
-  auto kernel = decode_tc_kernel<T, D, NC, NS>;
+  using S = Pipe<D, NC, NP, NS>;
+  auto kernel = decode_tc_kernel<T, D, NC, NP, NS>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const long long items = (long long)p.num_seqs * p.num_kv_heads * p.head_groups * p.pmax;
@@ -471,13 +481,13 @@ static cudaError_t launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const
   return cudaGetLastError();
 }
 
-// One persistent CTA per SM: 8 consumer warps + 1 producer warp; the ring
+// One persistent CTA per SM: 8 consumer warps + 4 producer warps; the ring
 // takes the shared memory left after the consumers' merge buffers.
 template <typename T>
 static cudaError_t dispatch_tc(int head_size, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                                cudaStream_t stream) {
-  if (head_size == 128) return launch_tc<T, 128, 8, 22>(tk, tv, p, stream);
-  if (head_size == 64) return launch_tc<T, 64, 8, 48>(tk, tv, p, stream);
+  if (head_size == 128) return launch_tc<T, 128, 8, 4, 20>(tk, tv, p, stream);
+  if (head_size == 64) return launch_tc<T, 64, 8, 4, 48>(tk, tv, p, stream);
   return cudaErrorInvalidValue;
 }
 
