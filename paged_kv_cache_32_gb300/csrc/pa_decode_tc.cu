@@ -19,7 +19,10 @@
 //    ahead and never waits for compute except when the ring is full, and it
 //    runs on into the next item while the consumers finish the current one,
 //    so HBM sees one continuous stream per SM.
-//  * NC consumer warps take the slabs of an item round-robin.  Per 16-token
+//  * NC consumer warps take the slabs round-robin (slab kk -> warp kk % NC).
+//    Stage s = kk % NS is filled only by producer s % NP and drained only by
+//    consumer s % NC, so each stage's uses are issued and consumed in order
+//    and parity-based barrier waits never alias.  Per 16-token
 //    slab a warp computes S^T[16 tokens x 8 heads] = K Q^T and
 //    O^T[D x 8 heads] += V^T P^T on the tensor cores (mma.m16n8k16, fp32
 //    accumulate) from ldmatrix reads of the swizzled tiles, with movmatrix
@@ -69,7 +72,7 @@ struct Pipe {
   static constexpr int SMEM_BYTES = ABORT_OFF + 16 + 1024;  // + alignment slack
   static constexpr int THREADS = (NC + NP) * 32;
   static_assert(D % 64 == 0, "head_size must be a multiple of 64");
-  static_assert(NS % NP == 0, "each producer warp owns every NP-th stage");
+  static_assert(NS % NP == 0 && NS % NC == 0, "each stage has one producer and one consumer warp");
   static_assert(Q_OFF % 16 == 0 && FULL_OFF % 8 == 0, "alignment of the q buffers and barriers");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
@@ -301,7 +304,10 @@ __global__ void __launch_bounds__(Pipe<D, NC, NP, NS>::THREADS, 1)
     float m_a = -INFINITY, m_b = -INFINITY;  // running max (log2 units) of heads 2q4, 2q4+1
     float l_a = 0.f, l_b = 0.f;              // this lane's share of the running sums
 
-    for (int j = warp; j < it.nslabs; j += NC) {
+    // slab kk goes to consumer kk % NC: with NS a multiple of NC every stage is
+    // consumed by one warp, which therefore waits for its uses strictly in order
+    // (a warp never tests a stage's barrier two phases ahead).
+    for (int j = (int)((warp + NC - kk_base % NC) % NC); j < it.nslabs; j += NC) {
       const uint32_t kk = kk_base + j;
       const int stage = kk % NS;
       if (!__all_sync(0xffffffffu, wait_phase(&full[stage], (kk / NS) & 1, abort_flag))) break;
@@ -486,7 +492,7 @@ static cudaError_t launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const
 template <typename T>
 static cudaError_t dispatch_tc(int head_size, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                                cudaStream_t stream) {
-  if (head_size == 128) return launch_tc<T, 128, 8, 4, 20>(tk, tv, p, stream);
+  if (head_size == 128) return launch_tc<T, 128, 8, 4, 16>(tk, tv, p, stream);
   if (head_size == 64) return launch_tc<T, 64, 8, 4, 48>(tk, tv, p, stream);
   return cudaErrorInvalidValue;
 }
