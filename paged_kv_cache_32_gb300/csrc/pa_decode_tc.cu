@@ -389,13 +389,14 @@ static cudaError_t launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const
   return cudaGetLastError();
 }
 
-// Four warps per CTA, three 8 KB slab buffers per warp: 96 KB per CTA, two
-// CTAs (eight copy-issuing warps, 16 slabs in flight) per SM.
+// Four warps per CTA, two slab buffers per warp (64 KB per CTA at D = 128):
+// three CTAs, i.e. twelve copy-issuing warps, per SM.  Measured best among
+// 1-8 warps x 2-4 buffers on the MHA, GQA and long-context workloads.
 template <typename T>
 static cudaError_t dispatch_tc(int head_size, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                                cudaStream_t stream) {
-  if (head_size == 128) return launch_tc<T, 128, 4, 3>(tk, tv, p, stream);
-  if (head_size == 64) return launch_tc<T, 64, 4, 6>(tk, tv, p, stream);
+  if (head_size == 128) return launch_tc<T, 128, 4, 2>(tk, tv, p, stream);
+  if (head_size == 64) return launch_tc<T, 64, 4, 4>(tk, tv, p, stream);
   return cudaErrorInvalidValue;
 }
 
