@@ -147,6 +147,30 @@ int pa_reshape_and_cache(void* k_cache, void* v_cache, const void* key, const vo
 int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pairs, int32_t num_pairs,
                    const pa_cache_desc* cache, int32_t* err_flag, void* stream);
 
+/*
+ * pa_decode_noalloc - pa_decode for callers that cannot allocate device memory
+ *   while they decode (for example a serving plugin whose host engine owns all
+ *   device memory, or a decode loop that must stay out of the CUDA allocator).
+ *   The pages have no counterpart: this is a deployment convenience.
+ *
+ *   Same arguments and results as pa_decode, without workspace: the split-KV
+ *   scratch is a library-owned device array of PA_NOALLOC_MAX_WORKSPACE_BYTES
+ *   bytes, which every GPU that loads the library holds until the process
+ *   exits.  Sizes whose pa_decode_workspace_size() exceeds that limit return
+ *   PA_ERR_WORKSPACE and launch nothing.  The call allocates nothing.
+ *   - The first call on a device looks up the array's device address (with that
+ *     device current) and caches it; make that first call before any stream
+ *     capture.  It returns PA_ERR_CUDA if the lookup fails.
+ *   - All calls share the one array and it keeps the previous call's contents;
+ *     nothing in it needs clearing, but calls that overlap on the GPU (other
+ *     streams, other host threads) race on it: order them on one stream.
+ */
+#define PA_NOALLOC_MAX_WORKSPACE_BYTES ((size_t)16 << 20)
+int pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                      int32_t max_blocks_per_seq, const pa_cache_desc* cache, float scale, int32_t partition_size,
+                      int32_t* err_flag, void* stream);
+
 /* Static description of a status code (never NULL). */
 const char* pa_status_string(int status);
 

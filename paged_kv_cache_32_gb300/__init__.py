@@ -23,7 +23,7 @@ PA_DEVERR = {0: "none", 1: "block id out of range", 2: "slot out of range", 3: "
              4: "wait on an asynchronous copy timed out"}
 
 EXPORTED = ("pa_decode", "pa_decode_partition_size", "pa_decode_workspace_size", "pa_reshape_and_cache",
-            "pa_copy_blocks", "pa_status_string", "pa_version")
+            "pa_copy_blocks", "pa_status_string", "pa_version", "pa_decode_noalloc")
 
 
 class pa_cache_desc(ctypes.Structure):
