@@ -95,8 +95,8 @@ enum {
  *   seq_lens     int32 [num_seqs]; each <= max_blocks_per_seq * block_size (not checked
  *                on the device beyond the table width: longer values are clamped)
  *   scale        softmax scale (usually 1/sqrt(head_size))
- *   partition_size  0 = library default; else tokens per partition, a multiple of
- *                block_size.  Sequences longer
+ *   partition_size  0 = library default (1024 tokens); else tokens per partition, a
+ *                multiple of block_size.  Sequences longer
  *                than one partition are split across CTAs and merged with a
  *                log-sum-exp reduction [P4 "PagedAttention Kernel在做什麼？"].
  *   workspace    device scratch of at least pa_decode_workspace_size(...) bytes,

@@ -13,7 +13,7 @@
 
 namespace {
 
-constexpr int32_t kDefaultPartition = 512;  // tokens per partition when the caller passes 0
+constexpr int32_t kDefaultPartition = 1024;  // tokens per partition when the caller passes 0 (measured best)
 constexpr int64_t kInt32Max = 2147483647;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }

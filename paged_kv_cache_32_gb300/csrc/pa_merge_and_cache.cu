@@ -84,10 +84,13 @@ cudaError_t launch_merge(int dtype, int head_size, const DecodeParams& p, cudaSt
 // ---------------------------------------------------------------------------
 // Slot-mapping append ("PagedAttention 详解：缓存的存储结构", section "写入新
 // K/V"): block = slot / B, offset = slot % B; the token's [Hkv][D] key and
-// value rows go to (block, h, offset) of each cache.  One CTA per token, each
-// thread moving 16-byte vectors; negative slots are padding and skipped.
+// value rows go to (block, h, offset) of each cache.  Grid (token, chunk):
+// every thread moves one 16-byte vector of K and one of V, so a step's few
+// new tokens finish in one load-store round trip.  Negative slots are padding.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128)
+constexpr int kAppendThreads = 256;
+
+__global__ void __launch_bounds__(kAppendThreads)
     reshape_and_cache_kernel(uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
                              const uint8_t* __restrict__ key, const uint8_t* __restrict__ value,
                              const int64_t* __restrict__ slot_mapping, int32_t num_blocks, int32_t block_size,
@@ -98,22 +101,20 @@ __global__ void __launch_bounds__(128)
   const int64_t block = slot / block_size;
   const int64_t off = slot % block_size;
   if (block >= num_blocks) {
-    if (threadIdx.x == 0) report_error(err_flag, PA_DEVERR_SLOT);
+    if (threadIdx.x == 0 && blockIdx.y == 0) report_error(err_flag, PA_DEVERR_SLOT);
     return;
   }
   const int vec_per_row = row_bytes / 16;
-  const int total = num_kv_heads * vec_per_row;
-  const size_t src_base = (size_t)t * num_kv_heads * row_bytes;
-  for (int i = threadIdx.x; i < total; i += blockDim.x) {
-    const int h = i / vec_per_row;
-    const int c = i % vec_per_row;
-    const size_t src = src_base + (size_t)h * row_bytes + (size_t)c * 16;
-    const size_t dst = (((size_t)block * num_kv_heads + h) * block_size + off) * row_bytes + (size_t)c * 16;
-    const uint4 kx = __ldg(reinterpret_cast<const uint4*>(key + src));
-    const uint4 vx = __ldg(reinterpret_cast<const uint4*>(value + src));
-    *reinterpret_cast<uint4*>(k_cache + dst) = kx;
-    *reinterpret_cast<uint4*>(v_cache + dst) = vx;
-  }
+  const int i = blockIdx.y * kAppendThreads + threadIdx.x;
+  if (i >= num_kv_heads * vec_per_row) return;
+  const int h = i / vec_per_row;
+  const int c = i % vec_per_row;
+  const size_t src = ((size_t)t * num_kv_heads + h) * row_bytes + (size_t)c * 16;
+  const size_t dst = (((size_t)block * num_kv_heads + h) * block_size + off) * row_bytes + (size_t)c * 16;
+  const uint4 kx = __ldg(reinterpret_cast<const uint4*>(key + src));
+  const uint4 vx = __ldg(reinterpret_cast<const uint4*>(value + src));
+  *reinterpret_cast<uint4*>(k_cache + dst) = kx;
+  *reinterpret_cast<uint4*>(v_cache + dst) = vx;
 }
 
 cudaError_t launch_reshape_and_cache(void* k_cache, void* v_cache, const void* key, const void* value,
@@ -121,7 +122,9 @@ cudaError_t launch_reshape_and_cache(void* k_cache, void* v_cache, const void* k
                                      int32_t block_size, int32_t num_kv_heads, int32_t row_bytes,
                                      int32_t* err_flag, cudaStream_t stream) {
   if (num_tokens == 0) return cudaSuccess;
-  reshape_and_cache_kernel<<<num_tokens, 128, 0, stream>>>(
+  const int vectors = num_kv_heads * (row_bytes / 16);
+  dim3 grid((unsigned)num_tokens, (unsigned)((vectors + kAppendThreads - 1) / kAppendThreads));
+  reshape_and_cache_kernel<<<grid, kAppendThreads, 0, stream>>>(
       static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), static_cast<const uint8_t*>(key),
       static_cast<const uint8_t*>(value), slot_mapping, num_blocks, block_size, num_kv_heads, row_bytes, err_flag);
   return cudaGetLastError();

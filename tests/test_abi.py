@@ -74,8 +74,8 @@ def test_decode_argument_errors(lib):
 
 def test_partition_and_workspace_sizes(lib):
     d = desc(nb=16384, bs=16, hkv=8, d=128, dtype=pa.PA_BF16)
-    assert pa.pa_decode_partition_size(2048, d, 0) == 512
-    assert pa.pa_decode_partition_size(2048, d, 1024) == 1024
+    assert pa.pa_decode_partition_size(2048, d, 0) == 1024            # library default
+    assert pa.pa_decode_partition_size(2048, d, 512) == 512
     assert pa.pa_decode_partition_size(16, d, 0) == 256              # whole context fits: no split
     with pytest.raises(pa.PaError):
         pa.pa_decode_partition_size(2048, d, 100)
