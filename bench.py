@@ -97,7 +97,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
@@ -122,7 +122,7 @@ class ClockSampler:
     def summary(self, t0: float, t1: float):
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
-        inside = [p for (t, p) in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        inside = [p for (t, p) in self.samples if t0 - 0.05 <= t <= t1 + 0.05]
         if not inside:  # the timed region was shorter than the sampling period: nearest sample
             mid = 0.5 * (t0 + t1)
             inside = [min(self.samples, key=lambda tp: abs(tp[0] - mid))[1]]
@@ -310,6 +310,35 @@ def time_e2e(ds: DeviceStep, steps: int, warmup: int, world: int):
     return start.elapsed_time(end) / steps, h2d, d2h
 
 
+def block_manager_step_us(w: W.Workload, steps: int = 200, model=None) -> float:
+    """Host time of one decode step's metadata with a block manager: one
+    append_slots call for every sequence (slots + copy-on-write pairs) and one
+    build_tables call, averaged over `steps` steps."""
+    if model is None:
+        from paged_kv_cache_32_gb300.block_manager import BlockManager
+        bm = BlockManager(w.num_blocks + w.num_seqs * (steps // w.block_size + 2), w.block_size, shuffle_seed=1)
+        seqs = np.arange(w.num_seqs, dtype=np.int64)
+        for s in seqs:
+            bm.allocate(int(s), int(w.seq_lens[s]))
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            bm.append_slots(seqs)
+            bm.build_tables(seqs)
+        return 1e6 * (time.perf_counter() - t0) / steps
+    m = model(w.num_blocks + w.num_seqs * (steps // w.block_size + 2), w.block_size, 1)
+    for s in range(w.num_seqs):
+        m.allocate(s, int(w.seq_lens[s]))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        for s in range(w.num_seqs):
+            m.append_slot(s)
+        width = max(len(m.tables[s]) for s in range(w.num_seqs))
+        tables = np.zeros((w.num_seqs, width), np.int32)
+        for s in range(w.num_seqs):
+            tables[s, :len(m.tables[s])] = m.tables[s]
+    return 1e6 * (time.perf_counter() - t0) / steps
+
+
 def cpu_baseline(w_meta: W.Workload, budget_s: float = 12.0):
     """The oracle as it stands, on the host cores, over a bounded sample of the
     workload (whole sequences, in order), repeated until the budget is used."""
@@ -331,7 +360,9 @@ def cpu_baseline(w_meta: W.Workload, budget_s: float = 12.0):
         t_total += time.perf_counter() - t0
         reps += 1
     gbs = reps * sample.kv_bytes() / t_total / 1e9
+    from oracle.block_manager import BlockManagerModel
     return {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "block_manager_model_step_us": round(block_manager_step_us(w_meta, 50, BlockManagerModel), 1),
             "sample": f"{len(take)} of {n} sequences ({int(sample.seq_lens.sum())} tokens) x {reps} repetitions, "
                       f"{t_total:.1f} s wall, OpenMP over (seq, q head)",
             "tokens_per_s": reps * len(take) / t_total}
@@ -387,6 +418,8 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": round(world * kv / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": ds.launches_per_step() * args.steps,
+        "block_manager": {"step_us": round(block_manager_step_us(w), 2), "seqs": w.num_seqs,
+                          "ops": "append_slots + build_tables (C++ manager in libpa)"},
         "clocks": clocks,
     }
     if not args.no_extra and world == 1:

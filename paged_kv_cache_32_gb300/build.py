@@ -1,6 +1,6 @@
 """Build libpa.so in-tree (paged_kv_cache_32_gb300/_build/libpa.so) for sm_103a.
 
-Each .cu under csrc/ compiles to an object file in parallel, then nvcc links
+Each .cu (device code) and .cpp (host code) under csrc/ compiles to an object file in parallel, then nvcc links
 the shared library with the CUDA runtime linked statically, so the library
 loads without a GPU (the driver is reached at run time through the runtime's
 entry-point query).  No cmake; a couple of nvcc invocations.
@@ -34,7 +34,7 @@ def _nvcc() -> str:
 
 
 def _sources() -> list[str]:
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps() -> list[str]:
@@ -57,7 +57,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     flags = NVCC_FLAGS + (extra_flags or [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OUT_DIR, os.path.basename(src).replace(".cu", ".o"))
+        obj = os.path.join(OUT_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [nvcc, *ARCH, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
