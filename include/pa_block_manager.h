@@ -90,6 +90,10 @@ int pa_bm_free(pa_block_manager* bm, int64_t seq);
 int32_t pa_bm_seq_len(const pa_block_manager* bm, int64_t seq);
 int32_t pa_bm_num_seq_blocks(const pa_block_manager* bm, int64_t seq);
 
+/* Largest number of blocks among seqs[0..n) (the table width a decode step
+ * needs); PA_BM_ERR_UNKNOWN_SEQ / PA_BM_ERR_INVALID_ARG on errors. */
+int32_t pa_bm_max_seq_blocks(const pa_block_manager* bm, const int64_t* seqs, int32_t n);
+
 /* Decode-step metadata: row i of tables_out (width entries, zero-padded) is the
  * block table of seqs[i], lens_out[i] its length.  PA_BM_ERR_INVALID_ARG if a
  * table is wider than `width`. */

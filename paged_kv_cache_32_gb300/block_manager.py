@@ -60,6 +60,8 @@ def _L():
         L.pa_bm_seq_len.restype = i32
         L.pa_bm_num_seq_blocks.argtypes = [vp, i64]
         L.pa_bm_num_seq_blocks.restype = i32
+        L.pa_bm_max_seq_blocks.argtypes = [vp, vp, i32]
+        L.pa_bm_max_seq_blocks.restype = i32
         L.pa_bm_build_tables.argtypes = [vp, vp, i32, i32, vp, vp]
         L.pa_bm_build_tables.restype = ctypes.c_int
         _configured = True
@@ -135,7 +137,10 @@ class BlockManager:
     def build_tables(self, seqs, width: int | None = None):
         s = np.ascontiguousarray(seqs, dtype=np.int64)
         if width is None:
-            width = max([self.num_seq_blocks(int(x)) for x in s] + [1])
+            width = _L().pa_bm_max_seq_blocks(self._h, s.ctypes.data, len(s))
+            if width < 0:
+                raise BlockManagerError(width, "max_seq_blocks")
+            width = max(width, 1)
         tables = np.zeros((len(s), width), np.int32)
         lens = np.zeros(len(s), np.int32)
         self._check(_L().pa_bm_build_tables(self._h, s.ctypes.data, len(s), int(width), tables.ctypes.data,

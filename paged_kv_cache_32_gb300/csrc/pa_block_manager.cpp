@@ -290,6 +290,17 @@ int32_t pa_bm_num_seq_blocks(const pa_block_manager* bm, int64_t seq) {
   return it == bm->seqs.end() ? PA_BM_ERR_UNKNOWN_SEQ : (int32_t)it->second.blocks.size();
 }
 
+int32_t pa_bm_max_seq_blocks(const pa_block_manager* bm, const int64_t* seqs, int32_t n) {
+  if (!bm || n < 0 || (n > 0 && !seqs)) return PA_BM_ERR_INVALID_ARG;
+  int32_t width = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    auto it = bm->seqs.find(seqs[i]);
+    if (it == bm->seqs.end()) return PA_BM_ERR_UNKNOWN_SEQ;
+    if ((int32_t)it->second.blocks.size() > width) width = (int32_t)it->second.blocks.size();
+  }
+  return width;
+}
+
 int pa_bm_build_tables(const pa_block_manager* bm, const int64_t* seqs, int32_t n, int32_t width,
                        int32_t* tables_out, int32_t* lens_out) {
   if (!bm || n < 0 || width < 0 || (n > 0 && (!seqs || !tables_out || !lens_out))) return PA_BM_ERR_INVALID_ARG;
