@@ -58,10 +58,14 @@ def measured_peaks():
         return None
 
 
+# sources that define the decode call's kernels and launch configuration
+KERNEL_SOURCES = ("pa_api.cu", "pa_decode_tc.cu", "pa_device.cuh", "pa_internal.h", "pa_merge_and_cache.cu")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_32_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in KERNEL_SOURCES:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
