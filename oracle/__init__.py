@@ -48,7 +48,7 @@ def _load(path: str) -> ctypes.CDLL:
     L.pao_key_offset_prior.restype = i64
     L.pao_value_offset_prior.argtypes = [i64, i64, i64, i64, i32, i32, i32]
     L.pao_value_offset_prior.restype = i64
-    L.pao_attention.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp] + [i32] * 7 + [dbl, i32, i32]
+    L.pao_attention.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp] + [i32] * 7 + [dbl, i32, i32, vp]
     L.pao_attention.restype = i32
     L.pao_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32]
     L.pao_reshape_and_cache.restype = i32
@@ -126,12 +126,13 @@ def value_offset_prior(block, head, slot, d, num_kv_heads, block_size, head_size
 
 def paged_attention(q, k_cache, v_cache, block_tables, seq_lens, *, dtype: str, num_kv_heads: int,
                     block_size: int, scale: float, layout: str = "ours", partition_size: int = 0,
-                    threads: int = 0) -> np.ndarray:
+                    threads: int = 0, alibi_slopes=None) -> np.ndarray:
     """out[s, h, :] = softmax(scale * q[s,h] . K_s^T) V_s, in float64.
 
     q: [N, Hq, D]; k_cache/v_cache: the whole pool in ``layout``;
     block_tables: int32 [N, M]; seq_lens: int32 [N].
     partition_size > 0 evaluates the partitioned form with the log-sum-exp merge.
+    alibi_slopes: optional per-query-head slopes; score_i += slope * (i - (L - 1)).
     """
     q = np.ascontiguousarray(q)
     _check_storage(q, dtype, "q")
@@ -144,9 +145,13 @@ def paged_attention(q, k_cache, v_cache, block_tables, seq_lens, *, dtype: str, 
     per_block = num_kv_heads * block_size * D
     num_blocks = k_cache.size // per_block
     out = np.zeros((N, Hq, D), dtype=np.float64)
+    slopes = None if alibi_slopes is None else np.ascontiguousarray(alibi_slopes, dtype=np.float64)
+    if slopes is not None and slopes.shape != (Hq,):
+        raise ValueError("alibi_slopes must have one entry per query head")
     rc = lib().pao_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), DTYPE_CODE[dtype],
                              LAYOUT_CODE[layout], _ptr(bt), _ptr(sl), N, Hq, num_kv_heads, D, block_size, M,
-                             num_blocks, float(scale), int(partition_size), int(threads))
+                             num_blocks, float(scale), int(partition_size), int(threads),
+                             None if slopes is None else _ptr(slopes))
     if rc != 0:
         raise OracleError(f"pao_attention failed: {rc}")
     return out

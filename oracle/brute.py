@@ -33,8 +33,11 @@ def _flat_values(arr, dtype: str) -> list[float]:
 
 
 def paged_attention(q, k_cache, v_cache, block_tables, seq_lens, *, dtype: str, num_kv_heads: int,
-                    block_size: int, scale: float) -> list:
-    """Nested lists out[s][h][d]; cache layout [blocks][kv_heads][block_size][head_size]."""
+                    block_size: int, scale: float, alibi_slopes=None) -> list:
+    """Nested lists out[s][h][d]; cache layout [blocks][kv_heads][block_size][head_size].
+    With alibi_slopes, score i of head h gains slope_h * (i - (L - 1)) (linear
+    bias towards the query's own position, read from the per-head alibi_slopes
+    of "vLLM 核心工程深度剖析", section "3.1 Kernel 签名与分块策略")."""
     N, Hq, D = q.shape
     G = Hq // num_kv_heads
     qf = _flat_values(q, dtype)
@@ -62,6 +65,8 @@ def paged_attention(q, k_cache, v_cache, block_tables, seq_lens, *, dtype: str, 
                 per_head.append([0.0] * D)
                 continue
             scores = [scale * sum(a * b for a, b in zip(qv, k)) for k in keys]
+            if alibi_slopes is not None:
+                scores = [x + float(alibi_slopes[h]) * (i - (L - 1)) for i, x in enumerate(scores)]
             mx = max(scores)
             ex = [math.exp(x - mx) for x in scores]
             den = sum(ex)

@@ -32,6 +32,12 @@
  *       - "常見問題" (FAQ): paging changes only where K/V are stored, never
  *         the attention result.
  *
+ * Optional ALiBi: the kernel signature of [P3 "3.1"] carries per-head
+ * `alibi_slopes` without defining their use.  The reading taken is the
+ * standard linear bias of the query (at position L-1) towards key i:
+ * s_i += slope_h * (i - (L - 1)), i.e. zero for the newest token and
+ * increasingly negative for older ones (positive slopes).
+ *
  * Layout codes: PAO_LAYOUT_OURS is [blocks][kv_heads][B][head_size], dense.
  * PAO_LAYOUT_PRIOR is the [P1] prior-art pair above, kept to pin the address
  * arithmetic against the page's worked example.
@@ -143,6 +149,7 @@ typedef struct {
   const int32_t* seq_lens;
   int N, Hq, Hkv, D, B, M, num_blocks;
   double scale;
+  const double* alibi; /* nullable: one slope per query head */
 } pao_problem;
 
 /* Scores s_i = scale * <q, k_i> for tokens [t0, t1) of one (seq, query head),
@@ -163,6 +170,7 @@ static int gather_scores(const pao_problem* p, int s, int h, int64_t t0, int64_t
       dot += qd * kd;
     }
     scores[i - t0] = p->scale * dot;
+    if (p->alibi) scores[i - t0] += p->alibi[h] * (double)(i - (p->seq_lens[s] - 1));
     blocks[i - t0] = blk;
     slots[i - t0] = off;
   }
@@ -267,8 +275,9 @@ static int check_problem(const pao_problem* p) {
 /* partition_size <= 0: unsplit definition; > 0: partitioned form + merge. */
 int pao_attention(double* out, const void* q, const void* k_cache, const void* v_cache, int dtype, int layout,
                   const int32_t* block_tables, const int32_t* seq_lens, int N, int Hq, int Hkv, int D, int B, int M,
-                  int num_blocks, double scale, int partition_size, int threads) {
-  pao_problem p = {q, k_cache, v_cache, dtype, layout, block_tables, seq_lens, N, Hq, Hkv, D, B, M, num_blocks, scale};
+                  int num_blocks, double scale, int partition_size, int threads, const double* alibi_slopes) {
+  pao_problem p = {q, k_cache, v_cache, dtype, layout, block_tables, seq_lens, N,
+                   Hq, Hkv, D, B, M, num_blocks, scale, alibi_slopes};
   int rc = check_problem(&p);
   if (rc != PAO_OK || !out) return rc != PAO_OK ? rc : PAO_BAD_ARG;
   int64_t total = (int64_t)N * Hq;

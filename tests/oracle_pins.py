@@ -336,9 +336,33 @@ def pin_bad_block_rejected():
     raise AssertionError("out-of-range block id was accepted")
 
 
+def pin_alibi():
+    """ALiBi (per-head slope, score_i += slope * (i - (L - 1))): zero slopes change
+    nothing, the C oracle equals the pure-Python evaluation, a steep slope leaves
+    only the newest token, and the partitioned form still equals the unsplit one."""
+    w = small_case(101, dtype="f16", N=3, Hq=4, Hkv=2, D=8, B=4, lens=[1, 9, 23])
+    base = _attn(w)
+    assert np.array_equal(_attn(w, alibi_slopes=np.zeros(4)), base)
+    slopes = np.array([0.5, -0.25, 2.0, 0.125])
+    got = _attn(w, alibi_slopes=slopes)
+    ref = np.array(brute.paged_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, dtype=w.dtype,
+                                         num_kv_heads=w.num_kv_heads, block_size=w.block_size, scale=w.scale,
+                                         alibi_slopes=slopes))
+    assert np.max(np.abs(got - ref)) < 1e-12
+    assert np.max(np.abs(got - base)) > 1e-3          # the bias really acts
+    steep = _attn(w, alibi_slopes=np.full(4, 1e4))
+    for s, L in enumerate(w.seq_lens):
+        blk, off = int(w.block_tables[s, (L - 1) // 4]), (L - 1) % 4
+        newest = O.to_f64(w.v_cache[blk, :, off, :], "f16")       # [Hkv, D]
+        for h in range(4):
+            assert np.max(np.abs(steep[s, h] - newest[h // 2])) < 1e-12
+    for P in (4, 8):
+        assert np.max(np.abs(_attn(w, alibi_slopes=slopes, partition_size=P) - got)) < 1e-12
+
+
 ALL_PINS = [
     pin_f16_decoding, pin_bf16_decoding, pin_35_token_example, pin_worked_offset, pin_prior_layout_offsets,
     pin_prior_layout_attention, pin_slot_round_trip, pin_padding_slots_skipped, pin_identity_tables_vs_contiguous,
     pin_permutation_invariance, pin_shared_prefix_equals_private, pin_cow_isolation, pin_brute_force,
-    pin_special_cases, pin_split_identity, pin_zero_length, pin_bad_block_rejected,
+    pin_special_cases, pin_split_identity, pin_zero_length, pin_bad_block_rejected, pin_alibi,
 ]

@@ -33,6 +33,8 @@ MUTANTS = [
     ("copy_direction", "int32_t src = pairs[2 * i], dst = pairs[2 * i + 1];",
      "int32_t dst = pairs[2 * i], src = pairs[2 * i + 1];"),
     ("padding_written", "if (slot < 0) continue;", "if (slot < 0) slot = -slot;"),
+    ("alibi_sign", "p->alibi[h] * (double)(i - (p->seq_lens[s] - 1))", "p->alibi[h] * (double)((p->seq_lens[s] - 1) - i)"),
+    ("alibi_kv_head_slope", "p->alibi[h] * (double)(i", "p->alibi[h / (p->Hq / p->Hkv)] * (double)(i"),
 ]
 
 
