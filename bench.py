@@ -181,10 +181,13 @@ def all_max(x: float, world: int) -> float:
 class DeviceStep:
     """All device buffers of one workload and the library calls of one step."""
 
-    def __init__(self, w: W.Workload, device):
+    def __init__(self, w: W.Workload, device, alibi: bool = False):
         import torch
         import paged_kv_cache_32_gb300 as pa
         self.pa, self.w, self.dev = pa, w, device
+        # ALiBi: the usual geometric per-head slopes 2^(-8 i / H)
+        self.alibi = (torch.tensor([2.0 ** (-8.0 * (i + 1) / w.num_q_heads) for i in range(w.num_q_heads)],
+                                   dtype=torch.float32, device=device) if alibi else None)
         tdt = getattr(torch, TORCH_DT[w.dtype])
         self.k, self.v = W.device_caches(w, device)
         self.desc = pa.cache_desc(self.k)
@@ -226,7 +229,7 @@ class DeviceStep:
         self.pa.pa_decode(self.out if out is None else out, self.q if q is None else q, self.k, self.v,
                           self.tables if tables is None else tables, self.lens if lens is None else lens,
                           self.w.scale, partition_size=self.w.partition_size, workspace=self.ws,
-                          err_flag=self.err, stream=stream, desc=self.desc)
+                          err_flag=self.err, stream=stream, desc=self.desc, alibi_slopes=self.alibi)
 
     def decode_bytes(self) -> int:
         """Algorithmic HBM bytes of one pa_decode call: K+V of every token, q in,
@@ -431,8 +434,9 @@ def run_ours(args, world, rank, local):
         for name in args.extra:
             if name == args.workload:
                 continue
-            wx = W.WORKLOADS[name](materialize=False)
-            dx = DeviceStep(wx, device)
+            base, _, suffix = name.partition("+")
+            wx = W.WORKLOADS[base](materialize=False)
+            dx = DeviceStep(wx, device, alibi=suffix == "alibi")
             msx, dmx, _, _ = time_device(dx, max(5, args.steps), args.warmup, 1)
             dm = statistics.mean(dmx)
             ab = dx.decode_bytes()
@@ -497,8 +501,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mha_f16", choices=sorted(W.WORKLOADS))
-    ap.add_argument("--extra", nargs="*", default=["gqa_bf16", "long_bf16_b16", "long_bf16_b32", "long_bf16_b64",
-                                                   "shared_prefix_f16"])
+    ap.add_argument("--extra", nargs="*", default=["gqa_bf16", "gqa_bf16+alibi", "long_bf16_b16", "long_bf16_b32",
+                                                   "long_bf16_b64", "shared_prefix_f16"])
     ap.add_argument("--no-extra", action="store_true", help="time only the headline workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--partition", type=int, default=None,

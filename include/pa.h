@@ -108,6 +108,24 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
               const pa_cache_desc* cache, float scale, int32_t partition_size, void* workspace,
               size_t workspace_bytes, int32_t* err_flag, void* stream);
 
+/*
+ * pa_decode_ex - pa_decode with optional extensions (options may be NULL, which
+ * is exactly pa_decode).
+ *   alibi_slopes  nullable device fp32 [num_q_heads], 4-byte aligned.  The kernel
+ *                 signature of [P3 "3.1"] carries per-head ALiBi slopes without
+ *                 defining them; the reading implemented is the standard linear
+ *                 bias towards the query's own position: score_i of head h gains
+ *                 alibi_slopes[h] * (i - (seq_lens[s] - 1)).
+ */
+typedef struct {
+  const float* alibi_slopes;
+} pa_decode_options;
+
+int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                 const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                 const pa_cache_desc* cache, float scale, int32_t partition_size, void* workspace,
+                 size_t workspace_bytes, int32_t* err_flag, void* stream, const pa_decode_options* options);
+
 /* Partition size pa_decode uses for these arguments (resolves 0 to the default);
  * returns a value >= max_blocks_per_seq * block_size when no split happens, or a
  * negative PA_ERR_* code for invalid arguments. */

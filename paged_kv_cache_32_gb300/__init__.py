@@ -22,8 +22,12 @@ PA_OK = 0
 PA_DEVERR = {0: "none", 1: "block id out of range", 2: "slot out of range", 3: "copy pair id out of range",
              4: "wait on an asynchronous copy timed out"}
 
-EXPORTED = ("pa_decode", "pa_decode_partition_size", "pa_decode_workspace_size", "pa_reshape_and_cache",
+EXPORTED = ("pa_decode", "pa_decode_ex", "pa_decode_partition_size", "pa_decode_workspace_size", "pa_reshape_and_cache",
             "pa_copy_blocks", "pa_status_string", "pa_version", "pa_decode_noalloc")
+
+
+class pa_decode_options(ctypes.Structure):
+    _fields_ = [("alibi_slopes", ctypes.c_void_p)]
 
 
 class pa_cache_desc(ctypes.Structure):
@@ -55,6 +59,8 @@ def lib() -> ctypes.CDLL:
         desc_p = ctypes.POINTER(pa_cache_desc)
         L.pa_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, desc_p, ctypes.c_float, i32, vp, sz, vp, vp]
         L.pa_decode.restype = ctypes.c_int
+        L.pa_decode_ex.argtypes = L.pa_decode.argtypes + [ctypes.POINTER(pa_decode_options)]
+        L.pa_decode_ex.restype = ctypes.c_int
         L.pa_decode_partition_size.argtypes = [i32, desc_p, i32]
         L.pa_decode_partition_size.restype = i32
         L.pa_decode_workspace_size.argtypes = [i32, i32, i32, desc_p, i32]
@@ -141,13 +147,15 @@ def pa_decode_workspace_size(num_seqs: int, num_q_heads: int, max_blocks_per_seq
 
 
 def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale: float, partition_size: int = 0,
-              workspace=None, err_flag=None, stream=None, desc: pa_cache_desc | None = None) -> None:
+              workspace=None, err_flag=None, stream=None, desc: pa_cache_desc | None = None,
+              alibi_slopes=None) -> None:
     """out[s, h] = softmax(scale * q[s, h] K_s^T) V_s over seq_lens[s] paged tokens.
 
     out, q: [num_seqs, num_q_heads, head_size] (cache dtype); block_tables: int32
     [num_seqs, max_blocks_per_seq]; seq_lens: int32 [num_seqs].  ``workspace`` is a
     uint8 device tensor of at least pa_decode_workspace_size(...) bytes; when None
-    and one is needed, it is allocated with torch.
+    and one is needed, it is allocated with torch.  ``alibi_slopes``: optional
+    float32 device tensor [num_q_heads] (calls pa_decode_ex).
     """
     desc = desc or cache_desc(k_cache)
     for t, n in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"),
@@ -160,10 +168,15 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale: float, pa
         import torch
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    status = lib().pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(seq_lens),
-                             num_seqs, num_q_heads, max_blocks, ctypes.byref(desc), float(scale),
-                             int(partition_size), _ptr(workspace), ws_bytes, _ptr(err_flag), _stream(stream))
-    _check(status, "pa_decode")
+    args = (_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(seq_lens), num_seqs,
+            num_q_heads, max_blocks, ctypes.byref(desc), float(scale), int(partition_size), _ptr(workspace), ws_bytes,
+            _ptr(err_flag), _stream(stream))
+    if alibi_slopes is None:
+        _check(lib().pa_decode(*args), "pa_decode")
+    else:
+        _dense(alibi_slopes, "alibi_slopes")
+        opts = pa_decode_options(_ptr(alibi_slopes))
+        _check(lib().pa_decode_ex(*args, ctypes.byref(opts)), "pa_decode_ex")
 
 
 def pa_reshape_and_cache(k_cache, v_cache, key, value, slot_mapping, err_flag=None, stream=None,

@@ -126,6 +126,14 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
               const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
               const pa_cache_desc* cache, float scale, int32_t partition_size, void* workspace,
               size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  return pa_decode_ex(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_q_heads, max_blocks_per_seq,
+                      cache, scale, partition_size, workspace, workspace_bytes, err_flag, stream, nullptr);
+}
+
+int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                 const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                 const pa_cache_desc* cache, float scale, int32_t partition_size, void* workspace,
+                 size_t workspace_bytes, int32_t* err_flag, void* stream, const pa_decode_options* options) {
   int rc = check_cache(cache);
   if (rc != PA_OK) return rc;
   if (num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq < 0) return PA_ERR_INVALID_ARG;
@@ -145,6 +153,8 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
   const uintptr_t qalign = cache->dtype == PA_F32 ? 4 : 16;
   if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, qalign) || !aligned(out, 4))
     return PA_ERR_MISALIGNED;
+  const float* alibi = options != nullptr ? options->alibi_slopes : nullptr;
+  if (alibi != nullptr && !aligned(alibi, 4)) return PA_ERR_MISALIGNED;
   const int G = num_q_heads / cache->num_kv_heads;
   const int head_groups = (G + 7) / 8;
   const long long grid = (long long)num_seqs * cache->num_kv_heads * head_groups * pmax;
@@ -174,6 +184,7 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
   p.partition_size = part;
   p.pmax = pmax;
   p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+  p.alibi = alibi;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;

@@ -62,6 +62,10 @@ __global__ void __launch_bounds__(NW * 32)
                                                                   lane * VEC + e]
                               : 0.f;
   }
+  float bias[8];  // ALiBi slopes in log2 units (0: no bias)
+#pragma unroll
+  for (int gh = 0; gh < 8; ++gh)
+    bias[gh] = (p.alibi != nullptr && gh < gcount) ? __ldg(p.alibi + hq0 + gh) * 1.4426950408889634f : 0.f;
   float m[8], l[8], o[8][VEC];
 #pragma unroll
   for (int gh = 0; gh < 8; ++gh) {
@@ -92,7 +96,7 @@ __global__ void __launch_bounds__(NW * 32)
       for (int e = 0; e < VEC; ++e) dot = fmaf(qv[gh][e], kv[e], dot);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-      const float sc = dot * p.scale_log2;
+      const float sc = fmaf(bias[gh], (float)(t - (L - 1)), dot * p.scale_log2);
       const float mn = fmaxf(m[gh], sc);
       const float al = fast_exp2(m[gh] - mn);
       const float pe = fast_exp2(sc - mn);

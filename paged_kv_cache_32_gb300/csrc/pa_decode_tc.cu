@@ -71,6 +71,7 @@ struct Shape {
 // One work item.
 struct Item {
   int s, hkv, hq0, gcount, part;
+  int L;           // tokens of the sequence
   int t_end;       // end of this partition
   int j0;          // first slab (16 tokens) of the partition
   int nslabs;
@@ -89,6 +90,7 @@ __device__ __forceinline__ bool decode_item(const DecodeParams& p, int id, Item&
   it.gcount = min(8, G - hg * 8);
   int L = __ldg(p.seq_lens + it.s);
   L = max(0, min(L, p.max_blocks * p.block_size));
+  it.L = L;
   const int t_begin = it.part * p.partition_size;
   if (L == 0) {  // an empty sequence: partition 0 writes a zero row
     it.t_end = 0;
@@ -122,11 +124,14 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
 
 // One 16-token slab: S^T = K Q^T, online softmax update, O^T += V^T P^T.
 // kst / vst: the slab's swizzled K and V tiles; nvalid: tokens of the slab
-// inside the partition (1..16).
+// inside the partition (1..16).  ALiBi: bias_a / bias_b are the slopes of
+// heads 2q4 / 2q4+1 in log2 units (0 without ALiBi) and rel0 is the position
+// of the slab's first token relative to the query, i.e. first token - (L - 1).
 template <typename T, int D>
 __device__ __forceinline__ void process_slab(const uint8_t* kst, const uint8_t* vst, int nvalid,
                                              const uint32_t (&qf)[D / 16][2], float (&o)[D / 16][4], float& m_a,
-                                             float& m_b, float& l_a, float& l_b, int lane, float sl2) {
+                                             float& m_b, float& l_a, float& l_b, int lane, float sl2, float bias_a,
+                                             float bias_b, float rel0) {
   constexpr int KSTEPS = D / 16;
   constexpr int BOX_BYTES = kTcSlabTokens * 128;
   const int g = lane >> 2, q4 = lane & 3;
@@ -148,8 +153,9 @@ __device__ __forceinline__ void process_slab(const uint8_t* kst, const uint8_t* 
     }
   }
   // scores: (token g, head 2q4), (token g, head 2q4+1), (token g+8, head 2q4), (token g+8, head 2q4+1)
-  float s0 = (sc[0] + sd[0]) * sl2, s1 = (sc[1] + sd[1]) * sl2;
-  float s2 = (sc[2] + sd[2]) * sl2, s3 = (sc[3] + sd[3]) * sl2;
+  const float r_lo = rel0 + (float)g, r_hi = r_lo + 8.f;  // tokens g and g + 8 of the slab
+  float s0 = fmaf(bias_a, r_lo, (sc[0] + sd[0]) * sl2), s1 = fmaf(bias_b, r_lo, (sc[1] + sd[1]) * sl2);
+  float s2 = fmaf(bias_a, r_hi, (sc[2] + sd[2]) * sl2), s3 = fmaf(bias_b, r_hi, (sc[3] + sd[3]) * sl2);
   if (nvalid < 16) {
     if (g >= nvalid) s0 = s1 = -INFINITY;
     if (g + 8 >= nvalid) s2 = s3 = -INFINITY;
@@ -265,6 +271,14 @@ __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
     }
   }
 
+  // ALiBi slopes of this lane's two heads, in log2 units (0: no bias)
+  float bias_a = 0.f, bias_b = 0.f;
+  if (p.alibi != nullptr) {
+    constexpr float kLog2e = 1.4426950408889634f;
+    if (2 * q4 < it.gcount) bias_a = __ldg(p.alibi + it.hq0 + 2 * q4) * kLog2e;
+    if (2 * q4 + 1 < it.gcount) bias_b = __ldg(p.alibi + it.hq0 + 2 * q4 + 1) * kLog2e;
+  }
+
   uint32_t valid_mask = 0;  // bit `stage`: the slab in that buffer was loaded
   auto issue = [&](int k) {  // called by the whole warp, k increasing
     if ((k >> 5) != pb_batch) {
@@ -306,9 +320,11 @@ __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
     const int stage = k % NS;
     if (!__all_sync(0xffffffffu, wait_phase(&bars[stage], (k / NS) & 1, abort_flag))) break;
     if ((valid_mask >> stage) & 1u) {
-      const int nvalid = min(S::SB, it.t_end - (it.j0 + warp + k * NW) * S::SB);
+      const int tok0 = (it.j0 + warp + k * NW) * S::SB;
+      const int nvalid = min(S::SB, it.t_end - tok0);
       const uint8_t* kst = ring + stage * S::SLAB_BYTES;
-      process_slab<T, D>(kst, kst + S::NBOX * S::BOX_BYTES, nvalid, qf, o, m_a, m_b, l_a, l_b, lane, p.scale_log2);
+      process_slab<T, D>(kst, kst + S::NBOX * S::BOX_BYTES, nvalid, qf, o, m_a, m_b, l_a, l_b, lane, p.scale_log2,
+                         bias_a, bias_b, (float)(tok0 - (it.L - 1)));
     }
     __syncwarp();
     if (k + NS < n_my) issue(k + NS);

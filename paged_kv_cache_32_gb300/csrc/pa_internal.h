@@ -25,6 +25,7 @@ struct DecodeParams {
   int32_t partition_size;     // tokens per partition (multiple of B)
   int32_t pmax;               // partitions per sequence in the grid
   float scale_log2;           // scale * log2(e)
+  const float* alibi;         // nullable [Hq]: score_i += slope_h * (i - (L - 1))
 };
 
 // Kernel launchers (return the cudaGetLastError of the launch).

@@ -163,3 +163,49 @@ def test_cow_leaves_other_branches_untouched_on_gpu():
     assert np.array_equal(k[keep], w.k_cache.view(np.uint16)[keep])
     # 1020 = 63 * 16 + 12: the copied block is partial and the first suffix tokens land in the copy
     assert dsts & written
+
+
+# ---------------------------------------------------------------- ALiBi (pa_decode_ex)
+def alibi_slopes(num_heads: int) -> np.ndarray:
+    """The usual geometric slopes 2^(-8 i / H), i = 1..H (a choice of inputs; any slopes are valid)."""
+    return (2.0 ** (-8.0 * np.arange(1, num_heads + 1) / num_heads)).astype(np.float32)
+
+
+@pytest.mark.parametrize("case", [
+    ("f16", 8, 8, 128, 16, [1, 15, 33, 300]),
+    ("bf16", 16, 2, 128, 32, [2, 64, 65, 700]),
+    ("f32", 8, 2, 64, 16, [1, 17, 90, 600]),
+], ids=lambda c: f"{c[0]}-Hq{c[1]}-Hkv{c[2]}-D{c[3]}-B{c[4]}")
+@pytest.mark.parametrize("partition", [0, "one_block"])
+def test_alibi_small_cases(case, partition):
+    import torch
+    dtype, Hq, Hkv, D, B, lens = case
+    w = W.build_decode("alibi", seed=zlib.crc32(repr(case).encode()) % 10000, dtype=dtype, seq_lens=lens,
+                       num_q_heads=Hq, num_kv_heads=Hkv, head_size=D, block_size=B, pool_factor=1.3)
+    slopes = alibi_slopes(Hq)
+    g = GpuStep(w)
+    part = 0 if partition == 0 else B
+    need = g.pa.pa_decode_workspace_size(w.num_seqs, Hq, w.max_blocks_per_seq, g.desc, part)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+    g.pa.pa_decode(g.out, g.q, g.k, g.v, g.tables, g.lens, w.scale, partition_size=part, workspace=ws,
+                   err_flag=g.err, desc=g.desc, alibi_slopes=torch.from_numpy(slopes).cuda())
+    torch.cuda.synchronize()
+    ref = O.paged_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, dtype=dtype, num_kv_heads=Hkv,
+                            block_size=B, scale=w.scale, alibi_slopes=slopes.astype(np.float64))
+    ok, err, _ = within_bound(out_f64(g.out), ref, dtype)
+    assert ok and int(g.err.item()) == 0, f"max abs err {err}"
+
+
+def test_alibi_gqa_bf16_full():
+    import torch
+    w = W.gqa_bf16()
+    slopes = alibi_slopes(w.num_q_heads)
+    g = GpuStep(w)
+    g.pa.pa_decode(g.out, g.q, g.k, g.v, g.tables, g.lens, w.scale, workspace=g.ws, err_flag=g.err, desc=g.desc,
+                   alibi_slopes=torch.from_numpy(slopes).cuda())
+    torch.cuda.synchronize()
+    ref = O.paged_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, dtype="bf16",
+                            num_kv_heads=w.num_kv_heads, block_size=w.block_size, scale=w.scale,
+                            alibi_slopes=slopes.astype(np.float64))
+    ok, err, _ = within_bound(out_f64(g.out), ref, "bf16")
+    assert ok and int(g.err.item()) == 0, f"max abs err {err}"
