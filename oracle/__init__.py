@@ -50,6 +50,8 @@ def _load(path: str) -> ctypes.CDLL:
     L.pao_value_offset_prior.restype = i64
     L.pao_attention.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp] + [i32] * 7 + [dbl, i32, i32, vp]
     L.pao_attention.restype = i32
+    L.pao_prefill_attention.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp] + [i32] * 7 + [dbl, i32]
+    L.pao_prefill_attention.restype = i32
     L.pao_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32]
     L.pao_reshape_and_cache.restype = i32
     L.pao_copy_blocks.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32]
@@ -154,6 +156,36 @@ def paged_attention(q, k_cache, v_cache, block_tables, seq_lens, *, dtype: str, 
                              None if slopes is None else _ptr(slopes))
     if rc != 0:
         raise OracleError(f"pao_attention failed: {rc}")
+    return out
+
+
+def prefill_attention(q, k_cache, v_cache, block_tables, seq_lens, query_start, *, dtype: str, num_kv_heads: int,
+                      block_size: int, scale: float, threads: int = 0) -> np.ndarray:
+    """Chunked prefill over the paged cache, float64 [total_q, Hq, D].
+
+    q: packed [total_q, Hq, D]; query_start: int32 [N + 1] offsets of each
+    sequence's chunk in q; seq_lens: int32 [N] cached tokens including the
+    chunk.  Query j of sequence s attends causally to cache positions
+    0 .. seq_lens[s] - n_s + j.
+    """
+    q = np.ascontiguousarray(q)
+    _check_storage(q, dtype, "q")
+    _check_storage(k_cache, dtype, "k_cache")
+    _check_storage(v_cache, dtype, "v_cache")
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    qs = np.ascontiguousarray(query_start, dtype=np.int32)
+    T, Hq, D = q.shape
+    N = len(sl)
+    assert qs.shape == (N + 1,) and qs[-1] == T
+    M = bt.shape[1] if bt.ndim == 2 else 0
+    num_blocks = k_cache.size // (num_kv_heads * block_size * D)
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    rc = lib().pao_prefill_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), DTYPE_CODE[dtype], _ptr(bt),
+                                     _ptr(sl), _ptr(qs), N, Hq, num_kv_heads, D, block_size, M, num_blocks,
+                                     float(scale), int(threads))
+    if rc != 0:
+        raise OracleError(f"pao_prefill_attention failed: {rc}")
     return out
 
 

@@ -73,3 +73,21 @@ def paged_attention(q, k_cache, v_cache, block_tables, seq_lens, *, dtype: str, 
             per_head.append([sum(e * v[d] for e, v in zip(ex, values)) / den for d in range(D)])
         out.append(per_head)
     return out
+
+
+def prefill_attention(q, k_cache, v_cache, block_tables, seq_lens, query_start, *, dtype: str, num_kv_heads: int,
+                      block_size: int, scale: float) -> list:
+    """Chunked prefill by brute force: query j of sequence s (chunk of n_s tokens
+    at the end of its seq_lens[s] cached tokens) attends to cache positions
+    0 .. seq_lens[s] - n_s + j, evaluated as a one-query problem each."""
+    import numpy as np
+    out = []
+    for s in range(len(seq_lens)):
+        n = int(query_start[s + 1]) - int(query_start[s])
+        for j in range(n):
+            t = int(query_start[s]) + j
+            pos = int(seq_lens[s]) - n + j
+            res = paged_attention(q[t:t + 1], k_cache, v_cache, [list(block_tables[s])], [pos + 1], dtype=dtype,
+                                  num_kv_heads=num_kv_heads, block_size=block_size, scale=scale)
+            out.append(res[0])
+    return out

@@ -301,6 +301,58 @@ int pao_attention(double* out, const void* q, const void* k_cache, const void* v
   return err;
 }
 
+/* ---------- prefill (chunked) attention ---------- */
+
+/* The prefill step reads the same paged cache as decode ("PagedAttention 详解：
+ * 缓存的存储结构", section "使用流程": prompt blocks that hit the prefix cache
+ * "directly take part in the attention computation" and only the missed
+ * blocks' K/V are computed and written through slot_mapping; "vLLM 核心工程深度
+ * 剖析", section "6.1": long prompts are prefilled in chunks).  Sequence s holds
+ * seq_lens[s] tokens in the cache, the last n_s = query_start[s+1] -
+ * query_start[s] of which are this chunk's queries.  Query j of the chunk sits
+ * at position p = seq_lens[s] - n_s + j and attends causally to the cached
+ * tokens 0..p:  out = softmax_i(scale * q . k_i) v_i, i in [0, p].
+ * q and out are packed [total_query_tokens][Hq][D]. */
+int pao_prefill_attention(double* out, const void* q, const void* k_cache, const void* v_cache, int dtype,
+                          const int32_t* block_tables, const int32_t* seq_lens, const int32_t* query_start, int N,
+                          int Hq, int Hkv, int D, int B, int M, int num_blocks, double scale, int threads) {
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start) return PAO_BAD_ARG;
+  if (N < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || B <= 0 || M < 0) return PAO_BAD_ARG;
+  for (int s = 0; s < N; ++s) {
+    int32_t n = query_start[s + 1] - query_start[s];
+    if (n < 0 || n > seq_lens[s] || (int64_t)seq_lens[s] > (int64_t)M * B) return PAO_BAD_ARG;
+  }
+  const int64_t total_q = query_start[N];
+  int err = PAO_OK;
+#ifdef _OPENMP
+  if (threads <= 0) threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(threads)
+#endif
+  for (int64_t th = 0; th < total_q * Hq; ++th) {
+    const int64_t t = th / Hq;
+    const int h = (int)(th % Hq);
+    int s = 0;
+    while (query_start[s + 1] <= t) ++s; /* the sequence that owns query token t */
+    const int64_t n = query_start[s + 1] - query_start[s];
+    const int64_t pos = seq_lens[s] - n + (t - query_start[s]);
+    /* a one-sequence problem over the cache prefix [0, pos]: the decode definition with L = pos + 1 */
+    const int32_t len = (int32_t)(pos + 1);
+    pao_problem p = {(const char*)q + (size_t)t * Hq * D * elem_size(dtype) - (size_t)0,
+                     k_cache, v_cache, dtype, PAO_LAYOUT_OURS, block_tables + (int64_t)s * M, &len,
+                     1, Hq, Hkv, D, B, M, num_blocks, scale, NULL};
+    double* o = out + (size_t)th * D;
+    int r = attend_one(&p, 0, h, o);
+    if (r != PAO_OK) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+      err = r;
+    }
+  }
+  (void)threads;
+  return err;
+}
+
 /* ---------- write operations ---------- */
 
 /* [P1 "写入新 K/V"]: block = slot / B, offset = slot % B; token t's key and

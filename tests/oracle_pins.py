@@ -360,9 +360,78 @@ def pin_alibi():
         assert np.max(np.abs(_attn(w, alibi_slopes=slopes, partition_size=P) - got)) < 1e-12
 
 
+def _prefill_case(seed, dtype="f32", lens=(9, 20, 13), chunks=(9, 6, 1), Hq=4, Hkv=2, D=8, B=4):
+    w = W.build_decode(f"pf{seed}", seed=seed, dtype=dtype, seq_lens=list(lens), num_q_heads=Hq, num_kv_heads=Hkv,
+                       head_size=D, block_size=B, pool_factor=1.5)
+    qs = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    q = W.normal(np.random.default_rng(seed + 1), (int(qs[-1]), Hq, D), dtype)
+    return w, q, qs
+
+
+def _prefill(w, q, qs, **kw):
+    return O.prefill_attention(q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, qs, dtype=w.dtype,
+                               num_kv_heads=w.num_kv_heads, block_size=w.block_size, scale=w.scale, **kw)
+
+
+def pin_prefill():
+    """Chunked prefill: one query = decode over the whole context (bit-identical),
+    a chunk's last query = decode, the query at position 0 returns v_0, and the
+    pure-Python evaluation agrees to 1e-12."""
+    w, q, qs = _prefill_case(121, "f16", lens=(9, 20, 13), chunks=(9, 6, 1))
+    got = _prefill(w, q, qs)
+    ref = np.array(brute.prefill_attention(q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, qs, dtype=w.dtype,
+                                           num_kv_heads=w.num_kv_heads, block_size=w.block_size, scale=w.scale))
+    assert np.max(np.abs(got - ref)) < 1e-12
+    # the last query of every chunk is the decode query of that sequence
+    last = q[qs[1:] - 1]
+    dec = O.paged_attention(last, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, dtype=w.dtype,
+                            num_kv_heads=w.num_kv_heads, block_size=w.block_size, scale=w.scale)
+    assert np.array_equal(got[qs[1:] - 1], dec)
+    # sequence 0's chunk starts at position 0: its first query sees token 0 only
+    blk = int(w.block_tables[0, 0])
+    v0 = O.to_f64(w.v_cache[blk, :, 0, :], w.dtype)
+    for h in range(w.num_q_heads):
+        assert np.array_equal(got[0, h], v0[h // 2])
+
+
+def pin_prefill_contiguous():
+    """With identity tables the chunk equals causal attention over contiguous K/V
+    (numpy with an explicit causal mask, and torch SDPA with a boolean mask, fp64)."""
+    import torch
+    N, M, B, Hq, Hkv, D = 2, 4, 4, 4, 2, 8
+    lens, chunks = [13, 16], [5, 16]
+    fixed = {s: list(range(s * M, s * M + -(-L // B))) for s, L in enumerate(lens)}
+    w = W.build_decode("pfc", seed=131, dtype="f32", seq_lens=lens, num_q_heads=Hq, num_kv_heads=Hkv, head_size=D,
+                       block_size=B, num_blocks=N * M, fixed_tables=fixed, table_width=M)
+    tables = np.arange(N * M, dtype=np.int32).reshape(N, M)
+    qs = np.array([0, 5, 21], np.int32)
+    q = W.normal(np.random.default_rng(132), (21, Hq, D), "f32")
+    got = O.prefill_attention(q, w.k_cache, w.v_cache, tables, w.seq_lens, qs, dtype="f32", num_kv_heads=Hkv,
+                              block_size=B, scale=w.scale)
+    Kc = w.k_cache.astype(np.float64).reshape(N, M, Hkv, B, D).transpose(0, 2, 1, 3, 4).reshape(N, Hkv, M * B, D)
+    Vc = w.v_cache.astype(np.float64).reshape(N, M, Hkv, B, D).transpose(0, 2, 1, 3, 4).reshape(N, Hkv, M * B, D)
+    for s, (L, n) in enumerate(zip(lens, chunks)):
+        Q = q[qs[s]:qs[s + 1]].astype(np.float64)               # [n, Hq, D]
+        pos = np.arange(L - n, L)
+        mask = np.arange(L)[None, :] <= pos[:, None]             # [n, L]
+        for h in range(Hq):
+            sc = (Q[:, h] @ Kc[s, h // 2, :L].T) * w.scale
+            sc = np.where(mask, sc, -np.inf)
+            pr = np.exp(sc - sc.max(axis=1, keepdims=True))
+            ref = (pr / pr.sum(axis=1, keepdims=True)) @ Vc[s, h // 2, :L]
+            assert np.max(np.abs(got[qs[s]:qs[s + 1], h] - ref)) < 1e-12
+        qt = torch.from_numpy(Q.transpose(1, 0, 2)[None])                               # [1, Hq, n, D]
+        kt = torch.from_numpy(np.repeat(Kc[s, :, :L], 2, axis=0)[None])
+        vt = torch.from_numpy(np.repeat(Vc[s, :, :L], 2, axis=0)[None])
+        sd = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=torch.from_numpy(mask),
+                                                              scale=w.scale)[0].numpy().transpose(1, 0, 2)
+        assert np.max(np.abs(got[qs[s]:qs[s + 1]] - sd)) < 1e-12
+
+
 ALL_PINS = [
     pin_f16_decoding, pin_bf16_decoding, pin_35_token_example, pin_worked_offset, pin_prior_layout_offsets,
     pin_prior_layout_attention, pin_slot_round_trip, pin_padding_slots_skipped, pin_identity_tables_vs_contiguous,
     pin_permutation_invariance, pin_shared_prefix_equals_private, pin_cow_isolation, pin_brute_force,
-    pin_special_cases, pin_split_identity, pin_zero_length, pin_bad_block_rejected, pin_alibi,
+    pin_special_cases, pin_split_identity, pin_zero_length, pin_bad_block_rejected, pin_alibi, pin_prefill,
+    pin_prefill_contiguous,
 ]

@@ -34,6 +34,9 @@ MUTANTS = [
      "int32_t dst = pairs[2 * i], src = pairs[2 * i + 1];"),
     ("padding_written", "if (slot < 0) continue;", "if (slot < 0) slot = -slot;"),
     ("alibi_sign", "p->alibi[h] * (double)(i - (p->seq_lens[s] - 1))", "p->alibi[h] * (double)((p->seq_lens[s] - 1) - i)"),
+    ("prefill_causal_offset", "const int32_t len = (int32_t)(pos + 1);", "const int32_t len = (int32_t)(pos + 2);"),
+    ("prefill_query_origin", "const int64_t pos = seq_lens[s] - n + (t - query_start[s]);",
+     "const int64_t pos = seq_lens[s] - n + t;"),
     ("alibi_kv_head_slope", "p->alibi[h] * (double)(i", "p->alibi[h / (p->Hq / p->Hkv)] * (double)(i"),
 ]
 
