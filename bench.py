@@ -45,6 +45,8 @@ WORKLOAD_DESC = {
     "long_bf16_b16": "long bf16 split-KV: 8 seqs x 32768 tokens, 32 q / 8 kv heads, D 128, B 16, 512-token partitions",
     "long_bf16_b32": "long bf16 split-KV: 8 seqs x 32768 tokens, 32 q / 8 kv heads, D 128, B 32, 512-token partitions",
     "long_bf16_b64": "long bf16 split-KV: 8 seqs x 32768 tokens, 32 q / 8 kv heads, D 128, B 64, 512-token partitions",
+    "prefill_bf16": "chunked prefill bf16: 16 seqs, cached prefix U[0,2048] + chunk U[256,2048] tokens, 32 q / 8 kv "
+                    "heads, D 128, B 16, pool 1.2x needed, shuffled; chunk K/V appended, then causal attention",
 }
 TORCH_DT = {"f32": "float32", "f16": "float16", "bf16": "bfloat16"}
 
@@ -231,6 +233,9 @@ class DeviceStep:
                           self.w.scale, partition_size=self.w.partition_size, workspace=self.ws,
                           err_flag=self.err, stream=stream, desc=self.desc, alibi_slopes=self.alibi)
 
+    def attend(self, stream):
+        self.decode(stream)
+
     def decode_bytes(self) -> int:
         """Algorithmic HBM bytes of one pa_decode call: K+V of every token, q in,
         out, table entries, and the split-KV partial results (written then read)."""
@@ -245,13 +250,49 @@ class DeviceStep:
         return b
 
 
-def time_device(ds: DeviceStep, steps: int, warmup: int, world: int):
+class PrefillDeviceStep:
+    """Device buffers of a chunked-prefill workload and the calls of one step:
+    the chunk's K/V appended through slot_mapping, then prefill attention of the
+    chunk's queries over each whole sequence."""
+
+    def __init__(self, w: W.Workload, device):
+        import torch
+        import paged_kv_cache_32_gb300 as pa
+        self.pa, self.w, self.dev = pa, w, device
+        tdt = getattr(torch, TORCH_DT[w.dtype])
+        self.k, self.v = W.device_caches(w, device)
+        self.desc = pa.cache_desc(self.k)
+        gen = torch.Generator(device=device)
+        gen.manual_seed(int(w.info.get("seed", 0)) + 1)
+        T = w.num_query_tokens
+
+        def draw(heads):
+            return torch.randn((T, heads, w.head_size), generator=gen, device=device, dtype=torch.float32).to(tdt)
+        self.q, self.nk, self.nv = draw(w.num_q_heads), draw(w.num_kv_heads), draw(w.num_kv_heads)
+        self.slots = torch.from_numpy(w.slot_mapping).to(device)
+        self.tables = torch.from_numpy(w.block_tables).to(device)
+        self.lens = torch.from_numpy(w.seq_lens).to(device)
+        self.qs = torch.from_numpy(w.query_start).to(device)
+        self.out = torch.empty_like(self.q)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.max_q = int(np.diff(w.query_start).max())
+
+    def writes(self, stream):
+        self.pa.pa_reshape_and_cache(self.k, self.v, self.nk, self.nv, self.slots, err_flag=self.err, stream=stream,
+                                     desc=self.desc)
+
+    def attend(self, stream):
+        self.pa.pa_prefill(self.out, self.q, self.k, self.v, self.tables, self.lens, self.qs, self.max_q, self.w.scale,
+                           err_flag=self.err, stream=stream, desc=self.desc)
+
+
+def time_device(ds, steps: int, warmup: int, world: int):
     import torch
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             ds.writes(stream)
-            ds.decode(stream)
+            ds.attend(stream)
         stream.synchronize()
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
         barrier(world)
@@ -261,7 +302,7 @@ def time_device(ds: DeviceStep, steps: int, warmup: int, world: int):
             ev[i][0].record(stream)
             ds.writes(stream)
             ev[i][1].record(stream)
-            ds.decode(stream)
+            ds.attend(stream)
             ev[i][2].record(stream)
         torch.cuda.synchronize()
         t1 = time.time()
@@ -448,10 +489,46 @@ def run_ours(args, world, rank, local):
                 line["other_workloads"][name]["unique_kv_bytes"] = wx.unique_kv_bytes()
             del dx
             torch.cuda.empty_cache()
+    if not args.no_extra and world == 1 and args.prefill:
+        line["prefill"] = bench_prefill(args.prefill, device, max(5, min(args.steps, 20)), args.warmup, peaks)
+        torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def bench_prefill(name: str, device, steps: int, warmup: int, peaks):
+    """Chunked prefill on the tensor cores: the chunk's K/V append and the
+    attention call, timed per launch with CUDA events on the launching stream.
+    Its roofline is the dense bf16 tensor peak: algorithmic FLOPs (4 D Hq per
+    visible (query, key) pair) over the attention launch's duration."""
+    import torch
+    w = W.WORKLOADS[name](materialize=False)
+    ps = PrefillDeviceStep(w, device)
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    ms_step, att_ms, write_ms, (t0, t1) = time_device(ps, steps, warmup, 1)
+    sampler.stop()
+    if int(ps.err.item()):
+        raise RuntimeError(f"device error flag {int(ps.err.item())} in prefill")
+    att = statistics.mean(att_ms)
+    flops = w.prefill_flops()
+    tflops = flops / (att * 1e-3) / 1e12
+    peak = (peaks or {}).get("bf16_tflops")
+    peak_src = "measured (burst)" if peak else "fallback"
+    peak = peak or 1900.0
+    T = w.num_query_tokens
+    return {"workload": name, "description": WORKLOAD_DESC.get(name, name), "query_tokens": T,
+            "context_tokens": int(w.seq_lens.sum()), "ms_per_step": round(ms_step, 5),
+            "attention_ms": round(att, 5), "append_ms": round(statistics.mean(write_ms), 5),
+            "query_tokens_per_s": round(T / (ms_step * 1e-3), 1), "gpu_launches": 2 * steps,
+            "roofline": {"bound": "tensor", "kernel": "pa_prefill (prefill_tc_kernel)", "achieved": round(tflops, 1),
+                         "peak": peak, "peak_source": peak_src, "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                         "traffic": None, "algorithmic_flops_per_launch": flops,
+                         "sustained_peak": (peaks or {}).get("bf16_tflops_sustained")},
+            "l2": "q + out + K/V of the chunk's sequences exceed L2; no flush",
+            "clocks": sampler.summary(t0, t1)}
 
 
 def run_reference(args, world, rank):
@@ -500,10 +577,11 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mha_f16", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", default="mha_f16", choices=sorted(k for k in W.WORKLOADS if not k.startswith("prefill")))
     ap.add_argument("--extra", nargs="*", default=["gqa_bf16", "gqa_bf16+alibi", "long_bf16_b16", "long_bf16_b32",
                                                    "long_bf16_b64", "shared_prefix_f16"])
     ap.add_argument("--no-extra", action="store_true", help="time only the headline workload")
+    ap.add_argument("--prefill", default="prefill_bf16", help="chunked-prefill workload timed beside decode ('' = none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--partition", type=int, default=None,
                     help="tokens per split-KV partition (multiple of the block size; 0 = library default)")

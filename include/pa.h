@@ -71,7 +71,9 @@ enum {
   PA_DEVERR_BLOCK_ID = 1, /* a block_tables entry outside [0, num_blocks) */
   PA_DEVERR_SLOT = 2,     /* a slot_mapping entry >= num_blocks * block_size */
   PA_DEVERR_PAIR = 3,     /* a copy pair with an ID outside [0, num_blocks) */
-  PA_DEVERR_TIMEOUT = 4   /* a bounded wait on an asynchronous copy expired */
+  PA_DEVERR_TIMEOUT = 4,  /* a bounded wait on an asynchronous copy expired */
+  PA_DEVERR_QUERY = 5     /* pa_prefill: a chunk outside [0, num_query_tokens), longer than
+                             max_query_len or than its sequence, or a sequence past its table */
 };
 
 /*
@@ -137,6 +139,37 @@ int32_t pa_decode_partition_size(int32_t max_blocks_per_seq, const pa_cache_desc
  * for invalid arguments as well (pa_decode then reports the argument error). */
 size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
                                 const pa_cache_desc* cache, int32_t partition_size);
+
+/*
+ * pa_prefill - chunked prefill attention over the paged cache.
+ *   ["PagedAttention 详解：缓存的存储结构" "使用流程": prompt blocks that hit the
+ *   prefix cache take part in attention directly, only missed blocks are
+ *   computed and written through slot_mapping; "vLLM 核心工程深度剖析" "6.1":
+ *   long prompts are prefilled in chunks.]
+ *   Sequence s holds seq_lens[s] = L tokens in the cache (the chunk's own K/V
+ *   already written, e.g. by pa_reshape_and_cache), the last
+ *   n = query_start[s+1] - query_start[s] of which are this chunk's queries.
+ *   Query j of head h (position L - n + j) attends causally to cache positions
+ *   0 .. L - n + j: out = softmax_i(scale * q . k_i) v_i, fp32 accumulation,
+ *   out rounded to dtype.
+ *
+ *   out, q           [num_query_tokens][num_q_heads][head_size], 16-byte aligned;
+ *                    out rows outside every chunk are not written
+ *   query_start      int32 [num_seqs + 1] on the device: chunk s is rows
+ *                    query_start[s] .. query_start[s+1] - 1
+ *   seq_lens         int32 [num_seqs], n <= L <= max_blocks_per_seq * block_size
+ *   max_query_len    upper bound on n over the sequences (sizes the grid)
+ *   A sequence whose chunk breaks these rules is skipped and PA_DEVERR_QUERY is
+ *   reported; a bad block ID gives PA_DEVERR_BLOCK_ID and that sequence's
+ *   output is undefined.
+ *   Supported: dtype f16 / bf16, head_size 128, block_size 16, 32, 64 or 128.
+ *   Runs on the tcgen05 tensor cores (one CTA per sequence, query head and tile
+ *   of 128 queries).
+ */
+int pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+               const int32_t* seq_lens, const int32_t* query_start, int32_t num_seqs, int32_t num_query_tokens,
+               int32_t num_q_heads, int32_t max_blocks_per_seq, int32_t max_query_len, const pa_cache_desc* cache,
+               float scale, int32_t* err_flag, void* stream);
 
 /*
  * pa_reshape_and_cache - append new tokens' K/V through slot_mapping.

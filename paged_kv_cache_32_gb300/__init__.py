@@ -20,10 +20,10 @@ from . import build as _build
 PA_F32, PA_F16, PA_BF16 = 0, 1, 2
 PA_OK = 0
 PA_DEVERR = {0: "none", 1: "block id out of range", 2: "slot out of range", 3: "copy pair id out of range",
-             4: "wait on an asynchronous copy timed out"}
+             4: "wait on an asynchronous copy timed out", 5: "prefill chunk inconsistent with q, grid or sequence"}
 
 EXPORTED = ("pa_decode", "pa_decode_ex", "pa_decode_partition_size", "pa_decode_workspace_size", "pa_reshape_and_cache",
-            "pa_copy_blocks", "pa_status_string", "pa_version", "pa_decode_noalloc")
+            "pa_copy_blocks", "pa_status_string", "pa_version", "pa_decode_noalloc", "pa_prefill")
 
 
 class pa_decode_options(ctypes.Structure):
@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
         L.pa_decode.restype = ctypes.c_int
         L.pa_decode_ex.argtypes = L.pa_decode.argtypes + [ctypes.POINTER(pa_decode_options)]
         L.pa_decode_ex.restype = ctypes.c_int
+        L.pa_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, desc_p, ctypes.c_float, vp, vp]
+        L.pa_prefill.restype = ctypes.c_int
         L.pa_decode_partition_size.argtypes = [i32, desc_p, i32]
         L.pa_decode_partition_size.restype = i32
         L.pa_decode_workspace_size.argtypes = [i32, i32, i32, desc_p, i32]
@@ -177,6 +179,27 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale: float, pa
         _dense(alibi_slopes, "alibi_slopes")
         opts = pa_decode_options(_ptr(alibi_slopes))
         _check(lib().pa_decode_ex(*args, ctypes.byref(opts)), "pa_decode_ex")
+
+
+def pa_prefill(out, q, k_cache, v_cache, block_tables, seq_lens, query_start, max_query_len: int, scale: float,
+               err_flag=None, stream=None, desc: pa_cache_desc | None = None) -> None:
+    """Chunked prefill: the queries q[query_start[s]:query_start[s+1]] are the last
+    n_s of seq_lens[s] cached tokens; query j attends to positions 0..L-n_s+j.
+
+    out, q: [num_query_tokens, num_q_heads, 128] (f16/bf16); block_tables int32
+    [num_seqs, max_blocks_per_seq]; seq_lens int32 [num_seqs]; query_start int32
+    [num_seqs + 1]; max_query_len bounds every n_s (it sizes the grid).
+    """
+    desc = desc or cache_desc(k_cache)
+    for t, n in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (block_tables, "block_tables"), (seq_lens, "seq_lens"), (query_start, "query_start")):
+        _dense(t, n)
+    num_seqs = int(seq_lens.shape[0])
+    max_blocks = int(block_tables.shape[1]) if block_tables.dim() == 2 else 0
+    status = lib().pa_prefill(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(seq_lens),
+                              _ptr(query_start), num_seqs, int(q.shape[0]), int(q.shape[1]), max_blocks,
+                              int(max_query_len), ctypes.byref(desc), float(scale), _ptr(err_flag), _stream(stream))
+    _check(status, "pa_prefill")
 
 
 def pa_reshape_and_cache(k_cache, v_cache, key, value, slot_mapping, err_flag=None, stream=None,

@@ -28,7 +28,23 @@ struct DecodeParams {
   const float* alibi;         // nullable [Hq]: score_i += slope_h * (i - (L - 1))
 };
 
+// Parameters of one chunked-prefill launch.
+struct PrefillParams {
+  void* out;                    // [total_q][Hq][D]
+  const int32_t* block_tables;  // [N][M]
+  const int32_t* seq_lens;      // [N] cached tokens including the chunk
+  const int32_t* query_start;   // [N + 1]
+  int32_t* err_flag;            // nullable
+  int32_t num_seqs, num_q_heads, num_kv_heads;
+  int32_t max_blocks, block_size, num_blocks;
+  int32_t q_tiles;              // ceil(max_query_len / 128)
+  int32_t num_query_tokens;     // rows of q and out
+  float scale_log2;
+};
+
 // Kernel launchers (return the cudaGetLastError of the launch).
+cudaError_t launch_prefill_tc(int dtype, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const PrefillParams& p, cudaStream_t stream);
 cudaError_t launch_decode_tc(int dtype, int head_size, int block_size, const CUtensorMap& tk, const CUtensorMap& tv,
                              const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_f32(int head_size, const float* k_cache, const float* v_cache, const DecodeParams& p,

@@ -85,6 +85,28 @@ def test_partition_and_workspace_sizes(lib):
     assert pa.pa_decode_workspace_size(8, 32, 16, d, 0) == 0
 
 
+def call_prefill(lib, d, out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, sl=FAKE, qs=FAKE, n=2, tq=64, hq=4, m=4, mql=32,
+                 scale=0.1):
+    return lib.pa_prefill(out, q, k, v, bt, sl, qs, n, tq, hq, m, mql, ctypes.byref(d), scale, None, None)
+
+
+def test_prefill_argument_errors(lib):
+    assert call_prefill(lib, desc(d=64)) == 2                         # only head_size 128 is built
+    assert call_prefill(lib, desc(dtype=pa.PA_F32, bs=16)) == 2      # no fp32 tensor-core path
+    assert call_prefill(lib, desc(bs=256)) == 2                      # a key tile holds whole blocks
+    assert call_prefill(lib, desc(), n=-1) == 3
+    assert call_prefill(lib, desc(), tq=-1) == 3
+    assert call_prefill(lib, desc(), hq=3) == 3                      # Hq % Hkv != 0
+    assert call_prefill(lib, desc(), mql=-5) == 3
+    assert call_prefill(lib, desc(), scale=float("nan")) == 3
+    assert call_prefill(lib, desc(), q=None) == 1
+    assert call_prefill(lib, desc(), qs=None) == 1
+    assert call_prefill(lib, desc(), out=FAKE + 8) == 5               # 16-byte alignment
+    assert call_prefill(lib, desc(), n=0) == 0                        # nothing to do: no launch
+    assert call_prefill(lib, desc(), tq=0) == 0
+    assert call_prefill(lib, desc(), mql=0) == 0
+
+
 def test_write_argument_errors(lib):
     d = desc()
     assert lib.pa_reshape_and_cache(FAKE, FAKE, FAKE, FAKE, FAKE, -1, ctypes.byref(d), None, None) == 3

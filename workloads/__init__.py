@@ -171,10 +171,24 @@ class Workload:
     new_value: np.ndarray | None = None
     partition_size: int = 0
     info: dict = dataclasses.field(default_factory=dict)
+    query_start: np.ndarray | None = None     # prefill: int32 [N + 1] chunk offsets into q
 
     @property
     def num_seqs(self) -> int:
+        return int(len(self.seq_lens))
+
+    @property
+    def num_query_tokens(self) -> int:
         return int(self.q.shape[0])
+
+    def prefill_flops(self) -> int:
+        """Algorithmic FLOPs of prefill attention: query j of a chunk of n at the
+        end of L cached tokens sees L - n + j + 1 keys, and each key costs 2 D
+        (q . k) + 2 D (p v) per query head: 4 D Hq (n L - n (n - 1) / 2) per sequence."""
+        n = np.diff(self.query_start.astype(np.int64))
+        L = self.seq_lens.astype(np.int64)
+        keys = n * L - n * (n - 1) // 2
+        return int(4 * self.head_size * self.num_q_heads * keys.sum())
 
     @property
     def max_blocks_per_seq(self) -> int:
@@ -200,7 +214,7 @@ class Workload:
         """Algorithmic HBM bytes of the whole step: copies + appends + attention."""
         eb = ELEM_BYTES[self.dtype]
         total = self.kv_bytes()
-        total += 2 * self.num_seqs * self.num_q_heads * self.head_size * eb          # q in, out
+        total += 2 * self.num_query_tokens * self.num_q_heads * self.head_size * eb  # q in, out
         total += int(np.sum(-(-self.seq_lens.astype(np.int64) // self.block_size))) * 4  # table reads
         if self.copy_pairs is not None:
             total += len(self.copy_pairs) * 2 * 2 * self.num_kv_heads * self.block_size * self.head_size * eb
@@ -370,6 +384,65 @@ def long_bf16(block_size: int = 16, num_seqs: int = 8, seq_len: int = 32768, par
                         partition_size=partition_size, materialize=materialize)
 
 
+def build_prefill(name: str, *, seed: int, dtype: str, prefix_lens, chunk_lens, num_q_heads: int, num_kv_heads: int,
+                  head_size: int, block_size: int, pool_factor: float = 1.2, materialize: bool = True) -> Workload:
+    """Chunked prefill: sequence s already holds prefix_lens[s] tokens in the cache
+    and this step appends chunk_lens[s] new tokens (their K/V written through
+    slot_mapping, slots start as NaN), then runs prefill attention for the chunk's
+    queries over the whole context.  q is packed [sum chunk_lens, Hq, D]."""
+    rng = np.random.default_rng(seed)
+    prefix_lens = [int(x) for x in prefix_lens]
+    chunk_lens = [int(x) for x in chunk_lens]
+    totals = [a + b for a, b in zip(prefix_lens, chunk_lens)]
+    need = sum(-(-L // block_size) for L in totals)
+    num_blocks = max(1, math.ceil(pool_factor * need))
+    alloc = BlockAllocator(num_blocks, block_size, rng)
+    for s, P in enumerate(prefix_lens):
+        alloc.allocate(s, P)
+    shape = (num_blocks, num_kv_heads, block_size, head_size)
+    k_cache = v_cache = None
+    if materialize:
+        k_cache, v_cache = nan_array(shape, dtype), nan_array(shape, dtype)
+        for s, P in enumerate(prefix_lens):
+            _fill_tokens(k_cache, v_cache, rng, alloc, s, 0, P, dtype)
+    slots = []
+    for s, n in enumerate(chunk_lens):  # the chunk's slots: block * B + offset, in token order
+        start = alloc.lens[s]
+        need_blocks = -(-(start + n) // block_size) - len(alloc.tables[s])
+        for _ in range(need_blocks):
+            alloc.tables[s].append(alloc._take())
+        alloc.lens[s] = start + n
+        pos = np.arange(start, start + n)
+        blocks = np.asarray(alloc.tables[s], dtype=np.int64)[pos // block_size]
+        slots.extend((blocks * block_size + pos % block_size).tolist())
+    T = len(slots)
+    new_key = new_value = q = None
+    if materialize:
+        new_key = normal(rng, (T, num_kv_heads, head_size), dtype)
+        new_value = normal(rng, (T, num_kv_heads, head_size), dtype)
+        q = normal(rng, (T, num_q_heads, head_size), dtype)
+    else:  # shapes only; the benchmark draws these on the device
+        q = np.empty((T, num_q_heads, head_size), NP_STORAGE[dtype])
+    tables = alloc.table_array(list(range(len(totals))))
+    return Workload(name=name, dtype=dtype, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_size=head_size,
+                    block_size=block_size, num_blocks=num_blocks, scale=1.0 / math.sqrt(head_size), q=q,
+                    k_cache=k_cache, v_cache=v_cache, block_tables=tables,
+                    seq_lens=np.asarray(totals, dtype=np.int32), slot_mapping=np.asarray(slots, dtype=np.int64),
+                    new_key=new_key, new_value=new_value, info={"seed": seed, "prefix_lens": prefix_lens},
+                    query_start=np.concatenate([[0], np.cumsum(chunk_lens)]).astype(np.int32))
+
+
+def prefill_bf16(num_seqs: int = 16, materialize: bool = True, max_prefix: int = 2048, min_chunk: int = 256,
+                 max_chunk: int = 2048) -> Workload:
+    """Chunked prefill, bf16: 16 sequences, cached prefix U[0, 2048] tokens, new
+    chunk U[256, 2048] tokens, 32 q / 8 kv heads, D = 128, B = 16."""
+    rng = np.random.default_rng(1005)
+    prefix = rng.integers(0, max_prefix, size=num_seqs, endpoint=True)
+    chunk = rng.integers(min_chunk, max_chunk, size=num_seqs, endpoint=True)
+    return build_prefill("prefill_bf16", seed=1005, dtype="bf16", prefix_lens=prefix, chunk_lens=chunk, num_q_heads=32,
+                         num_kv_heads=8, head_size=128, block_size=16, materialize=materialize)
+
+
 WORKLOADS = {
     "tiny_f32": lambda materialize=True: tiny_f32(),
     "mha_f16": mha_f16,
@@ -378,6 +451,7 @@ WORKLOADS = {
     "long_bf16_b16": lambda materialize=True: long_bf16(16, materialize=materialize),
     "long_bf16_b32": lambda materialize=True: long_bf16(32, materialize=materialize),
     "long_bf16_b64": lambda materialize=True: long_bf16(64, materialize=materialize),
+    "prefill_bf16": prefill_bf16,
 }
 
 
