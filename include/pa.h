@@ -159,6 +159,7 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t m
  *                    query_start[s] .. query_start[s+1] - 1
  *   seq_lens         int32 [num_seqs], n <= L <= max_blocks_per_seq * block_size
  *   max_query_len    upper bound on n over the sequences (sizes the grid)
+ *   scale            finite and > 0 (the softmax scale, e.g. 1/sqrt(head_size))
  *   A sequence whose chunk breaks these rules is skipped and PA_DEVERR_QUERY is
  *   reported; a bad block ID gives PA_DEVERR_BLOCK_ID and that sequence's
  *   output is undefined.

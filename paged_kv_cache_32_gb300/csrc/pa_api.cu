@@ -217,7 +217,7 @@ int pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cach
   if (num_seqs < 0 || num_query_tokens < 0 || num_q_heads <= 0 || max_blocks_per_seq < 0 || max_query_len < 0)
     return PA_ERR_INVALID_ARG;
   if (num_q_heads % cache->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
-  if (!(scale == scale) || isinf(scale)) return PA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || isinf(scale)) return PA_ERR_INVALID_ARG;  // the row max is taken on unscaled scores
   if (num_seqs == 0 || max_query_len == 0 || num_query_tokens == 0) return PA_OK;
   if (out == nullptr || q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr ||
       query_start == nullptr || block_tables == nullptr)

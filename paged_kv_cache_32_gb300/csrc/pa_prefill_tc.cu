@@ -10,24 +10,30 @@
 // 0..p: out = softmax_i(scale * q . k_i) v_i.  Keys and values of token i come
 // from offset i % B of block block_tables[s][i / B] (section "软件地址翻译").
 //
-// How:
-//  * One CTA (4 warps) per (sequence, query head, tile of 128 queries).  The
-//    query tile is fetched once by a 3-D tensor-map copy; key/value tiles of
-//    128 tokens are gathered block by block through the block table with 2-D
-//    tensor-map copies (128-byte swizzle) into a two-stage ring; the four
-//    warps issue the copies of a tile together.
-//  * S = Q K^T (M = 128 queries, N = 128 keys, K = D) and O_t = P V
-//    (M = 128, N = D, K = 128 keys) are tcgen05.mma (kind::f16, fp32
-//    accumulate) issued by one thread from shared-memory descriptors; the
-//    accumulators live in tensor memory (S in columns 0..127, O in 128..255).
-//  * With the 32x32b tensor-memory layout thread t owns query row t, so the
-//    online softmax (row max, exp2, row sum) needs no cross-thread reduction.
-//    P is written to shared memory in the 128-byte-swizzled K-major layout the
-//    second MMA reads (bf16 P as hi + lo terms, two MMAs, since 8 significant
-//    bits alone would cost up to 2^-9 of each weight).  O accumulates in tensor memory across key tiles; when
-//    a row's running max grows, its warp rescales its 32 rows of O in place
-//    (tcgen05.ld / st) after the previous P V has finished and before the next
-//    one is issued, so the rescale is skipped on most tiles.
+// How (one CTA per sequence, query head and tile of 128 queries; 9 warps):
+//  * Data: the query tile is fetched once by a 3-D tensor-map copy; key and
+//    value tiles of 128 tokens are gathered block by block through the block
+//    table with 2-D tensor-map copies (128-byte swizzle) into two-stage K and
+//    V rings.  Each copy (one block, one 64-column half) is issued by its own
+//    thread, which arrives on the stage barrier with the bytes it copies.
+//  * Tensor memory (512 columns): two S buffers (0..127, 128..255) and two
+//    output accumulators O0, O1 (256..383, 384..511).
+//  * Warp 8 (one thread) issues every MMA: S = Q K^T (M = 128 queries,
+//    N = 128 keys, K = D; A and B from shared memory) and O_g += P_g V_g
+//    (A = P from tensor memory, B = V from shared memory), kind::f16 with fp32
+//    accumulation.  S of tile kt + 2 goes into the buffer of tile kt once
+//    P V of tile kt has finished, so the softmax of tile kt + 1 overlaps both.
+//  * Warps 0..7 run the softmax as two groups: group g owns keys
+//    64g .. 64g + 63 of every key tile (columns of S), with its own running
+//    max m_g, sum l_g and accumulator O_g for every query row (thread = row
+//    in the 32x32b tensor-memory layout, no cross-thread reduction).  P is
+//    written back into the S columns it came from (tcgen05.st) and consumed
+//    there by the P V MMA; bf16 P is written as two terms hi + lo (two MMAs),
+//    since 8 significant bits alone would cost up to 2^-8 of each weight.
+//  * Rescaling: a row's reference max moves only when the tile max exceeds it
+//    by more than 8 (log2 units), so P <= 2^8 and O_g is rescaled in place
+//    (tcgen05.ld / st) on few tiles.  The epilogue merges the two groups:
+//    out = (O0 2^(m0-M) + O1 2^(m1-M)) / (l0 2^(m0-M) + l1 2^(m1-M)).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -42,14 +48,19 @@
 namespace pa {
 namespace {
 
-constexpr int kTile = 128;           // queries per CTA = keys per key tile
-constexpr int kD = 128;              // head size of this kernel
-constexpr int kHalf = kTile * 128;   // one 128-row x 128-byte swizzled region (16 KB)
-constexpr int kQOff = 0;             // Q: 2 regions (dims 0-63, 64-127)
-constexpr int kKOff = 2 * kHalf;     // K stages: 2 x 2 regions
-constexpr int kVOff = 6 * kHalf;     // V stages: 2 x 2 regions
-constexpr int kPOff = 10 * kHalf;    // P: 2 regions (keys 0-63, 64-127)
-constexpr int kPLoOff = 12 * kHalf;  // bf16 only: P - bf16(P), the same layout
+constexpr int kTile = 128;            // queries per CTA = keys per key tile
+constexpr int kD = 128;               // head size of this kernel
+constexpr int kHalf = kTile * 128;    // one 128-row x 128-byte swizzled region (16 KB)
+constexpr int kQOff = 0;              // Q: 2 regions (dims 0-63, 64-127)
+constexpr int kKOff = 2 * kHalf;      // K stages: 2 x 2 regions
+constexpr int kVOff = 6 * kHalf;      // V stages: 2 x 2 regions
+constexpr int kBarOff = 10 * kHalf;   // barriers, flags, the (m, l) exchange
+constexpr int kSmemBytes = kBarOff + 128 + 2 * kTile * 8 + 1024;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kThreads = (kSoftmaxWarps + 1) * 32;
+constexpr int kControlWarp = kSoftmaxWarps;
+constexpr float kRescaleThreshold = 8.f;  // log2 units: P <= 2^8 between rescales
+constexpr long long kWaitCyclesPf = 500ll * 1000 * 1000;
 
 // bf16 keeps 8 significant bits, so P is fed to the tensor cores as two bf16
 // terms (P = hi + lo, two MMAs); fp16's 11 bits need one
@@ -57,22 +68,26 @@ template <typename T>
 constexpr bool split_p() {
   return std::is_same<T, __nv_bfloat16>::value;
 }
-template <typename T>
-constexpr int bar_off() {  // barriers: q, kv[2], s, o; then the tensor-memory address
-  return split_p<T>() ? 14 * kHalf : 12 * kHalf;
-}
-template <typename T>
-constexpr int smem_bytes() {
-  return bar_off<T>() + 64 + 16 + 1024;
-}
-constexpr long long kWaitCyclesPf = 500ll * 1000 * 1000;
 
-__device__ __forceinline__ bool wait_cycles(uint64_t* bar, uint32_t parity) {
+// bounded wait; gives up at once when another thread has recorded a failure
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity))
-    if (clock64() - t0 > kWaitCyclesPf) return false;
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCyclesPf) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
   return true;
+}
+
+// drain wait: bounded, ignores the abort flag
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitCyclesPf) return;
 }
 
 // shared-memory matrix descriptor, 128-byte swizzle (version 1)
@@ -81,7 +96,8 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
          ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// instruction descriptor, kind::f16: fp32 accumulate, A/B element type (0 f16, 1 bf16), B major (0 K, 1 MN)
+// instruction descriptor, kind::f16: fp32 accumulate, A/B element type (0 f16, 1 bf16), B major (0 K, 1 MN),
+// M = N = 128
 template <typename T>
 __device__ __forceinline__ constexpr uint32_t idesc(uint32_t b_mn) {
   constexpr uint32_t ab = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
@@ -89,11 +105,21 @@ __device__ __forceinline__ constexpr uint32_t idesc(uint32_t b_mn) {
          ((uint32_t)(kTile >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t id, bool accumulate) {
+// D (tensor memory) (+)= A (shared memory) x B (shared memory)
+__device__ __forceinline__ void mma_ss(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t id, bool accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
       "l"(a), "l"(b), "r"(id), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+// D (tensor memory) (+)= A (tensor memory, row m in lane m, 2 elements per column) x B (shared memory)
+__device__ __forceinline__ void mma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t id, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(b), "r"(id), "r"((uint32_t)accumulate)
       : "memory");
 }
 
@@ -102,8 +128,9 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+// 32 consecutive columns of this warp's 32 lanes; completes with tmem_wait_ld()
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
       "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -112,29 +139,61 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
         "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// wait for outstanding tensor-memory loads, then tie each loaded register to the wait so that
+// no use of it is scheduled before the data has arrived
+template <int N>
+__device__ __forceinline__ void tmem_wait_ld(float* v) {
+  tmem_wait_ld();
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < N; ++i) asm volatile("" : "+f"(v[i]));
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
       "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
-      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
-      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])),
-      "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])),
-      "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])),
-      "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// packed fp32 pair arithmetic (one instruction for two lanes of work)
+__device__ __forceinline__ unsigned long long f2_bits(float2 a) {
+  return (unsigned long long)__float_as_uint(a.x) | ((unsigned long long)__float_as_uint(a.y) << 32);
+}
+__device__ __forceinline__ float2 bits_f2(unsigned long long d) {
+  return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+  return bits_f2(d);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(d);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(d);
+}
 
 __device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, int32_t x, int32_t y, int32_t z,
                                             uint64_t* bar) {
@@ -145,10 +204,42 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, in
       : "memory");
 }
 
+// P of one row's 64 keys (two per 32-bit column, lower key in the low half) from
+// the scores v (raw q . k), the scale in log2 units and the reference max; keys
+// i > lim are masked.  Writes hi (and for bf16 lo) words; returns the row sum
+// of the unrounded weights.
+template <typename T, bool kMasked>
+__device__ __forceinline__ float make_p(const float* v, float sl2, float m_ref, int lim, uint32_t* hi,
+                                        uint32_t* lo) {
+  float2 acc = make_float2(0.f, 0.f);
+  const float2 s2 = make_float2(sl2, sl2), nm2 = make_float2(-m_ref, -m_ref);
+#pragma unroll
+  for (int i = 0; i < 64; i += 2) {
+    const float2 x = fma2(make_float2(v[i], v[i + 1]), s2, nm2);
+    float e0 = fast_exp2(x.x), e1 = fast_exp2(x.y);
+    if (kMasked) {
+      e0 = i <= lim ? e0 : 0.f;
+      e1 = i + 1 <= lim ? e1 : 0.f;
+    }
+    acc = add2(acc, make_float2(e0, e1));
+    if constexpr (split_p<T>()) {
+      // hi = e truncated to bf16 (exact as a float), lo = the remainder rounded to bf16
+      const uint32_t b0 = __float_as_uint(e0), b1 = __float_as_uint(e1);
+      hi[i / 2] = __byte_perm(b0, b1, 0x7632);
+      const float2 r = sub2(make_float2(e0, e1), make_float2(__uint_as_float(b0 & 0xffff0000u),
+                                                            __uint_as_float(b1 & 0xffff0000u)));
+      lo[i / 2] = Mma<T>::pack(r.x, r.y);
+    } else {
+      hi[i / 2] = Mma<T>::pack(e0, e1);
+    }
+  }
+  return acc.x + acc.y;
+}
+
 }  // namespace
 
 template <typename T>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
   // ---- work item
@@ -169,35 +260,44 @@ __global__ void __launch_bounds__(128, 1)
   const int tile0 = qt * kTile;
   if (tile0 >= n) return;
   const int hkv = h / (p.num_q_heads / p.num_kv_heads);
-  const int rows = min(kTile, n - tile0);             // valid query rows of this tile
-  const int pos0 = L - n + tile0;                     // position of query row 0
+  const int rows = min(kTile, n - tile0);               // valid query rows of this tile
+  const int pos0 = L - n + tile0;                       // position of query row 0
   const int key_tiles = (pos0 + rows - 1) / kTile + 1;  // key tiles reaching the last row's position
   const int blocks_per_tile = kTile / B;
+  const int slots = 2 * blocks_per_tile;                // copies per K (or V) tile: one per block and half
   const int32_t* table = p.block_tables + (size_t)s * p.max_blocks;
-  const int nblocks_seq = min((L + B - 1) / B, p.max_blocks);  // never read past the table row
+  const int nblocks_seq = (L + B - 1) / B;              // <= max_blocks (checked above)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  constexpr int kBarOff = bar_off<T>();
   uint64_t* bar_q = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  uint64_t* bar_kv = bar_q + 1;  // [2]
-  uint64_t* bar_s = bar_q + 3;
-  uint64_t* bar_o = bar_q + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 64);
+  uint64_t* bar_k = bar_q + 1;  // [2] K stage landed
+  uint64_t* bar_v = bar_q + 3;  // [2] V stage landed
+  uint64_t* bar_s = bar_q + 5;  // [2] S buffer computed
+  uint64_t* bar_p = bar_q + 7;  // [2] P of the buffer written by all softmax warps
+  uint64_t* bar_o = bar_q + 9;  // O += P V done
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 96);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 104);
+  float2* ml = reinterpret_cast<float2*>(smem + kBarOff + 128);  // [2][128] (m, l) per group and row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = threadIdx.x;  // query row owned by this thread (TMEM lane)
+  int n_s = 0, n_o = 0;  // S / P V commits (control thread)
+  int n_k = 0, n_v = 0;  // K / V tiles requested (uniform over the softmax warps)
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    mbar_init(&bar_kv[0], 1);
-    mbar_init(&bar_kv[1], 1);
-    mbar_init(bar_s, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar_k[b], slots);  // every copy slot arrives once per tile (with its bytes, or none)
+      mbar_init(&bar_v[b], slots);
+      mbar_init(&bar_s[b], 1);
+      mbar_init(&bar_p[b], kSoftmaxWarps);
+    }
     mbar_init(bar_o, 1);
+    *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(256u)
+                 "r"(512u)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -205,247 +305,261 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_s = tmem, tmem_o = tmem + 128;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
 
-  // valid (loadable) blocks of key tile kt: in the sequence and with an in-range ID
+  // physical block of block i of key tile kt: -1 past the sequence, -2 for an ID outside the pool
   auto block_id = [&](int kt, int i) -> int {
     const int bi = kt * blocks_per_tile + i;
     if (bi >= nblocks_seq) return -1;
     const int pb = __ldg(table + bi);
     return (pb >= 0 && pb < p.num_blocks) ? pb : -2;
   };
-  // expect the bytes of tile kt on stage kt % 2 (thread 0), then every warp issues its share of the copies
-  auto expect_tile = [&](int kt) {
-    int nvalid = 0;
-    for (int i = 0; i < blocks_per_tile; ++i) {
-      const int pb = block_id(kt, i);
-      if (pb >= 0) ++nvalid;
-      else if (pb == -2) report_error(p.err_flag, PA_DEVERR_BLOCK_ID);
+  // copy slot c = lane * 8 + warp (block c / 2, column half c % 2), softmax warps only: each slot's
+  // thread arrives on the stage barrier with the bytes it is about to copy
+  auto load_tile = [&](bool is_v, int kt) {
+    const int c = lane * kSoftmaxWarps + warp;
+    if (c >= slots) return;
+    uint64_t* bar = is_v ? &bar_v[kt & 1] : &bar_k[kt & 1];
+    const int i = c >> 1, half = c & 1;
+    const int pb = block_id(kt, i);
+    if (pb < 0) {
+      if (pb == -2 && !is_v && half == 0) report_error(p.err_flag, PA_DEVERR_BLOCK_ID);
+      mbar_arrive(bar);
+      return;
     }
-    mbar_arrive_expect_tx(&bar_kv[kt & 1], (uint32_t)nvalid * B * 128 * 4);
-  };
-  auto issue_tile = [&](int kt) {
-    if (lane != 0) return;
-    uint8_t* kst = smem + kKOff + (kt & 1) * 2 * kHalf;
-    uint8_t* vst = smem + kVOff + (kt & 1) * 2 * kHalf;
-    for (int i = warp; i < blocks_per_tile; i += 4) {
-      const int pb = block_id(kt, i);
-      if (pb < 0) continue;
-      const int y = (pb * p.num_kv_heads + hkv) * B;
-      for (int half = 0; half < 2; ++half) {
-        tma_load_2d(kst + half * kHalf + i * B * 128, &tmap_k, half * 64, y, &bar_kv[kt & 1]);
-        tma_load_2d(vst + half * kHalf + i * B * 128, &tmap_v, half * 64, y, &bar_kv[kt & 1]);
-      }
-    }
+    mbar_arrive_expect_tx(bar, (uint32_t)B * 128);
+    uint8_t* dst = smem + (is_v ? kVOff : kKOff) + (kt & 1) * 2 * kHalf + half * kHalf + i * B * 128;
+    tma_load_2d(dst, is_v ? (const void*)&tmap_v : (const void*)&tmap_k, half * 64, (pb * p.num_kv_heads + hkv) * B,
+                bar);
   };
 
-  // ---- prologue: the query tile and the first two key tiles
-  if (threadIdx.x == 0) {
-    tma_prefetch_descriptor(&tmap_q);
-    mbar_arrive_expect_tx(bar_q, 2 * kHalf);
-    for (int half = 0; half < 2; ++half)
-      tma_load_3d(smem + kQOff + half * kHalf, &tmap_q, half * 64, h, q0 + tile0, bar_q);
-    expect_tile(0);
-    if (key_tiles > 1) expect_tile(1);
-  }
-  __syncthreads();
-  issue_tile(0);
-  if (key_tiles > 1) issue_tile(1);
-
-  const float sl2 = p.scale_log2;
-  const int my_pos = pos0 + row;  // causal limit of this thread's row (row >= rows: unused)
-  float m_run = -INFINITY, l_run = 0.f;
-  bool ok = true;
-
-  int n_s = 0, n_o = 0, n_kv = key_tiles > 1 ? 2 : 1;  // S / PV commits and key tiles expected (thread 0)
-  const uint32_t id_s = idesc<T>(0), id_o = idesc<T>(1);
-  auto issue_s = [&](int kt) {  // S = Q K^T for key tile kt (thread 0)
-    const uint32_t qb = smem_u32(smem + kQOff), kb = smem_u32(smem + kKOff + (kt & 1) * 2 * kHalf);
+  if (warp == kControlWarp) {
+    // =================================================================== control warp: every MMA
+    if (lane == 0) {
+      const uint32_t id_s = idesc<T>(0), id_o = idesc<T>(1);
+      auto issue_s = [&](int kt) {  // S buffer kt % 2 = Q K^T of key tile kt
+        const uint32_t qb = smem_u32(smem + kQOff), kb = smem_u32(smem + kKOff + (kt & 1) * 2 * kHalf);
 #pragma unroll
-    for (int kk = 0; kk < kD / 16; ++kk) {
-      const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-      mma_f16(tmem_s, sw128_desc(qb + off, 16, 1024), sw128_desc(kb + off, 16, 1024), id_s, kk > 0);
-    }
-    mma_commit(bar_s);
-    ++n_s;
-  };
-  if (threadIdx.x == 0) {
-    ok = wait_cycles(bar_q, 0) && wait_cycles(&bar_kv[0], 0);
-    if (ok) {
-      tc_fence_after();
-      issue_s(0);
-    }
-  }
-  ok = __syncthreads_and(ok);
-
-  for (int kt = 0; kt < key_tiles; ++kt) {
-    // ---- pass 1 over the scores of tile kt: the row max (masked: causal and past the sequence)
-    ok = ok && wait_cycles(bar_s, kt & 1) && wait_cycles(&bar_kv[kt & 1], (kt >> 1) & 1);
-    ok = __syncthreads_and(ok);
-    if (!ok) break;
-    tc_fence_after();
-    const int kpos0 = kt * kTile;
-    float mx = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      float v[32];
-      tmem_ld32(tmem_s + lane_base + c * 32, v);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int kp = kpos0 + c * 32 + i;
-        if (kp <= my_pos && kp < L) mx = fmaxf(mx, v[i] * sl2);
-      }
-    }
-    const float m_new = fmaxf(m_run, mx);
-    const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run - m_new);
-    if (kt > 0) {
-      // the previous tile's O += P V is done: P, that tile's K/V stage and O may be touched
-      ok = wait_cycles(bar_o, (kt - 1) & 1);
-      tc_fence_after();
-      if (__any_sync(0xffffffffu, alpha != 1.f)) {  // rescale this warp's rows of O in tensor memory
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tmem_ld32(tmem_o + lane_base + c * 32, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= alpha;
-          tmem_st32(tmem_o + lane_base + c * 32, v);
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          mma_ss(tmem + (kt & 1) * 128, sw128_desc(qb + off, 16, 1024), sw128_desc(kb + off, 16, 1024), id_s, kk > 0);
         }
-      }
-    }
-    // ---- stage (kt + 1) & 1 held tile kt - 1, now consumed: fetch tile kt + 1's successor there
-    //      (tiles 0 and 1 were fetched up front; tile kt + 1 >= 2 goes into stage (kt + 1) & 1)
-    tc_fence_before();
-    if (threadIdx.x == 0 && kt >= 1 && kt + 1 < key_tiles) {
-      expect_tile(kt + 1);
-      ++n_kv;
-    }
-    ok = __syncthreads_and(ok);
-    if (!ok) break;
-    tc_fence_after();
-    if (kt >= 1 && kt + 1 < key_tiles) issue_tile(kt + 1);
-    // ---- pass 2: P = exp2(s - m) (f16/bf16, swizzled K-major; bf16 also the residual) and its row sum
-    float lsum = 0.f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      float v[32];
-      tmem_ld32(tmem_s + lane_base + c * 32, v);
-      // keys c*32 .. c*32+31 of this row: region c / 2, 16-byte chunks (c % 2) * 4 .. +3
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-          const int kp = kpos0 + c * 32 + j * 8 + i;
-          const float x0 = v[j * 8 + i] * sl2 - m_new, x1 = v[j * 8 + i + 1] * sl2 - m_new;
-          const float e0 = (kp <= my_pos && kp < L) ? fast_exp2(x0) : 0.f;
-          const float e1 = (kp + 1 <= my_pos && kp + 1 < L) ? fast_exp2(x1) : 0.f;
-          hi[i / 2] = Mma<T>::pack(e0, e1);
-          if constexpr (split_p<T>()) {
-            lo[i / 2] = Mma<T>::pack(e0 - Mma<T>::lo(hi[i / 2]), e1 - Mma<T>::hi(hi[i / 2]));
-            lsum += e0 + e1;
-          } else {
-            lsum += Mma<T>::lo(hi[i / 2]) + Mma<T>::hi(hi[i / 2]);  // the values the MMA multiplies with
-          }
-        }
-        const int off = (c >> 1) * kHalf + swz128(row, (c & 1) * 4 + j);
-        *reinterpret_cast<uint4*>(smem + kPOff + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        if constexpr (split_p<T>())
-          *reinterpret_cast<uint4*>(smem + kPLoOff + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      }
-    }
-    m_run = m_new;
-    l_run = l_run * alpha + lsum;
-    // values of key rows past the sequence (or of skipped blocks) may hold NaN: zero them
-    if (kpos0 + kTile > L || kt * blocks_per_tile + blocks_per_tile > nblocks_seq) {
-      uint8_t* vst = smem + kVOff + (kt & 1) * 2 * kHalf;
-      for (int idx = threadIdx.x; idx < kTile * 16; idx += 128) {  // 128 rows x 16 chunks of 16 bytes
-        const int r = idx >> 4, chunk = idx & 15;
-        const int kp = kpos0 + r;
-        if (kp >= L || block_id(kt, r / B) < 0)
-          *reinterpret_cast<uint4*>(vst + (chunk >> 3) * kHalf + swz128(r, chunk & 7)) = make_uint4(0, 0, 0, 0);
-      }
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P and V writes -> tensor-core reads
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    // ---- the next tile's scores, then O += P V (thread 0): P V runs while pass 1 of the next tile reads S
-    if (threadIdx.x == 0) {
-      if (kt + 1 < key_tiles) {
-        ok = wait_cycles(&bar_kv[(kt + 1) & 1], ((kt + 1) >> 1) & 1);
+        mma_commit(&bar_s[kt & 1]);
+        ++n_s;
+      };
+      tma_prefetch_descriptor(&tmap_q);
+      mbar_arrive_expect_tx(bar_q, 2 * kHalf);
+      for (int half = 0; half < 2; ++half)
+        tma_load_3d(smem + kQOff + half * kHalf, &tmap_q, half * 64, h, q0 + tile0, bar_q);
+      bool ok = wait_bar(bar_q, 0, abort_flag);
+      for (int t = 0; ok && t < 2 && t < key_tiles; ++t) {
+        ok = wait_bar(&bar_k[t], 0, abort_flag);
         if (ok) {
           tc_fence_after();
-          issue_s(kt + 1);
+          issue_s(t);
         }
       }
-      const uint32_t vb = smem_u32(smem + kVOff + (kt & 1) * 2 * kHalf);
+      for (int kt = 0; ok && kt < key_tiles; ++kt) {
+        const int buf = kt & 1;
+        // O_g += P_g V_g once every softmax warp has written P of tile kt and V of tile kt has landed
+        ok = wait_bar(&bar_p[buf], (kt >> 1) & 1, abort_flag) && wait_bar(&bar_v[buf], (kt >> 1) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t vb = smem_u32(smem + kVOff + buf * 2 * kHalf);
 #pragma unroll
-      for (int part = 0; part < (split_p<T>() ? 2 : 1); ++part) {
-        const uint32_t pb = smem_u32(smem + (part ? kPLoOff : kPOff));
+        for (int g = 0; g < 2; ++g) {
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_f16(tmem_o, sw128_desc(pb + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
-                  sw128_desc(vb + kk * 2048, kHalf, 1024), id_o, kt > 0 || part > 0 || kk > 0);
+          for (int part = 0; part < (split_p<T>() ? 2 : 1); ++part) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(tmem + 256 + 128 * g, tmem + buf * 128 + 64 * g + part * 32 + kk * 8,
+                     sw128_desc(vb + g * 8192 + kk * 2048, kHalf, 1024), id_o, kt > 0 || part > 0 || kk > 0);
+          }
+        }
+        mma_commit(bar_o);
+        ++n_o;
+        if (kt + 2 < key_tiles) {
+          // S of tile kt + 2 overwrites this buffer (P of tile kt): after that P V has finished
+          ok = wait_bar(bar_o, kt & 1, abort_flag) && wait_bar(&bar_k[buf], ((kt + 2) >> 1) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(kt + 2);
+        }
       }
-      mma_commit(bar_o);
-      ++n_o;
     }
-  }
-  // ---- out = O / l for this thread's query row
-  if (ok) ok = wait_cycles(bar_o, (key_tiles - 1) & 1);
-  ok = __syncthreads_and(ok);
-  if (!ok) {
-    // a wait expired: record it, then let the copies and MMAs this CTA started finish (each wait
-    // bounded) before the tensor memory is freed and the CTA's shared memory is released
-    if (threadIdx.x == 0) {
-      report_error(p.err_flag, PA_DEVERR_TIMEOUT);
-      if (n_s > 0) wait_cycles(bar_s, (n_s - 1) & 1);
-      if (n_o > 0) wait_cycles(bar_o, (n_o - 1) & 1);
-      for (int t = max(0, n_kv - 2); t < n_kv; ++t) wait_cycles(&bar_kv[t & 1], (t >> 1) & 1);
-    }
+    __syncwarp();
   } else {
-    tc_fence_after();
-    T* out = reinterpret_cast<T*>(p.out) + ((size_t)(q0 + tile0 + row) * p.num_q_heads + h) * kD;
-    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    // =================================================================== softmax warps
+    const int g = warp >> 2;                         // key columns 64g .. 64g + 63 of every tile
+    const int row = (warp & 3) * 32 + lane;          // query row = tensor-memory lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t o_addr = tmem + lane_base + 256 + 128 * g;
+    const float sl2 = p.scale_log2;
+    const int lim_base = min(pos0 + row, L - 1);     // last key position this row sees
+    float m_ref = -INFINITY, l_run = 0.f;
+    // a wait whose outcome every lane of the warp shares (warp-collective tensor-memory ops follow)
+    auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag));
+    };
+    for (int t = 0; t < 2 && t < key_tiles; ++t) {
+      load_tile(false, t);
+      load_tile(true, t);
+      ++n_k;
+      ++n_v;
+    }
+    bool ok = true;
+    for (int kt = 0; kt < key_tiles; ++kt) {
+      const int buf = kt & 1;
+      ok = warp_wait(&bar_s[buf], (kt >> 1) & 1);
+      if (!ok) break;
+      tc_fence_after();
+      if (kt + 2 < key_tiles) {  // S(kt) done: its K stage takes key tile kt + 2
+        load_tile(false, kt + 2);
+        ++n_k;
+      }
+      const uint32_t s_addr = tmem + lane_base + buf * 128 + 64 * g;
+      float v[64];
+      tmem_ld32(s_addr, v);
+      tmem_ld32(s_addr + 32, v + 32);
+      tmem_wait_ld<64>(v);
+      const int lim = lim_base - (kt * kTile + 64 * g);  // keys 0..lim of these 64 are visible
+      const bool unmasked = __all_sync(0xffffffffu, lim >= 63);
+      // ---- the tile's row max, and the reference max it implies
+      float mx = -INFINITY;
+      if (unmasked) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      float v[32];
-      tmem_ld32(tmem_o + lane_base + c * 32, v);  // warp-collective: every lane loads
-      if (row < rows) {
+        for (int i = 0; i < 64; i += 2) mx = max3(mx, v[i], v[i + 1]);
+      } else {
 #pragma unroll
-        for (int i = 0; i < 32; i += 8) {
-          uint4 val = make_uint4(Mma<T>::pack(v[i] * inv, v[i + 1] * inv), Mma<T>::pack(v[i + 2] * inv, v[i + 3] * inv),
-                                 Mma<T>::pack(v[i + 4] * inv, v[i + 5] * inv),
-                                 Mma<T>::pack(v[i + 6] * inv, v[i + 7] * inv));
-          *reinterpret_cast<uint4*>(out + c * 32 + i) = val;
+        for (int i = 0; i < 64; i += 2)
+          mx = max3(mx, i <= lim ? v[i] : -INFINITY, i + 1 <= lim ? v[i + 1] : -INFINITY);
+      }
+      const float mx_s = mx * sl2;  // scale > 0
+      const bool upd = mx_s > m_ref + kRescaleThreshold;
+      const float alpha = upd ? fast_exp2(m_ref - mx_s) : 1.f;
+      // P V of tile kt - 1 is confirmed once per tile, in order (phase kt - 1 of bar_o; phase kt cannot
+      // complete before this warp's P arrival below): first here if O must be rescaled, else before the arrival
+      bool o_prev_done = kt == 0;
+      if (__any_sync(0xffffffffu, upd) && kt > 0) {
+        // O_g of these rows is rescaled between P V of tile kt - 1 (done) and that of tile kt
+        ok = warp_wait(bar_o, (kt - 1) & 1);
+        if (!ok) break;
+        o_prev_done = true;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float o[32];
+          tmem_ld32(o_addr + c * 32, o);
+          tmem_wait_ld<32>(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(o_addr + c * 32, reinterpret_cast<const uint32_t*>(o));
+        }
+        tmem_wait_st();
+      }
+      if (upd) m_ref = mx_s;
+      // ---- P into the S columns it came from
+      uint32_t hi[32], lo[32];
+      const float lsum = unmasked ? make_p<T, false>(v, sl2, m_ref, lim, hi, lo)
+                                  : make_p<T, true>(v, sl2, m_ref, lim, hi, lo);
+      l_run = l_run * alpha + lsum;
+      tmem_st32(s_addr, hi);
+      if constexpr (split_p<T>()) tmem_st32(s_addr + 32, lo);
+      tmem_wait_st();
+      // ---- values of key rows past the sequence (or of blocks not loaded) may hold NaN: zero them
+      if (kt * kTile + kTile > L || (kt + 1) * blocks_per_tile > nblocks_seq) {
+        ok = warp_wait(&bar_v[buf], (kt >> 1) & 1);
+        if (!ok) break;
+        uint8_t* vst = smem + kVOff + buf * 2 * kHalf;
+        for (int idx = threadIdx.x; idx < kTile * 16; idx += kSoftmaxWarps * 32) {  // 128 rows x 16 chunks
+          const int r = idx >> 4, chunk = idx & 15;
+          if (kt * kTile + r >= L || block_id(kt, r / B) < 0)
+            *reinterpret_cast<uint4*>(vst + (chunk >> 3) * kHalf + swz128(r, chunk & 7)) = make_uint4(0, 0, 0, 0);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor-core reads
+      }
+      // ---- V stage (kt + 1) % 2 held tile kt - 1, whose P V is done: fetch value tile kt + 1 there
+      if (!o_prev_done) {
+        ok = warp_wait(bar_o, (kt - 1) & 1);
+        if (!ok) break;
+      }
+      if (kt >= 1 && kt + 1 < key_tiles) {
+        load_tile(true, kt + 1);
+        ++n_v;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_p[buf]);
+    }
+    // ---- epilogue: merge the two groups' (m, l, O) per row and write out (P V of every tile before
+    //      the last was confirmed inside the loop, so this parity wait cannot pass early)
+    if (ok) ok = warp_wait(bar_o, (key_tiles - 1) & 1);
+    ml[g * kTile + row] = make_float2(m_ref, l_run);
+    asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxWarps * 32) : "memory");
+    if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
+      tc_fence_after();
+      const float2 a = ml[row], b = ml[kTile + row];
+      const float M = fmaxf(a.x, b.x);
+      const float w0 = a.x == -INFINITY ? 0.f : fast_exp2(a.x - M), w1 = b.x == -INFINITY ? 0.f : fast_exp2(b.x - M);
+      const float den = a.y * w0 + b.y * w1;
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      const float c0 = w0 * inv, c1 = w1 * inv;
+      T* out = reinterpret_cast<T*>(p.out) + ((size_t)(q0 + tile0 + row) * p.num_q_heads + h) * kD + 64 * g;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {  // this group writes output columns 64g .. 64g + 63
+        float o0[32], o1[32];
+        tmem_ld32(tmem + lane_base + 256 + 64 * g + 32 * c, o0);
+        tmem_ld32(tmem + lane_base + 384 + 64 * g + 32 * c, o1);
+        tmem_wait_ld<32>(o0);
+        tmem_wait_ld<32>(o1);
+        if (row < rows) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 val;
+            val.x = Mma<T>::pack(o0[i] * c0 + o1[i] * c1, o0[i + 1] * c0 + o1[i + 1] * c1);
+            val.y = Mma<T>::pack(o0[i + 2] * c0 + o1[i + 2] * c1, o0[i + 3] * c0 + o1[i + 3] * c1);
+            val.z = Mma<T>::pack(o0[i + 4] * c0 + o1[i + 4] * c1, o0[i + 5] * c0 + o1[i + 5] * c1);
+            val.w = Mma<T>::pack(o0[i + 6] * c0 + o1[i + 6] * c1, o0[i + 7] * c0 + o1[i + 7] * c1);
+            *reinterpret_cast<uint4*>(out + 32 * c + i) = val;
+          }
         }
       }
     }
   }
   tc_fence_before();
   __syncthreads();
+  if (*abort_flag) {
+    // a wait expired (the flag is stable: every thread has left its loop): record it, and let the
+    // copies and MMAs this CTA started finish, each wait bounded, before its memory is released
+    if (threadIdx.x == 0) {
+      report_error(p.err_flag, PA_DEVERR_TIMEOUT);
+      for (int t = max(0, n_k - 2); t < n_k; ++t) drain_wait(&bar_k[t & 1], (t >> 1) & 1);
+      for (int t = max(0, n_v - 2); t < n_v; ++t) drain_wait(&bar_v[t & 1], (t >> 1) & 1);
+    }
+    if (warp == kControlWarp && lane == 0) {
+      for (int t = max(0, n_s - 2); t < n_s; ++t) drain_wait(&bar_s[t & 1], (t >> 1) & 1);
+      if (n_o > 0) drain_wait(bar_o, (n_o - 1) & 1);
+    }
+    __syncthreads();
+  }
   if (warp == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256u) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512u) : "memory");
 }
 
 cudaError_t launch_prefill_tc(int dtype, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const PrefillParams& p, cudaStream_t stream) {
   const long long grid = (long long)p.num_seqs * p.num_q_heads * p.q_tiles;
   if (grid == 0) return cudaSuccess;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   if (dtype == PA_F16) {
-    constexpr int smem = smem_bytes<__half>();
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(prefill_tc_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<__half><<<(unsigned)grid, 128, smem, stream>>>(tq, tk, tv, p);
+    prefill_tc_kernel<__half><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
   } else if (dtype == PA_BF16) {
-    constexpr int smem = smem_bytes<__nv_bfloat16>();
-    static_assert(smem <= 227 * 1024, "shared memory per CTA");
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<__nv_bfloat16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<__nv_bfloat16><<<(unsigned)grid, 128, smem, stream>>>(tq, tk, tv, p);
+    prefill_tc_kernel<__nv_bfloat16><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
   } else {
     return cudaErrorInvalidValue;
   }

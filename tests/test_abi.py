@@ -99,6 +99,8 @@ def test_prefill_argument_errors(lib):
     assert call_prefill(lib, desc(), hq=3) == 3                      # Hq % Hkv != 0
     assert call_prefill(lib, desc(), mql=-5) == 3
     assert call_prefill(lib, desc(), scale=float("nan")) == 3
+    assert call_prefill(lib, desc(), scale=-0.1) == 3                 # softmax scale must be positive
+    assert call_prefill(lib, desc(), scale=0.0) == 3
     assert call_prefill(lib, desc(), q=None) == 1
     assert call_prefill(lib, desc(), qs=None) == 1
     assert call_prefill(lib, desc(), out=FAKE + 8) == 5               # 16-byte alignment
