@@ -229,28 +229,17 @@ int pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cach
   if ((long long)max_blocks_per_seq * cache->block_size > kInt32Max) return PA_ERR_TOO_LARGE;
   if ((long long)num_query_tokens * num_q_heads * 128 > ((long long)1 << 40)) return PA_ERR_TOO_LARGE;
 
-  // q viewed as [tokens][Hq][D]: a 3-D map whose box is 128 tokens of one head, 64 columns
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return PA_ERR_CUDA;
-  CUtensorMap tq, tk, tv;
-  {
-    // rows past num_query_tokens are never read: the copy fills them with zeros
-    cuuint64_t dims[3] = {128, (cuuint64_t)num_q_heads, (cuuint64_t)num_query_tokens};
-    cuuint64_t strides[2] = {256, (cuuint64_t)num_q_heads * 256};
-    cuuint32_t box[3] = {64, 1, 128};
-    cuuint32_t estr[3] = {1, 1, 1};
-    const CUtensorMapDataType dt =
-        cache->dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    if (enc(&tq, dt, 3, const_cast<void*>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return PA_ERR_CUDA;
-  }
+  CUtensorMap tk, tv;
   if (!encode_cache_map(&tk, k_cache, cache, cache->block_size) ||
       !encode_cache_map(&tv, v_cache, cache, cache->block_size))
     return PA_ERR_CUDA;
   pa::PrefillParams p;
   p.out = out;
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
   p.block_tables = block_tables;
   p.seq_lens = seq_lens;
   p.query_start = query_start;
@@ -264,7 +253,7 @@ int pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cach
   p.q_tiles = (int32_t)q_tiles;
   p.num_query_tokens = num_query_tokens;
   p.scale_log2 = scale * 1.4426950408889634f;
-  cudaError_t e = pa::launch_prefill_tc(cache->dtype, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  cudaError_t e = pa::launch_prefill_tc(cache->dtype, tk, tv, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -31,6 +31,9 @@ struct DecodeParams {
 // Parameters of one chunked-prefill launch.
 struct PrefillParams {
   void* out;                    // [total_q][Hq][D]
+  const void* q;                // [total_q][Hq][D]
+  const void* k_cache;          // [num_blocks][Hkv][B][D]
+  const void* v_cache;
   const int32_t* block_tables;  // [N][M]
   const int32_t* seq_lens;      // [N] cached tokens including the chunk
   const int32_t* query_start;   // [N + 1]
@@ -43,8 +46,8 @@ struct PrefillParams {
 };
 
 // Kernel launchers (return the cudaGetLastError of the launch).
-cudaError_t launch_prefill_tc(int dtype, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const PrefillParams& p, cudaStream_t stream);
+cudaError_t launch_prefill_tc(int dtype, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                              cudaStream_t stream);
 cudaError_t launch_decode_tc(int dtype, int head_size, int block_size, const CUtensorMap& tk, const CUtensorMap& tv,
                              const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_f32(int head_size, const float* k_cache, const float* v_cache, const DecodeParams& p,

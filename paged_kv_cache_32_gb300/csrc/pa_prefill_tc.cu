@@ -10,33 +10,44 @@
 // 0..p: out = softmax_i(scale * q . k_i) v_i.  Keys and values of token i come
 // from offset i % B of block block_tables[s][i / B] (section "软件地址翻译").
 //
-// How (one CTA per sequence, query head and tile of 128 queries; 9 warps):
-//  * Data: the query tile is fetched once by a 3-D tensor-map copy; key and
-//    value tiles of 128 tokens are gathered block by block through the block
-//    table with 2-D tensor-map copies (128-byte swizzle) into two-stage K and
-//    V rings.  Each copy (one block, one 64-column half) is issued by its own
-//    thread, which arrives on the stage barrier with the bytes it copies.
-//  * Tensor memory (512 columns): two S buffers (0..127, 128..255) and two
-//    output accumulators O0, O1 (256..383, 384..511).
-//  * Warp 8 (one thread) issues every MMA: S = Q K^T (M = 128 queries,
-//    N = 128 keys, K = D; A and B from shared memory) and O_g += P_g V_g
-//    (A = P from tensor memory, B = V from shared memory), kind::f16 with fp32
-//    accumulation.  S of tile kt + 2 goes into the buffer of tile kt once
-//    P V of tile kt has finished, so the softmax of tile kt + 1 overlaps both.
+// How (one CTA per sequence, query head and tile of 128 queries; 12 warps):
+//  * Tensor memory (512 columns): two S buffers (0..127, 128..255), the
+//    output accumulator O (256..383) and the query tile Q (384..447, two
+//    16-bit elements per column).  Q is written there once by the first four
+//    warps straight from global memory, so both MMAs take their A operand
+//    from tensor memory; only K and V stream through shared memory (an
+//    MMA with both operands in shared memory runs at about half rate at this
+//    shape, limited by the shared-memory read bandwidth).
+//  * Data: key and value tiles of 128 tokens are gathered block by block
+//    through the block table by two producer warps (one for K, one for V)
+//    with 2-D tensor-map copies (one per block and 64-column half, 128-byte
+//    swizzle) into two-stage rings; each copy's lane arrives on the stage
+//    barrier with its bytes.  A producer refills a stage as soon as the MMA
+//    that read it has finished.  Value rows past the sequence must read as
+//    zeros (P is 0 there, but 0 * NaN is not): the V producer copies the
+//    last, partial block row by row with cp.async and zero-fills the rest,
+//    then fences those generic-proxy writes before its extra arrival.
+//  * Two threads in different warps issue the MMAs (kind::f16, fp32
+//    accumulation): warp 11 S = Q K^T (M = 128 queries, N = 128 keys, K = D),
+//    warp 8 O += P V (M = 128, N = D, K = 128 keys; P from tensor memory).
+//    S of tile kt + 2 goes into the buffer of tile kt once P V of tile kt has
+//    finished; with separate issuers that wait never delays the next P V, and
+//    the softmax of tile kt + 1 overlaps P V of tile kt and S of tile kt + 2.
 //  * Warps 0..7 run the softmax as two groups: group g owns keys
-//    64g .. 64g + 63 of every key tile (columns of S), with its own running
-//    max m_g, sum l_g and accumulator O_g for every query row (thread = row
-//    in the 32x32b tensor-memory layout, no cross-thread reduction).  P is
-//    written back into the S columns it came from (tcgen05.st) and consumed
-//    there by the P V MMA; bf16 P is written as two terms hi + lo (two MMAs),
-//    since 8 significant bits alone would cost up to 2^-8 of each weight.
+//    64g .. 64g + 63 of every key tile (columns of S); thread = query row in
+//    the 32x32b tensor-memory layout.  The groups exchange their tile row
+//    maxima through shared memory, so both use one reference max per row and
+//    accumulate into the same O.  P is written back into the S columns it
+//    came from (tcgen05.st); bf16 P is written as two terms hi + lo (two
+//    MMAs), since 8 significant bits alone would cost up to 2^-8 of a weight.
 //  * Rescaling: a row's reference max moves only when the tile max exceeds it
-//    by more than 8 (log2 units), so P <= 2^8 and O_g is rescaled in place
-//    (tcgen05.ld / st) on few tiles.  The epilogue merges the two groups:
-//    out = (O0 2^(m0-M) + O1 2^(m1-M)) / (l0 2^(m0-M) + l1 2^(m1-M)).
+//    by more than 8 (log2 units), so P <= 2^8 and O is rescaled in place
+//    (tcgen05.ld / st, each group its 64 columns) on few tiles.
+//  * Epilogue: out = O / (l0 + l1), each group writing its 64 columns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <climits>
 #include <math.h>
 
 #include <type_traits>
@@ -51,14 +62,18 @@ namespace {
 constexpr int kTile = 128;            // queries per CTA = keys per key tile
 constexpr int kD = 128;               // head size of this kernel
 constexpr int kHalf = kTile * 128;    // one 128-row x 128-byte swizzled region (16 KB)
-constexpr int kQOff = 0;              // Q: 2 regions (dims 0-63, 64-127)
-constexpr int kKOff = 2 * kHalf;      // K stages: 2 x 2 regions
-constexpr int kVOff = 6 * kHalf;      // V stages: 2 x 2 regions
-constexpr int kBarOff = 10 * kHalf;   // barriers, flags, the (m, l) exchange
-constexpr int kSmemBytes = kBarOff + 128 + 2 * kTile * 8 + 1024;
+constexpr int kKOff = 0;              // K stages: 2 x 2 regions (dims 0-63, 64-127)
+constexpr int kVOff = 4 * kHalf;      // V stages: 2 x 2 regions
+constexpr int kBarOff = 8 * kHalf;    // barriers, flags, the row-max and row-sum exchange
+constexpr int kSmemBytes = kBarOff + 128 + 2 * 2 * kTile * 4 + 2 * kTile * 4 + 1024;
+constexpr uint32_t kOCol = 256;       // tensor-memory column of O
+constexpr uint32_t kQCol = 384;       // tensor-memory column of Q
 constexpr int kSoftmaxWarps = 8;
-constexpr int kThreads = (kSoftmaxWarps + 1) * 32;
-constexpr int kControlWarp = kSoftmaxWarps;
+constexpr int kPVWarp = kSoftmaxWarps;     // issues O += P V
+constexpr int kKLoadWarp = kSoftmaxWarps + 1;
+constexpr int kVLoadWarp = kSoftmaxWarps + 2;
+constexpr int kSWarp = kSoftmaxWarps + 3;  // issues S = Q K^T
+constexpr int kThreads = (kSoftmaxWarps + 4) * 32;
 constexpr float kRescaleThreshold = 8.f;  // log2 units: P <= 2^8 between rescales
 constexpr long long kWaitCyclesPf = 500ll * 1000 * 1000;
 
@@ -69,11 +84,25 @@ constexpr bool split_p() {
   return std::is_same<T, __nv_bfloat16>::value;
 }
 
+// try_wait that lets the hardware park the thread (up to ~20 us) until the phase completes,
+// instead of spinning on the barrier and taking issue slots from the softmax warps
+__device__ __forceinline__ bool mbar_try_wait_parked(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
+      : "memory");
+  return ok != 0;
+}
+
 // bounded wait; gives up at once when another thread has recorded a failure
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait_parked(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_parked(bar, parity)) {
     if (*abort_flag) return false;
     if (clock64() - t0 > kWaitCyclesPf) {
       *abort_flag = 1;
@@ -103,15 +132,6 @@ __device__ __forceinline__ constexpr uint32_t idesc(uint32_t b_mn) {
   constexpr uint32_t ab = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
   return (1u << 4) | (ab << 7) | (ab << 10) | (b_mn << 16) | ((uint32_t)(kTile >> 3) << 17) |
          ((uint32_t)(kTile >> 4) << 24);
-}
-
-// D (tensor memory) (+)= A (shared memory) x B (shared memory)
-__device__ __forceinline__ void mma_ss(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t id, bool accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(a), "l"(b), "r"(id), "r"((uint32_t)accumulate)
-      : "memory");
 }
 
 // D (tensor memory) (+)= A (tensor memory, row m in lane m, 2 elements per column) x B (shared memory)
@@ -195,14 +215,11 @@ __device__ __forceinline__ float2 sub2(float2 a, float2 b) {
   return bits_f2(d);
 }
 
-__device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, int32_t x, int32_t y, int32_t z,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
-          "r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-      : "memory");
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
 }
+// all of this thread's cp.async copies have landed (commits the pending ones first)
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // P of one row's 64 keys (two per 32-bit column, lower key in the low half) from
 // the scores v (raw q . k), the scale in log2 units and the reference max; keys
@@ -211,7 +228,7 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, in
 template <typename T, bool kMasked>
 __device__ __forceinline__ float make_p(const float* v, float sl2, float m_ref, int lim, uint32_t* hi,
                                         uint32_t* lo) {
-  float2 acc = make_float2(0.f, 0.f);
+  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
   const float2 s2 = make_float2(sl2, sl2), nm2 = make_float2(-m_ref, -m_ref);
 #pragma unroll
   for (int i = 0; i < 64; i += 2) {
@@ -221,7 +238,7 @@ __device__ __forceinline__ float make_p(const float* v, float sl2, float m_ref, 
       e0 = i <= lim ? e0 : 0.f;
       e1 = i + 1 <= lim ? e1 : 0.f;
     }
-    acc = add2(acc, make_float2(e0, e1));
+    acc[(i >> 1) & 3] = add2(acc[(i >> 1) & 3], make_float2(e0, e1));
     if constexpr (split_p<T>()) {
       // hi = e truncated to bf16 (exact as a float), lo = the remainder rounded to bf16
       const uint32_t b0 = __float_as_uint(e0), b1 = __float_as_uint(e1);
@@ -233,15 +250,16 @@ __device__ __forceinline__ float make_p(const float* v, float sl2, float m_ref, 
       hi[i / 2] = Mma<T>::pack(e0, e1);
     }
   }
-  return acc.x + acc.y;
+  const float2 t = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+  return t.x + t.y;
 }
 
 }  // namespace
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                      const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                      const PrefillParams p) {
   // ---- work item
   const int tiles = p.q_tiles;
   const int qt = tiles - 1 - (int)(blockIdx.x % tiles);  // the longest (last) query tiles start first
@@ -264,34 +282,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int pos0 = L - n + tile0;                       // position of query row 0
   const int key_tiles = (pos0 + rows - 1) / kTile + 1;  // key tiles reaching the last row's position
   const int blocks_per_tile = kTile / B;
-  const int slots = 2 * blocks_per_tile;                // copies per K (or V) tile: one per block and half
+  const int slots = 2 * blocks_per_tile;                // tensor-map copies per tile: one per block and half
   const int32_t* table = p.block_tables + (size_t)s * p.max_blocks;
   const int nblocks_seq = (L + B - 1) / B;              // <= max_blocks (checked above)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bar_q = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  uint64_t* bar_k = bar_q + 1;  // [2] K stage landed
-  uint64_t* bar_v = bar_q + 3;  // [2] V stage landed
-  uint64_t* bar_s = bar_q + 5;  // [2] S buffer computed
-  uint64_t* bar_p = bar_q + 7;  // [2] P of the buffer written by all softmax warps
-  uint64_t* bar_o = bar_q + 9;  // O += P V done
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 96);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 104);
-  float2* ml = reinterpret_cast<float2*>(smem + kBarOff + 128);  // [2][128] (m, l) per group and row
+  uint64_t* bar_q = reinterpret_cast<uint64_t*>(smem + kBarOff);  // Q written into tensor memory
+  uint64_t* bar_k = bar_q + 1;     // [2] K stage filled
+  uint64_t* bar_v = bar_q + 3;     // [2] V stage filled
+  uint64_t* bar_s = bar_q + 5;     // [2] S buffer computed
+  uint64_t* bar_p = bar_q + 7;     // [2] P of the buffer written by all softmax warps
+  uint64_t* bar_o = bar_q + 9;     // [2] O += P V of the tile in V stage b done (one phase per tile held)
+  uint64_t* bar_done = bar_q + 11; // every P V done
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 112);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 120);
+  float* xmax = reinterpret_cast<float*>(smem + kBarOff + 128);  // [2 tiles][2 groups][128] row maxima
+  float* xsum = xmax + 2 * 2 * kTile;                             // [2 groups][128] row sums
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int n_s = 0, n_o = 0;  // S / P V commits (control thread)
-  int n_k = 0, n_v = 0;  // K / V tiles requested (uniform over the softmax warps)
+  int n_issued = 0;      // tiles whose copies this producer warp has issued
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1);
+    mbar_init(bar_q, 4);  // the four warps that write Q
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&bar_k[b], slots);  // every copy slot arrives once per tile (with its bytes, or none)
-      mbar_init(&bar_v[b], slots);
+      mbar_init(&bar_k[b], slots);      // each copy slot arrives once per tile (with its bytes, or none)
+      mbar_init(&bar_v[b], slots + 1);  // + the partial-block / zero-fill arrival
       mbar_init(&bar_s[b], 1);
       mbar_init(&bar_p[b], kSoftmaxWarps);
+      mbar_init(&bar_o[b], 1);
     }
-    mbar_init(bar_o, 1);
+    mbar_init(bar_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -305,86 +326,117 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
-  // physical block of block i of key tile kt: -1 past the sequence, -2 for an ID outside the pool
-  auto block_id = [&](int kt, int i) -> int {
-    const int bi = kt * blocks_per_tile + i;
-    if (bi >= nblocks_seq) return -1;
-    const int pb = __ldg(table + bi);
-    return (pb >= 0 && pb < p.num_blocks) ? pb : -2;
-  };
-  // copy slot c = lane * 8 + warp (block c / 2, column half c % 2), softmax warps only: each slot's
-  // thread arrives on the stage barrier with the bytes it is about to copy
-  auto load_tile = [&](bool is_v, int kt) {
-    const int c = lane * kSoftmaxWarps + warp;
-    if (c >= slots) return;
-    uint64_t* bar = is_v ? &bar_v[kt & 1] : &bar_k[kt & 1];
-    const int i = c >> 1, half = c & 1;
-    const int pb = block_id(kt, i);
-    if (pb < 0) {
-      if (pb == -2 && !is_v && half == 0) report_error(p.err_flag, PA_DEVERR_BLOCK_ID);
-      mbar_arrive(bar);
-      return;
-    }
-    mbar_arrive_expect_tx(bar, (uint32_t)B * 128);
-    uint8_t* dst = smem + (is_v ? kVOff : kKOff) + (kt & 1) * 2 * kHalf + half * kHalf + i * B * 128;
-    tma_load_2d(dst, is_v ? (const void*)&tmap_v : (const void*)&tmap_k, half * 64, (pb * p.num_kv_heads + hkv) * B,
-                bar);
+  // a wait whose outcome every lane of the warp shares (warp-collective instructions follow)
+  auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag));
   };
 
-  if (warp == kControlWarp) {
-    // =================================================================== control warp: every MMA
-    if (lane == 0) {
-      const uint32_t id_s = idesc<T>(0), id_o = idesc<T>(1);
-      auto issue_s = [&](int kt) {  // S buffer kt % 2 = Q K^T of key tile kt
-        const uint32_t qb = smem_u32(smem + kQOff), kb = smem_u32(smem + kKOff + (kt & 1) * 2 * kHalf);
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          mma_ss(tmem + (kt & 1) * 128, sw128_desc(qb + off, 16, 1024), sw128_desc(kb + off, 16, 1024), id_s, kk > 0);
-        }
-        mma_commit(&bar_s[kt & 1]);
-        ++n_s;
-      };
-      tma_prefetch_descriptor(&tmap_q);
-      mbar_arrive_expect_tx(bar_q, 2 * kHalf);
-      for (int half = 0; half < 2; ++half)
-        tma_load_3d(smem + kQOff + half * kHalf, &tmap_q, half * 64, h, q0 + tile0, bar_q);
-      bool ok = wait_bar(bar_q, 0, abort_flag);
-      for (int t = 0; ok && t < 2 && t < key_tiles; ++t) {
-        ok = wait_bar(&bar_k[t], 0, abort_flag);
-        if (ok) {
-          tc_fence_after();
-          issue_s(t);
+  if (warp == kKLoadWarp || warp == kVLoadWarp) {
+    // =================================================================== producers: K or V tiles
+    const bool is_v = warp == kVLoadWarp;
+    const T* cache = static_cast<const T*>(is_v ? p.v_cache : p.k_cache);
+    const CUtensorMap* tmap = is_v ? &tmap_v : &tmap_k;
+    uint8_t* ring = smem + (is_v ? kVOff : kKOff);
+    constexpr int kPastEnd = INT_MIN;
+    // lane c < slots copies block c / 2, column half c % 2 of every tile; its table entry is read one tile ahead
+    const int blk = lane >> 1, half = lane & 1;
+    auto fetch = [&](int kt) -> int {
+      const int bi = kt * blocks_per_tile + blk;
+      return (lane < slots && kt < key_tiles && bi < nblocks_seq) ? __ldg(table + bi) : kPastEnd;
+    };
+    if (lane == 0) tma_prefetch_descriptor(tmap);
+    int entry_next = fetch(0);
+    for (int t = 0; t < key_tiles; ++t) {
+      // the stage of tile t held tile t - 2: wait until the MMA that read it has finished (the
+      // stage's barrier has one phase per tile held; its next phase needs this tile, so the wait is exact)
+      if (t >= 2 && !warp_wait(is_v ? &bar_o[t & 1] : &bar_s[t & 1], ((t - 2) >> 1) & 1)) break;
+      const int entry = entry_next;
+      entry_next = fetch(t + 1);
+      uint64_t* bar = is_v ? &bar_v[t & 1] : &bar_k[t & 1];
+      uint8_t* st = ring + (t & 1) * 2 * kHalf;
+      const bool in_pool = entry >= 0 && entry < p.num_blocks;
+      if (!is_v && half == 0 && entry != kPastEnd && !in_pool) report_error(p.err_flag, PA_DEVERR_BLOCK_ID);
+      // V: only blocks entirely inside the sequence go by tensor-map copy
+      const bool whole = in_pool && (!is_v || (t * blocks_per_tile + blk + 1) * B <= L);
+      if (lane < slots) {
+        if (whole) {
+          mbar_arrive_expect_tx(bar, (uint32_t)B * 128);
+          tma_load_2d(st + half * kHalf + blk * B * 128, tmap, half * 64, (entry * p.num_kv_heads + hkv) * B, bar);
+        } else {
+          mbar_arrive(bar);
         }
       }
+      if (is_v) {
+        // blocks not copied above: rows inside the sequence of an in-pool block by cp.async, the rest zeros
+        const unsigned partial = __ballot_sync(0xffffffffu, lane < slots && half == 0 && !whole);
+        if (partial) {
+          for (int r = lane >> 4; r < kTile; r += 2) {  // 16 chunks of 16 bytes per row, two rows per step
+            const int b = r / B;
+            if (!((partial >> (2 * b)) & 1)) continue;
+            const int e = __shfl_sync(__activemask(), entry, 2 * b);
+            const int pos = t * kTile + r, chunk = lane & 15;
+            uint8_t* dst = st + (chunk >> 3) * kHalf + swz128(r, chunk & 7);
+            if (pos < L && e >= 0 && e < p.num_blocks)
+              cp_async16(dst, cache + (((size_t)e * p.num_kv_heads + hkv) * B + (pos % B)) * kD + chunk * 8);
+            else
+              *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+          }
+          cp_async_wait_all();
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor-core reads
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar);
+      }
+      ++n_issued;
+    }
+  } else if (warp == kSWarp) {
+    // =================================================================== S = Q K^T issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc<T>(0);
+      bool ok = wait_bar(bar_q, 0, abort_flag);
+      for (int t = 0; ok && t < key_tiles; ++t) {
+        // buffer t % 2 held P of tile t - 2 (its P V must have finished; the barrier's next phase,
+        // tile t, needs this S, so the wait is exact) and K stage t % 2 must hold key tile t
+        if (t >= 2) ok = wait_bar(&bar_o[t & 1], ((t - 2) >> 1) & 1, abort_flag);
+        ok = ok && wait_bar(&bar_k[t & 1], (t >> 1) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t kb = smem_u32(smem + kKOff + (t & 1) * 2 * kHalf);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ts(tmem + (t & 1) * 128, tmem + kQCol + kk * 8,
+                 sw128_desc(kb + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
+        mma_commit(&bar_s[t & 1]);
+        ++n_s;
+      }
+    }
+    __syncwarp();
+  } else if (warp == kPVWarp) {
+    // =================================================================== O += P V issuer
+    if (lane == 0) {
+      const uint32_t id_o = idesc<T>(1);
+      bool ok = true;
       for (int kt = 0; ok && kt < key_tiles; ++kt) {
         const int buf = kt & 1;
-        // O_g += P_g V_g once every softmax warp has written P of tile kt and V of tile kt has landed
+        // once every softmax warp has written P of tile kt and V of tile kt is in place
         ok = wait_bar(&bar_p[buf], (kt >> 1) & 1, abort_flag) && wait_bar(&bar_v[buf], (kt >> 1) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
         const uint32_t vb = smem_u32(smem + kVOff + buf * 2 * kHalf);
+        // keys 64g + 16kk' of the tile: P hi (lo) of group g in columns 64g (+ 32) + 8kk' of the buffer
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
+        for (int part = 0; part < (split_p<T>() ? 2 : 1); ++part) {
 #pragma unroll
-          for (int part = 0; part < (split_p<T>() ? 2 : 1); ++part) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ts(tmem + 256 + 128 * g, tmem + buf * 128 + 64 * g + part * 32 + kk * 8,
-                     sw128_desc(vb + g * 8192 + kk * 2048, kHalf, 1024), id_o, kt > 0 || part > 0 || kk > 0);
-          }
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ts(tmem + kOCol, tmem + buf * 128 + 64 * (kk >> 2) + part * 32 + (kk & 3) * 8,
+                   sw128_desc(vb + kk * 2048, kHalf, 1024), id_o, kt > 0 || part > 0 || kk > 0);
         }
-        mma_commit(bar_o);
+        mma_commit(&bar_o[buf]);
         ++n_o;
-        if (kt + 2 < key_tiles) {
-          // S of tile kt + 2 overwrites this buffer (P of tile kt): after that P V has finished
-          ok = wait_bar(bar_o, kt & 1, abort_flag) && wait_bar(&bar_k[buf], ((kt + 2) >> 1) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(kt + 2);
-        }
       }
+      // the last P V on each stage barrier (earlier ones finished before the S that fed the later P)
+      for (int t = max(0, n_o - 2); ok && t < n_o; ++t) ok = wait_bar(&bar_o[t & 1], (t >> 1) & 1, abort_flag);
+      if (ok && n_o == key_tiles) mbar_arrive(bar_done);
     }
     __syncwarp();
   } else {
@@ -392,30 +444,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = warp >> 2;                         // key columns 64g .. 64g + 63 of every tile
     const int row = (warp & 3) * 32 + lane;          // query row = tensor-memory lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t o_addr = tmem + lane_base + 256 + 128 * g;
+    const uint32_t o_addr = tmem + lane_base + kOCol + 64 * g;  // this group's 64 columns of O
+    if (g == 0) {
+      // Q row -> tensor memory columns kQCol.. (two elements per column, lower index in the low half)
+      uint32_t qw[64];
+      if (row < rows) {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
+                                                          ((size_t)(q0 + tile0 + row) * p.num_q_heads + h) * kD);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint4 u = __ldg(src + i);
+          qw[4 * i] = u.x, qw[4 * i + 1] = u.y, qw[4 * i + 2] = u.z, qw[4 * i + 3] = u.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) qw[i] = 0;
+      }
+      tmem_st32(tmem + lane_base + kQCol, qw);
+      tmem_st32(tmem + lane_base + kQCol + 32, qw + 32);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_q);
+    }
     const float sl2 = p.scale_log2;
     const int lim_base = min(pos0 + row, L - 1);     // last key position this row sees
     float m_ref = -INFINITY, l_run = 0.f;
-    // a wait whose outcome every lane of the warp shares (warp-collective tensor-memory ops follow)
-    auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
-      return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag));
-    };
-    for (int t = 0; t < 2 && t < key_tiles; ++t) {
-      load_tile(false, t);
-      load_tile(true, t);
-      ++n_k;
-      ++n_v;
-    }
     bool ok = true;
+    // Every softmax warp runs all key_tiles iterations and passes the named barrier of each: after a
+    // failure the waits return at once (the abort flag is set) and the arithmetic is just discarded,
+    // so no warp can be left waiting on a barrier that another warp has stopped visiting.
     for (int kt = 0; kt < key_tiles; ++kt) {
       const int buf = kt & 1;
-      ok = warp_wait(&bar_s[buf], (kt >> 1) & 1);
-      if (!ok) break;
+      ok = warp_wait(&bar_s[buf], (kt >> 1) & 1) && ok;
       tc_fence_after();
-      if (kt + 2 < key_tiles) {  // S(kt) done: its K stage takes key tile kt + 2
-        load_tile(false, kt + 2);
-        ++n_k;
-      }
       const uint32_t s_addr = tmem + lane_base + buf * 128 + 64 * g;
       float v[64];
       tmem_ld32(s_addr, v);
@@ -423,30 +485,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld<64>(v);
       const int lim = lim_base - (kt * kTile + 64 * g);  // keys 0..lim of these 64 are visible
       const bool unmasked = __all_sync(0xffffffffu, lim >= 63);
-      // ---- the tile's row max, and the reference max it implies
-      float mx = -INFINITY;
+      // ---- the tile's row max over both groups, and the reference max it implies
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
       if (unmasked) {
 #pragma unroll
-        for (int i = 0; i < 64; i += 2) mx = max3(mx, v[i], v[i + 1]);
+        for (int i = 0; i < 64; i += 2) mq[(i >> 1) & 3] = max3(mq[(i >> 1) & 3], v[i], v[i + 1]);
       } else {
 #pragma unroll
         for (int i = 0; i < 64; i += 2)
-          mx = max3(mx, i <= lim ? v[i] : -INFINITY, i + 1 <= lim ? v[i + 1] : -INFINITY);
+          mq[(i >> 1) & 3] = max3(mq[(i >> 1) & 3], i <= lim ? v[i] : -INFINITY, i + 1 <= lim ? v[i + 1] : -INFINITY);
       }
-      const float mx_s = mx * sl2;  // scale > 0
+      float* xm = xmax + buf * 2 * kTile;  // two buffers: tile kt + 2 writes after tile kt + 1's exchange
+      xm[g * kTile + row] = fmaxf(max3(mq[0], mq[1], mq[2]), mq[3]);
+      asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxWarps * 32) : "memory");
+      const float mx_s = fmaxf(xm[row], xm[kTile + row]) * sl2;  // scale > 0; the same in both groups
       const bool upd = mx_s > m_ref + kRescaleThreshold;
       const float alpha = upd ? fast_exp2(m_ref - mx_s) : 1.f;
-      // P V of tile kt - 1 is confirmed once per tile, in order (phase kt - 1 of bar_o; phase kt cannot
-      // complete before this warp's P arrival below): first here if O must be rescaled, else before the arrival
-      bool o_prev_done = kt == 0;
-      if (__any_sync(0xffffffffu, upd) && kt > 0) {
-        // O_g of these rows is rescaled between P V of tile kt - 1 (done) and that of tile kt
-        ok = warp_wait(bar_o, (kt - 1) & 1);
-        if (!ok) break;
-        o_prev_done = true;
+      if (__any_sync(0xffffffffu, upd) && kt > 0 && ok) {
+        // O of these rows (this group's columns) is rescaled between P V of tile kt - 1 and that of
+        // tile kt.  The barrier of its V stage finished tile kt - 3 before S(kt - 1) was issued and its
+        // next phase (tile kt + 1) needs this warp's P, so the parity wait below is exact.
+        ok = warp_wait(&bar_o[(kt - 1) & 1], ((kt - 1) >> 1) & 1);
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           float o[32];
           tmem_ld32(o_addr + c * 32, o);
           tmem_wait_ld<32>(o);
@@ -465,60 +527,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32(s_addr, hi);
       if constexpr (split_p<T>()) tmem_st32(s_addr + 32, lo);
       tmem_wait_st();
-      // ---- values of key rows past the sequence (or of blocks not loaded) may hold NaN: zero them
-      if (kt * kTile + kTile > L || (kt + 1) * blocks_per_tile > nblocks_seq) {
-        ok = warp_wait(&bar_v[buf], (kt >> 1) & 1);
-        if (!ok) break;
-        uint8_t* vst = smem + kVOff + buf * 2 * kHalf;
-        for (int idx = threadIdx.x; idx < kTile * 16; idx += kSoftmaxWarps * 32) {  // 128 rows x 16 chunks
-          const int r = idx >> 4, chunk = idx & 15;
-          if (kt * kTile + r >= L || block_id(kt, r / B) < 0)
-            *reinterpret_cast<uint4*>(vst + (chunk >> 3) * kHalf + swz128(r, chunk & 7)) = make_uint4(0, 0, 0, 0);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor-core reads
-      }
-      // ---- V stage (kt + 1) % 2 held tile kt - 1, whose P V is done: fetch value tile kt + 1 there
-      if (!o_prev_done) {
-        ok = warp_wait(bar_o, (kt - 1) & 1);
-        if (!ok) break;
-      }
-      if (kt >= 1 && kt + 1 < key_tiles) {
-        load_tile(true, kt + 1);
-        ++n_v;
-      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_p[buf]);
     }
-    // ---- epilogue: merge the two groups' (m, l, O) per row and write out (P V of every tile before
-    //      the last was confirmed inside the loop, so this parity wait cannot pass early)
-    if (ok) ok = warp_wait(bar_o, (key_tiles - 1) & 1);
-    ml[g * kTile + row] = make_float2(m_ref, l_run);
+    // ---- epilogue: out = O / (l0 + l1), this group's 64 columns
+    if (ok) ok = warp_wait(bar_done, 0);
+    xsum[g * kTile + row] = l_run;
     asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxWarps * 32) : "memory");
     if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
       tc_fence_after();
-      const float2 a = ml[row], b = ml[kTile + row];
-      const float M = fmaxf(a.x, b.x);
-      const float w0 = a.x == -INFINITY ? 0.f : fast_exp2(a.x - M), w1 = b.x == -INFINITY ? 0.f : fast_exp2(b.x - M);
-      const float den = a.y * w0 + b.y * w1;
+      const float den = xsum[row] + xsum[kTile + row];
       const float inv = den > 0.f ? 1.f / den : 0.f;
-      const float c0 = w0 * inv, c1 = w1 * inv;
       T* out = reinterpret_cast<T*>(p.out) + ((size_t)(q0 + tile0 + row) * p.num_q_heads + h) * kD + 64 * g;
 #pragma unroll 1
-      for (int c = 0; c < 2; ++c) {  // this group writes output columns 64g .. 64g + 63
-        float o0[32], o1[32];
-        tmem_ld32(tmem + lane_base + 256 + 64 * g + 32 * c, o0);
-        tmem_ld32(tmem + lane_base + 384 + 64 * g + 32 * c, o1);
-        tmem_wait_ld<32>(o0);
-        tmem_wait_ld<32>(o1);
+      for (int c = 0; c < 2; ++c) {
+        float o[32];
+        tmem_ld32(o_addr + 32 * c, o);
+        tmem_wait_ld<32>(o);
         if (row < rows) {
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             uint4 val;
-            val.x = Mma<T>::pack(o0[i] * c0 + o1[i] * c1, o0[i + 1] * c0 + o1[i + 1] * c1);
-            val.y = Mma<T>::pack(o0[i + 2] * c0 + o1[i + 2] * c1, o0[i + 3] * c0 + o1[i + 3] * c1);
-            val.z = Mma<T>::pack(o0[i + 4] * c0 + o1[i + 4] * c1, o0[i + 5] * c0 + o1[i + 5] * c1);
-            val.w = Mma<T>::pack(o0[i + 6] * c0 + o1[i + 6] * c1, o0[i + 7] * c0 + o1[i + 7] * c1);
+            val.x = Mma<T>::pack(o[i] * inv, o[i + 1] * inv);
+            val.y = Mma<T>::pack(o[i + 2] * inv, o[i + 3] * inv);
+            val.z = Mma<T>::pack(o[i + 4] * inv, o[i + 5] * inv);
+            val.w = Mma<T>::pack(o[i + 6] * inv, o[i + 7] * inv);
             *reinterpret_cast<uint4*>(out + 32 * c + i) = val;
           }
         }
@@ -530,23 +564,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (*abort_flag) {
     // a wait expired (the flag is stable: every thread has left its loop): record it, and let the
     // copies and MMAs this CTA started finish, each wait bounded, before its memory is released
-    if (threadIdx.x == 0) {
-      report_error(p.err_flag, PA_DEVERR_TIMEOUT);
-      for (int t = max(0, n_k - 2); t < n_k; ++t) drain_wait(&bar_k[t & 1], (t >> 1) & 1);
-      for (int t = max(0, n_v - 2); t < n_v; ++t) drain_wait(&bar_v[t & 1], (t >> 1) & 1);
+    if (threadIdx.x == 0) report_error(p.err_flag, PA_DEVERR_TIMEOUT);
+    if ((warp == kKLoadWarp || warp == kVLoadWarp) && lane == 0) {  // copies still landing
+      uint64_t* ring_bar = warp == kVLoadWarp ? bar_v : bar_k;
+      for (int t = max(0, n_issued - 2); t < n_issued; ++t) drain_wait(&ring_bar[t & 1], (t >> 1) & 1);
     }
-    if (warp == kControlWarp && lane == 0) {
+    if (warp == kSWarp && lane == 0)
       for (int t = max(0, n_s - 2); t < n_s; ++t) drain_wait(&bar_s[t & 1], (t >> 1) & 1);
-      if (n_o > 0) drain_wait(bar_o, (n_o - 1) & 1);
-    }
+    if (warp == kPVWarp && lane == 0)
+      for (int t = max(0, n_o - 2); t < n_o; ++t) drain_wait(&bar_o[t & 1], (t >> 1) & 1);
     __syncthreads();
   }
   if (warp == 0)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512u) : "memory");
 }
 
-cudaError_t launch_prefill_tc(int dtype, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const PrefillParams& p, cudaStream_t stream) {
+cudaError_t launch_prefill_tc(int dtype, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                              cudaStream_t stream) {
   const long long grid = (long long)p.num_seqs * p.num_q_heads * p.q_tiles;
   if (grid == 0) return cudaSuccess;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -554,12 +588,12 @@ cudaError_t launch_prefill_tc(int dtype, const CUtensorMap& tq, const CUtensorMa
     cudaError_t e =
         cudaFuncSetAttribute(prefill_tc_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<__half><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+    prefill_tc_kernel<__half><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(tk, tv, p);
   } else if (dtype == PA_BF16) {
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<__nv_bfloat16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<__nv_bfloat16><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+    prefill_tc_kernel<__nv_bfloat16><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(tk, tv, p);
   } else {
     return cudaErrorInvalidValue;
   }
