@@ -64,10 +64,14 @@ def measured_peaks():
 KERNEL_SOURCES = ("pa_api.cu", "pa_decode_tc.cu", "pa_device.cuh", "pa_internal.h", "pa_merge_and_cache.cu")
 
 
-def kernel_source_hash() -> str:
+# sources that define the prefill call's kernel
+PREFILL_SOURCES = ("pa_prefill_api.cu", "pa_prefill_tc.cu", "pa_prefill.h", "pa_device.cuh", "pa_internal.h")
+
+
+def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_32_gb300", "csrc")
-    for fn in KERNEL_SOURCES:
+    for fn in sources:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
@@ -83,7 +87,8 @@ def ncu_traffic(workload: str):
     except (OSError, ValueError):
         return None
     entry = rec.get(workload)
-    if not entry or entry.get("source_sha") != kernel_source_hash():
+    sources = PREFILL_SOURCES if workload.startswith("prefill") else KERNEL_SOURCES
+    if not entry or entry.get("source_sha") != kernel_source_hash(sources):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -525,7 +530,7 @@ def bench_prefill(name: str, device, steps: int, warmup: int, peaks):
             "query_tokens_per_s": round(T / (ms_step * 1e-3), 1), "gpu_launches": 2 * steps,
             "roofline": {"bound": "tensor", "kernel": "pa_prefill (prefill_tc_kernel)", "achieved": round(tflops, 1),
                          "peak": peak, "peak_source": peak_src, "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
-                         "traffic": None, "algorithmic_flops_per_launch": flops,
+                         "traffic": ncu_traffic(name), "algorithmic_flops_per_launch": flops,
                          "sustained_peak": (peaks or {}).get("bf16_tflops_sustained")},
             "l2": "q + out + K/V of the chunk's sequences exceed L2; no flush",
             "clocks": sampler.summary(t0, t1)}

@@ -11,10 +11,10 @@
 #include "pa.h"
 #include "pa_internal.h"
 
-namespace {
+namespace pa {
+namespace host {
 
 constexpr int32_t kDefaultPartition = 1024;  // tokens per partition when the caller passes 0 (measured best)
-constexpr int64_t kInt32Max = 2147483647;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -86,7 +86,10 @@ bool encode_cache_map(CUtensorMap* map, const void* base, const pa_cache_desc* c
   return r == CUDA_SUCCESS;
 }
 
-}  // namespace
+}  // namespace host
+}  // namespace pa
+
+using namespace pa::host;
 
 extern "C" {
 
@@ -204,57 +207,6 @@ int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_ca
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;
-}
-
-int pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
-               const int32_t* seq_lens, const int32_t* query_start, int32_t num_seqs, int32_t num_query_tokens,
-               int32_t num_q_heads, int32_t max_blocks_per_seq, int32_t max_query_len, const pa_cache_desc* cache,
-               float scale, int32_t* err_flag, void* stream) {
-  int rc = check_cache(cache);
-  if (rc != PA_OK) return rc;
-  if (cache->dtype == PA_F32 || cache->head_size != 128) return PA_ERR_UNSUPPORTED;
-  if (cache->block_size > 128 || 128 % cache->block_size != 0) return PA_ERR_UNSUPPORTED;
-  if (num_seqs < 0 || num_query_tokens < 0 || num_q_heads <= 0 || max_blocks_per_seq < 0 || max_query_len < 0)
-    return PA_ERR_INVALID_ARG;
-  if (num_q_heads % cache->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || isinf(scale)) return PA_ERR_INVALID_ARG;  // the row max is taken on unscaled scores
-  if (num_seqs == 0 || max_query_len == 0 || num_query_tokens == 0) return PA_OK;
-  if (out == nullptr || q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr ||
-      query_start == nullptr || block_tables == nullptr)
-    return PA_ERR_NULL_POINTER;
-  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 16))
-    return PA_ERR_MISALIGNED;
-  const long long q_tiles = (max_query_len + 127) / 128;
-  if ((long long)num_seqs * num_q_heads * q_tiles > kInt32Max) return PA_ERR_TOO_LARGE;
-  if ((long long)max_blocks_per_seq * cache->block_size > kInt32Max) return PA_ERR_TOO_LARGE;
-  if ((long long)num_query_tokens * num_q_heads * 128 > ((long long)1 << 40)) return PA_ERR_TOO_LARGE;
-
-  auto enc = tensor_map_encoder();
-  if (enc == nullptr) return PA_ERR_CUDA;
-  CUtensorMap tk, tv;
-  if (!encode_cache_map(&tk, k_cache, cache, cache->block_size) ||
-      !encode_cache_map(&tv, v_cache, cache, cache->block_size))
-    return PA_ERR_CUDA;
-  pa::PrefillParams p;
-  p.out = out;
-  p.q = q;
-  p.k_cache = k_cache;
-  p.v_cache = v_cache;
-  p.block_tables = block_tables;
-  p.seq_lens = seq_lens;
-  p.query_start = query_start;
-  p.err_flag = err_flag;
-  p.num_seqs = num_seqs;
-  p.num_q_heads = num_q_heads;
-  p.num_kv_heads = cache->num_kv_heads;
-  p.max_blocks = max_blocks_per_seq;
-  p.block_size = cache->block_size;
-  p.num_blocks = cache->num_blocks;
-  p.q_tiles = (int32_t)q_tiles;
-  p.num_query_tokens = num_query_tokens;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  cudaError_t e = pa::launch_prefill_tc(cache->dtype, tk, tv, p, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 int pa_reshape_and_cache(void* k_cache, void* v_cache, const void* key, const void* value,

@@ -4,7 +4,10 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
+
+#include "pa.h"
 
 namespace pa {
 
@@ -28,26 +31,7 @@ struct DecodeParams {
   const float* alibi;         // nullable [Hq]: score_i += slope_h * (i - (L - 1))
 };
 
-// Parameters of one chunked-prefill launch.
-struct PrefillParams {
-  void* out;                    // [total_q][Hq][D]
-  const void* q;                // [total_q][Hq][D]
-  const void* k_cache;          // [num_blocks][Hkv][B][D]
-  const void* v_cache;
-  const int32_t* block_tables;  // [N][M]
-  const int32_t* seq_lens;      // [N] cached tokens including the chunk
-  const int32_t* query_start;   // [N + 1]
-  int32_t* err_flag;            // nullable
-  int32_t num_seqs, num_q_heads, num_kv_heads;
-  int32_t max_blocks, block_size, num_blocks;
-  int32_t q_tiles;              // ceil(max_query_len / 128)
-  int32_t num_query_tokens;     // rows of q and out
-  float scale_log2;
-};
-
 // Kernel launchers (return the cudaGetLastError of the launch).
-cudaError_t launch_prefill_tc(int dtype, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
-                              cudaStream_t stream);
 cudaError_t launch_decode_tc(int dtype, int head_size, int block_size, const CUtensorMap& tk, const CUtensorMap& tv,
                              const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_f32(int head_size, const float* k_cache, const float* v_cache, const DecodeParams& p,
@@ -59,6 +43,17 @@ cudaError_t launch_reshape_and_cache(void* k_cache, void* v_cache, const void* k
                                      int32_t* err_flag, cudaStream_t stream);
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int32_t num_pairs,
                                int32_t num_blocks, int64_t block_bytes, int32_t* err_flag, cudaStream_t stream);
+
+// Host-side helpers of the C ABI (pa_api.cu), shared by the entry points in other files.
+namespace host {
+constexpr int64_t kInt32Max = 2147483647;
+bool aligned(const void* p, uintptr_t a);
+int elem_bytes(int32_t dtype);
+int check_cache(const pa_cache_desc* c);  // shape checks common to every call
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+// 2-D tensor map over a cache pool viewed as rows of head_size elements, box of `slab` rows x 64 columns
+bool encode_cache_map(CUtensorMap* map, const void* base, const pa_cache_desc* c, int slab);
+}  // namespace host
 
 // Slab (TMA box height in tokens) of the tensor-core decode: 16 tokens of one
 // block; the kernel's stage layout and transaction counts assume exactly this.

@@ -55,6 +55,7 @@
 #include "pa.h"
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "pa_prefill.h"
 
 namespace pa {
 namespace {
