@@ -26,9 +26,9 @@ import numpy as np
 
 from . import build as _build
 
-DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2}
-LAYOUT_CODE = {"ours": 0, "prior": 1}
-NP_STORAGE = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16}
+DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2, "fp8": 3}
+LAYOUT_CODE = {"ours": 0, "prior": 1, "fp8": 2}
+NP_STORAGE = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16, "fp8": np.uint8}
 
 _lib = None
 
@@ -58,6 +58,15 @@ def _load(path: str) -> ctypes.CDLL:
     L.pao_copy_blocks.restype = i32
     L.pao_max_threads.argtypes = []
     L.pao_max_threads.restype = i32
+    L.pao_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+    L.pao_e4m3_to_f64.restype = dbl
+    L.pao_f32_to_e4m3_sat.argtypes = [ctypes.c_float]
+    L.pao_f32_to_e4m3_sat.restype = ctypes.c_uint8
+    L.pao_attention_fp8.argtypes = [vp, vp, vp, vp, vp, vp] + [i32] * 7 + [dbl, dbl, dbl, i32, i32, vp]
+    L.pao_attention_fp8.restype = i32
+    L.pao_reshape_and_cache_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float,
+                                            ctypes.c_float]
+    L.pao_reshape_and_cache_fp8.restype = i32
     return L
 
 
@@ -102,6 +111,9 @@ def to_f64(a: np.ndarray, dtype: str) -> np.ndarray:
         return a.astype(np.float64)
     if dtype == "f16":
         return a.astype(np.float64)  # numpy's binary16 -> double is exact
+    if dtype == "fp8":
+        table = np.array([lib().pao_e4m3_to_f64(c) for c in range(256)], dtype=np.float64)
+        return table[np.ascontiguousarray(a)]
     # bfloat16 is the upper half of an IEEE binary32
     return (np.ascontiguousarray(a).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
@@ -218,3 +230,65 @@ def copy_blocks(k_cache, v_cache, pairs, *, dtype: str, num_kv_heads: int, block
 
 def max_threads() -> int:
     return lib().pao_max_threads()
+
+
+def e4m3_to_f64(code: int) -> float:
+    """Value of one E4M3 code (NaN for S.1111.111)."""
+    return lib().pao_e4m3_to_f64(int(code))
+
+
+def quantize_e4m3(r) -> np.ndarray:
+    """E4M3 codes nearest to the float32 values r (ties to even, saturating at +-448)."""
+    r = np.ascontiguousarray(r, dtype=np.float32)
+    f = lib().pao_f32_to_e4m3_sat
+    return np.array([f(float(x)) for x in r.reshape(-1)], dtype=np.uint8).reshape(r.shape)
+
+
+def quantize_cache_fp8(cache_f16: np.ndarray, scale: float, values: bool) -> np.ndarray:
+    """An fp16 pool [blocks][kv_heads][B][D] as E4M3 codes of x / scale (fp32 division),
+    in the FP8 layout: keys [blocks][kv_heads][B][D], values [blocks][kv_heads][D][B]."""
+    x = np.ascontiguousarray(cache_f16, dtype=np.float16).astype(np.float32)
+    codes = quantize_e4m3(x / np.float32(scale))
+    return np.ascontiguousarray(codes.transpose(0, 1, 3, 2)) if values else codes
+
+
+def paged_attention_fp8(q, k_cache, v_cache, block_tables, seq_lens, *, num_kv_heads: int, block_size: int,
+                        scale: float, k_scale: float, v_scale: float, partition_size: int = 0, threads: int = 0,
+                        alibi_slopes=None) -> np.ndarray:
+    """Decode attention over an FP8 (E4M3) cache in float64: fp16 q [N, Hq, D]; key codes
+    [blocks][kv_heads][B][D], value codes [blocks][kv_heads][D][B]; k = k_scale * e4m3(code),
+    v = v_scale * e4m3(code)."""
+    q = np.ascontiguousarray(q)
+    _check_storage(q, "f16", "q")
+    _check_storage(k_cache, "fp8", "k_cache")
+    _check_storage(v_cache, "fp8", "v_cache")
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    N, Hq, D = q.shape
+    M = bt.shape[1] if bt.ndim == 2 else 0
+    num_blocks = k_cache.size // (num_kv_heads * block_size * D)
+    out = np.zeros((N, Hq, D), dtype=np.float64)
+    slopes = None if alibi_slopes is None else np.ascontiguousarray(alibi_slopes, dtype=np.float64)
+    rc = lib().pao_attention_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt), _ptr(sl), N, Hq,
+                                 num_kv_heads, D, block_size, M, num_blocks, float(scale), float(k_scale),
+                                 float(v_scale), int(partition_size), int(threads),
+                                 None if slopes is None else _ptr(slopes))
+    if rc != 0:
+        raise OracleError(f"pao_attention_fp8 failed: {rc}")
+    return out
+
+
+def reshape_and_cache_fp8(k_cache, v_cache, key, value, slot_mapping, *, num_kv_heads: int, block_size: int,
+                          k_scale: float, v_scale: float) -> None:
+    """In place on the host FP8 pools: fp16 key/value [T, Hkv, D] -> E4M3 codes at the slots."""
+    _check_storage(k_cache, "fp8", "k_cache")
+    _check_storage(v_cache, "fp8", "v_cache")
+    key = np.ascontiguousarray(key, dtype=np.float16)
+    value = np.ascontiguousarray(value, dtype=np.float16)
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    T, Hkv, D = key.shape
+    num_blocks = k_cache.size // (Hkv * block_size * D)
+    rc = lib().pao_reshape_and_cache_fp8(_ptr(k_cache), _ptr(v_cache), _ptr(key), _ptr(value), _ptr(sm), T, Hkv, D,
+                                         block_size, num_blocks, float(k_scale), float(v_scale))
+    if rc != 0:
+        raise OracleError(f"pao_reshape_and_cache_fp8 failed: {rc}")

@@ -91,3 +91,49 @@ def prefill_attention(q, k_cache, v_cache, block_tables, seq_lens, query_start, 
                                   num_kv_heads=num_kv_heads, block_size=block_size, scale=scale)
             out.append(res[0])
     return out
+
+
+def e4m3_value(code: int) -> float:
+    """E4M3 code -> float from its fields: sign, 4 exponent bits (bias 7), 3 mantissa bits;
+    exponent 0 is subnormal (m/8 * 2^-6), S.1111.111 is NaN."""
+    sign = -1.0 if code & 0x80 else 1.0
+    e, m = (code >> 3) & 15, code & 7
+    if e == 15 and m == 7:
+        return float("nan")
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** -6
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def paged_attention_fp8(q_f16, k_codes, v_codes, block_tables, seq_lens, *, num_kv_heads: int, block_size: int,
+                        scale: float, k_scale: float, v_scale: float) -> list:
+    """Decode attention over an FP8 cache by brute force: keys [blocks][Hkv][B][D] and values
+    [blocks][Hkv][D][B] of E4M3 codes standing for k_scale (v_scale) times their value."""
+    N, Hq, D = q_f16.shape
+    G = Hq // num_kv_heads
+    qf = _flat_values(q_f16, "f16")
+    kc = [int(c) for c in k_codes.reshape(-1)]
+    vc = [int(c) for c in v_codes.reshape(-1)]
+    out = []
+    for s in range(N):
+        L = int(seq_lens[s])
+        per_head = []
+        for h in range(Hq):
+            hkv = h // G
+            qv = qf[(s * Hq + h) * D:(s * Hq + h + 1) * D]
+            if L == 0:
+                per_head.append([0.0] * D)
+                continue
+            scores, values = [], []
+            for i in range(L):
+                blk, off = int(block_tables[s][i // block_size]), i % block_size
+                base = (blk * num_kv_heads + hkv) * block_size * D
+                key = [k_scale * e4m3_value(kc[base + off * D + d]) for d in range(D)]
+                values.append([v_scale * e4m3_value(vc[base + d * block_size + off]) for d in range(D)])
+                scores.append(scale * sum(a * b for a, b in zip(qv, key)))
+            mx = max(scores)
+            ex = [math.exp(x - mx) for x in scores]
+            den = sum(ex)
+            per_head.append([sum(e * v[d] for e, v in zip(ex, values)) / den for d in range(D)])
+        out.append(per_head)
+    return out

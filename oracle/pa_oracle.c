@@ -40,7 +40,16 @@
  *
  * Layout codes: PAO_LAYOUT_OURS is [blocks][kv_heads][B][head_size], dense.
  * PAO_LAYOUT_PRIOR is the [P1] prior-art pair above, kept to pin the address
- * arithmetic against the page's worked example.
+ * arithmetic against the page's worked example.  PAO_LAYOUT_FP8 pairs our key
+ * layout with the [P1] value layout [blocks][kv_heads][head_size][B].
+ *
+ * FP8 KV cache: [P1 "软件地址翻译"] allows cache_t to be FP8 (x = 16 /
+ * sizeof(cache_t) = 16 elements per 16-byte access) and says nothing more.
+ * Reading taken: OCP E4M3 codes (1 sign, 4 exponent bits with bias 7, 3
+ * mantissa bits; S.1111.111 is NaN, no infinities), one fp32 scale for all of
+ * K and one for all of V; a stored code c stands for scale * e4m3(c), and a
+ * value x is written as the code nearest to x / scale (fp32 division, ties to
+ * the even code, overflow saturating to +-448).  Queries and outputs stay fp16.
  */
 #include <math.h>
 #include <stdint.h>
@@ -50,8 +59,8 @@
 #include <omp.h>
 #endif
 
-enum { PAO_F32 = 0, PAO_F16 = 1, PAO_BF16 = 2 };
-enum { PAO_LAYOUT_OURS = 0, PAO_LAYOUT_PRIOR = 1 };
+enum { PAO_F32 = 0, PAO_F16 = 1, PAO_BF16 = 2, PAO_FP8_E4M3 = 3 };
+enum { PAO_LAYOUT_OURS = 0, PAO_LAYOUT_PRIOR = 1, PAO_LAYOUT_FP8 = 2 };
 enum {
   PAO_OK = 0,
   PAO_BAD_ARG = -1,
@@ -86,10 +95,50 @@ double pao_bf16_to_f64(uint16_t b) {
   return (double)f;
 }
 
-static size_t elem_size(int dtype) { return dtype == PAO_F32 ? 4 : 2; }
+/* E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0
+ * holds the subnormals m * 2^-9; S.1111.111 is NaN; there is no infinity. */
+double pao_e4m3_to_f64(uint8_t c) {
+  int sign = (c >> 7) & 1;
+  int e = (c >> 3) & 0xf;
+  int m = c & 7;
+  double v;
+  if (e == 15 && m == 7) {
+    v = NAN;
+  } else if (e == 0) {
+    v = ldexp((double)m, -9);
+  } else {
+    v = ldexp((double)(8 + m), e - 10); /* (1 + m/8) * 2^(e-7) */
+  }
+  return sign ? -v : v;
+}
+
+/* The E4M3 code nearest to r, ties to the even code; a magnitude that rounds
+ * above the largest finite value 448 (infinity included) saturates to it; NaN
+ * gives S.1111.111.
+ * The grid spacing is 2^-9 below 2^-6 (subnormals) and 2^(e-3) in the binade
+ * [2^e, 2^(e+1)); a / spacing is exact in double, and nearbyint rounds half to
+ * even in the default rounding mode. */
+uint8_t pao_f32_to_e4m3_sat(float r) {
+  if (isnan(r)) return 0x7F;
+  const uint8_t sign = signbit(r) ? 0x80 : 0;
+  const double a = fabs((double)r);
+  if (isinf(a)) return sign | 0x7E; /* an infinite input saturates like any other overflow */
+  int e = a > 0.0 ? ilogb(a) : -6;
+  if (e < -6) e = -6;
+  const double v = nearbyint(a / ldexp(1.0, e - 3)) * ldexp(1.0, e - 3);
+  if (v > 448.0) return sign | 0x7E;
+  if (v == 0.0) return sign;
+  const int ev = ilogb(v);
+  if (ev < -6) return sign | (uint8_t)(v * 512.0); /* subnormal: m = v / 2^-9 */
+  const int m = (int)(v / ldexp(1.0, ev - 3)) - 8;
+  return sign | (uint8_t)((ev + 7) << 3) | (uint8_t)m;
+}
+
+static size_t elem_size(int dtype) { return dtype == PAO_F32 ? 4 : dtype == PAO_FP8_E4M3 ? 1 : 2; }
 
 double pao_load(const void* base, int64_t i, int dtype) {
   if (dtype == PAO_F32) return (double)((const float*)base)[i];
+  if (dtype == PAO_FP8_E4M3) return pao_e4m3_to_f64(((const uint8_t*)base)[i]);
   uint16_t bits = ((const uint16_t*)base)[i];
   return dtype == PAO_F16 ? pao_f16_to_f64(bits) : pao_bf16_to_f64(bits);
 }
@@ -134,7 +183,7 @@ static int64_t key_index(int layout, int64_t block, int64_t head, int64_t slot, 
 }
 
 static int64_t value_index(int layout, int64_t block, int64_t head, int64_t slot, int64_t d, int Hkv, int B, int D) {
-  if (layout == PAO_LAYOUT_PRIOR) return pao_value_offset_prior(block, head, slot, d, Hkv, B, D);
+  if (layout == PAO_LAYOUT_PRIOR || layout == PAO_LAYOUT_FP8) return pao_value_offset_prior(block, head, slot, d, Hkv, B, D);
   return pao_offset_ours(block, head, slot, d, Hkv, B, D);
 }
 
@@ -150,6 +199,8 @@ typedef struct {
   int N, Hq, Hkv, D, B, M, num_blocks;
   double scale;
   const double* alibi; /* nullable: one slope per query head */
+  int q_dtype;         /* element type of q (the cache's, except fp16 queries with an FP8 cache) */
+  double k_scale, v_scale; /* a stored key (value) element stands for k_scale (v_scale) times its decoded value */
 } pao_problem;
 
 /* Scores s_i = scale * <q, k_i> for tokens [t0, t1) of one (seq, query head),
@@ -165,8 +216,9 @@ static int gather_scores(const pao_problem* p, int s, int h, int64_t t0, int64_t
     if (blk < 0 || blk >= p->num_blocks) return PAO_BAD_BLOCK;
     double dot = 0.0;
     for (int d = 0; d < p->D; ++d) {
-      double qd = pao_load(p->q, ((int64_t)s * p->Hq + h) * p->D + d, p->dtype);
-      double kd = pao_load(p->k_cache, key_index(p->layout, blk, hkv, off, d, p->Hkv, p->B, p->D, p->dtype), p->dtype);
+      double qd = pao_load(p->q, ((int64_t)s * p->Hq + h) * p->D + d, p->q_dtype);
+      double kd = p->k_scale *
+                  pao_load(p->k_cache, key_index(p->layout, blk, hkv, off, d, p->Hkv, p->B, p->D, p->dtype), p->dtype);
       dot += qd * kd;
     }
     scores[i - t0] = p->scale * dot;
@@ -178,7 +230,7 @@ static int gather_scores(const pao_problem* p, int s, int h, int64_t t0, int64_t
 }
 
 static double value_at(const pao_problem* p, int32_t blk, int hkv, int32_t off, int d) {
-  return pao_load(p->v_cache, value_index(p->layout, blk, hkv, off, d, p->Hkv, p->B, p->D), p->dtype);
+  return p->v_scale * pao_load(p->v_cache, value_index(p->layout, blk, hkv, off, d, p->Hkv, p->B, p->D), p->dtype);
 }
 
 /* One (seq, query head): out = softmax(scale * q K^T) V over the seq_len tokens.
@@ -263,7 +315,8 @@ static int check_problem(const pao_problem* p) {
   if (!p->q || !p->k_cache || !p->v_cache || !p->block_tables || !p->seq_lens) return PAO_BAD_ARG;
   if (p->N < 0 || p->Hq <= 0 || p->Hkv <= 0 || p->D <= 0 || p->B <= 0 || p->M < 0 || p->num_blocks < 0) return PAO_BAD_ARG;
   if (p->Hq % p->Hkv != 0) return PAO_BAD_ARG;
-  if (p->dtype < PAO_F32 || p->dtype > PAO_BF16) return PAO_BAD_ARG;
+  if (p->dtype < PAO_F32 || p->dtype > PAO_FP8_E4M3) return PAO_BAD_ARG;
+  if ((p->dtype == PAO_FP8_E4M3) != (p->layout == PAO_LAYOUT_FP8)) return PAO_BAD_ARG;
   if (p->layout == PAO_LAYOUT_PRIOR && p->D % (int)(16 / elem_size(p->dtype)) != 0) return PAO_BAD_ARG;
   for (int s = 0; s < p->N; ++s) {
     if (p->seq_lens[s] < 0) return PAO_BAD_ARG;
@@ -277,7 +330,40 @@ int pao_attention(double* out, const void* q, const void* k_cache, const void* v
                   const int32_t* block_tables, const int32_t* seq_lens, int N, int Hq, int Hkv, int D, int B, int M,
                   int num_blocks, double scale, int partition_size, int threads, const double* alibi_slopes) {
   pao_problem p = {q, k_cache, v_cache, dtype, layout, block_tables, seq_lens, N,
-                   Hq, Hkv, D, B, M, num_blocks, scale, alibi_slopes};
+                   Hq, Hkv, D, B, M, num_blocks, scale, alibi_slopes, dtype, 1.0, 1.0};
+  int rc = check_problem(&p);
+  if (rc != PAO_OK || !out) return rc != PAO_OK ? rc : PAO_BAD_ARG;
+  int64_t total = (int64_t)N * Hq;
+  int err = PAO_OK;
+#ifdef _OPENMP
+  if (threads <= 0) threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(threads)
+#endif
+  for (int64_t sh = 0; sh < total; ++sh) {
+    int s = (int)(sh / Hq), h = (int)(sh % Hq);
+    int r = partition_size > 0 ? attend_one_split(&p, s, h, partition_size, out + sh * D)
+                               : attend_one(&p, s, h, out + sh * D);
+    if (r != PAO_OK) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+      err = r;
+    }
+  }
+  (void)threads;
+  return err;
+}
+
+/* FP8 (E4M3) cache: keys [blocks][kv_heads][B][D] and values [blocks][kv_heads][D][B]
+ * of E4M3 codes, fp16 queries; the definition above with k = k_scale * e4m3(code),
+ * v = v_scale * e4m3(code). */
+int pao_attention_fp8(double* out, const void* q_f16, const uint8_t* k_cache, const uint8_t* v_cache,
+                      const int32_t* block_tables, const int32_t* seq_lens, int N, int Hq, int Hkv, int D, int B,
+                      int M, int num_blocks, double scale, double k_scale, double v_scale, int partition_size,
+                      int threads, const double* alibi_slopes) {
+  if (!(k_scale > 0.0) || !(v_scale > 0.0)) return PAO_BAD_ARG;
+  pao_problem p = {q_f16, k_cache, v_cache, PAO_FP8_E4M3, PAO_LAYOUT_FP8, block_tables, seq_lens, N,
+                   Hq, Hkv, D, B, M, num_blocks, scale, alibi_slopes, PAO_F16, k_scale, v_scale};
   int rc = check_problem(&p);
   if (rc != PAO_OK || !out) return rc != PAO_OK ? rc : PAO_BAD_ARG;
   int64_t total = (int64_t)N * Hq;
@@ -339,7 +425,7 @@ int pao_prefill_attention(double* out, const void* q, const void* k_cache, const
     const int32_t len = (int32_t)(pos + 1);
     pao_problem p = {(const char*)q + (size_t)t * Hq * D * elem_size(dtype) - (size_t)0,
                      k_cache, v_cache, dtype, PAO_LAYOUT_OURS, block_tables + (int64_t)s * M, &len,
-                     1, Hq, Hkv, D, B, M, num_blocks, scale, NULL};
+                     1, Hq, Hkv, D, B, M, num_blocks, scale, NULL, dtype, 1.0, 1.0};
     double* o = out + (size_t)th * D;
     int r = attend_one(&p, 0, h, o);
     if (r != PAO_OK) {
@@ -372,6 +458,33 @@ int pao_reshape_and_cache(void* k_cache, void* v_cache, const void* key, const v
       size_t dst = (size_t)pao_offset_ours(block, h, off, 0, Hkv, B, D) * es;
       memcpy((char*)k_cache + dst, (const char*)key + src, D * es);
       memcpy((char*)v_cache + dst, (const char*)value + src, D * es);
+    }
+  }
+  return PAO_OK;
+}
+
+/* The FP8 append: as above, but each element of the fp16 key (value) row is
+ * written as the E4M3 code of x / k_scale (x / v_scale), the division in fp32;
+ * keys go to [block][head][offset][d], values to [block][head][d][offset]. */
+int pao_reshape_and_cache_fp8(uint8_t* k_cache, uint8_t* v_cache, const uint16_t* key_f16, const uint16_t* value_f16,
+                              const int64_t* slot_mapping, int T, int Hkv, int D, int B, int num_blocks,
+                              float k_scale, float v_scale) {
+  if (!k_cache || !v_cache || !key_f16 || !value_f16 || !slot_mapping || T < 0) return PAO_BAD_ARG;
+  if (!(k_scale > 0.0f) || !(v_scale > 0.0f)) return PAO_BAD_ARG;
+  for (int t = 0; t < T; ++t) {
+    int64_t sl = slot_mapping[t];
+    if (sl < 0) continue; /* padding token */
+    const int64_t blk = sl / B, off = sl % B;
+    if (blk >= num_blocks) return PAO_BAD_SLOT;
+    for (int h = 0; h < Hkv; ++h) {
+      for (int d = 0; d < D; ++d) {
+        const size_t src = ((size_t)t * Hkv + h) * D + d;
+        const float xk = (float)pao_f16_to_f64(key_f16[src]); /* exact: every fp16 value is a float */
+        const float xv = (float)pao_f16_to_f64(value_f16[src]);
+        const float rk = xk / k_scale, rv = xv / v_scale;
+        k_cache[pao_offset_ours(blk, h, off, d, Hkv, B, D)] = pao_f32_to_e4m3_sat(rk);
+        v_cache[pao_value_offset_prior(blk, h, off, d, Hkv, B, D)] = pao_f32_to_e4m3_sat(rv);
+      }
     }
   }
   return PAO_OK;

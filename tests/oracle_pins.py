@@ -428,10 +428,111 @@ def pin_prefill_contiguous():
         assert np.max(np.abs(got[qs[s]:qs[s + 1]] - sd)) < 1e-12
 
 
+# --------------------------------------------------------------------------- FP8 (E4M3) cache
+
+def pin_e4m3_codes():
+    """All 256 E4M3 codes against torch.float8_e4m3fn and against the pure-Python
+    decoding from the fields; textbook values: 0x38 = 1, 0x7E = 448 (largest),
+    0x08 = 2^-6 (smallest normal), 0x01 = 2^-9 (smallest subnormal), 0x7F NaN."""
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    got = O.to_f64(codes, "fp8")
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2
+    assert np.array_equal(got[~nan], ref[~nan])
+    py = np.array([brute.e4m3_value(int(c)) for c in codes])
+    assert np.array_equal(py[~nan], got[~nan])
+    assert (O.e4m3_to_f64(0x38), O.e4m3_to_f64(0x7E), O.e4m3_to_f64(0x08), O.e4m3_to_f64(0x01)) == \
+        (1.0, 448.0, 2.0 ** -6, 2.0 ** -9)
+    assert math.isnan(O.e4m3_to_f64(0x7F)) and O.e4m3_to_f64(0xB8) == -1.0
+
+
+def pin_e4m3_rounding():
+    """Writing x / scale as a code: torch's round-to-nearest-even conversion for
+    |r| < 464 (random values over the whole range, exact ties between codes,
+    subnormal ties), saturation to +-448 from there on (torch turns those into
+    NaN instead), and every finite code maps back to itself."""
+    import torch
+    rng = np.random.default_rng(171)
+    r = np.concatenate([rng.standard_normal(4000) * 60, rng.standard_normal(2000) * 0.02,
+                        np.ldexp(rng.uniform(1, 2, 2000), rng.integers(-12, 9, 2000))]).astype(np.float32)
+    finite = np.array([c for c in range(256) if not math.isnan(brute.e4m3_value(c))], dtype=np.uint8)
+    vals = np.array([brute.e4m3_value(int(c)) for c in finite])
+    mids = np.unique(np.abs(vals))
+    ties = ((mids[:-1] + mids[1:]) / 2).astype(np.float32)  # exact midpoints: ties to the even code
+    r = np.concatenate([r, ties, -ties, np.float32([447.9, 448.0, 449.0, 463.99, -463.99])])
+    r = r[np.abs(r) < 464]
+    ref = torch.from_numpy(r).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.quantize_e4m3(r), ref)
+    assert list(O.quantize_e4m3(np.float32([464.0, 480.0, 1e6, np.inf, -500.0, -np.inf]))) == [0x7E] * 4 + [0xFE] * 2
+    assert np.array_equal(O.quantize_e4m3(vals.astype(np.float32)), finite)
+
+
+def _fp8_case(seed, k_scale, v_scale, lens=None, Hq=4, Hkv=2, D=8, B=4):
+    w = small_case(seed, "f16", Hq=Hq, Hkv=Hkv, D=D, B=B, lens=lens)
+    kc = O.quantize_cache_fp8(w.k_cache, k_scale, values=False)
+    vc = O.quantize_cache_fp8(w.v_cache, v_scale, values=True)
+    return w, kc, vc
+
+
+def pin_fp8_attention():
+    """FP8 attention is the definition on the dequantised caches: with power-of-two
+    scales it equals, bit for bit, the float32 evaluation of k_scale * e4m3(code)
+    (the value pool transposed back to [B][D] with numpy); with any scales it
+    agrees with the pure-Python brute force to 1e-12, and its split form with the
+    unsplit one."""
+    ks, vs = 2.0 ** -5, 2.0 ** -3
+    w, kc, vc = _fp8_case(181, ks, vs)
+    got = O.paged_attention_fp8(w.q, kc, vc, w.block_tables, w.seq_lens, num_kv_heads=w.num_kv_heads,
+                                block_size=w.block_size, scale=w.scale, k_scale=ks, v_scale=vs)
+    kd = (O.to_f64(kc, "fp8") * ks).astype(np.float32)
+    vd = np.ascontiguousarray((O.to_f64(vc, "fp8") * vs).astype(np.float32).transpose(0, 1, 3, 2))
+    ref = O.paged_attention(w.q.astype(np.float32), kd, vd, w.block_tables, w.seq_lens, dtype="f32",
+                            num_kv_heads=w.num_kv_heads, block_size=w.block_size, scale=w.scale)
+    assert np.array_equal(got, ref)
+    ks, vs = 0.0113, 0.0371
+    w, kc, vc = _fp8_case(182, ks, vs, lens=[1, 6, 9])
+    kw = dict(num_kv_heads=w.num_kv_heads, block_size=w.block_size, scale=w.scale, k_scale=ks, v_scale=vs)
+    got = O.paged_attention_fp8(w.q, kc, vc, w.block_tables, w.seq_lens, **kw)
+    bf = np.array(brute.paged_attention_fp8(w.q, kc, vc, w.block_tables, w.seq_lens, **kw))
+    assert np.max(np.abs(got - bf)) < 1e-12
+    split = O.paged_attention_fp8(w.q, kc, vc, w.block_tables, w.seq_lens, partition_size=4, **kw)
+    assert np.max(np.abs(got - split)) < 1e-12
+
+
+def pin_fp8_append():
+    """The FP8 append writes the code of x / scale (fp32 division; torch's
+    conversion for in-range values) of token t's key at [block][head][offset][d]
+    and of its value at [block][head][d][offset]; padding slots are skipped and
+    every other byte is left as it was."""
+    import torch
+    rng = np.random.default_rng(191)
+    Hkv, D, B, nb = 2, 16, 4, 6
+    kc = rng.integers(0, 256, size=(nb, Hkv, B, D), dtype=np.uint8)
+    vc = rng.integers(0, 256, size=(nb, Hkv, D, B), dtype=np.uint8)
+    k0, v0 = kc.copy(), vc.copy()
+    key = (rng.standard_normal((5, Hkv, D)) * 2).astype(np.float16)
+    val = (rng.standard_normal((5, Hkv, D)) * 2).astype(np.float16)
+    slots = np.array([7, -1, 0, 23, 13], dtype=np.int64)
+    ks, vs = 0.0231, 2.0 ** -4
+    assert np.abs(key.astype(np.float32) / np.float32(ks)).max() < 448  # torch's conversion saturates nowhere here
+    O.reshape_and_cache_fp8(kc, vc, key, val, slots, num_kv_heads=Hkv, block_size=B, k_scale=ks, v_scale=vs)
+    kq = torch.from_numpy(key.astype(np.float32) / np.float32(ks)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    vq = torch.from_numpy(val.astype(np.float32) / np.float32(vs)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    for t, sl in enumerate(slots):
+        if sl < 0:
+            continue
+        b, off = sl // B, sl % B
+        k0[b, :, off, :] = kq[t]
+        v0[b, :, :, off] = vq[t]
+    assert np.array_equal(kc, k0) and np.array_equal(vc, v0)
+
+
 ALL_PINS = [
     pin_f16_decoding, pin_bf16_decoding, pin_35_token_example, pin_worked_offset, pin_prior_layout_offsets,
     pin_prior_layout_attention, pin_slot_round_trip, pin_padding_slots_skipped, pin_identity_tables_vs_contiguous,
     pin_permutation_invariance, pin_shared_prefix_equals_private, pin_cow_isolation, pin_brute_force,
     pin_special_cases, pin_split_identity, pin_zero_length, pin_bad_block_rejected, pin_alibi, pin_prefill,
-    pin_prefill_contiguous,
+    pin_prefill_contiguous, pin_e4m3_codes, pin_e4m3_rounding, pin_fp8_attention, pin_fp8_append,
 ]

@@ -38,6 +38,19 @@ MUTANTS = [
     ("prefill_query_origin", "const int64_t pos = seq_lens[s] - n + (t - query_start[s]);",
      "const int64_t pos = seq_lens[s] - n + t;"),
     ("alibi_kv_head_slope", "p->alibi[h] * (double)(i", "p->alibi[h / (p->Hq / p->Hkv)] * (double)(i"),
+    ("e4m3_bias", "ldexp((double)(8 + m), e - 10)", "ldexp((double)(8 + m), e - 9)"),
+    ("e4m3_subnormal", "v = ldexp((double)m, -9);", "v = ldexp((double)m, -8);"),
+    ("e4m3_round_down", "nearbyint(a / ldexp(1.0, e - 3))", "floor(a / ldexp(1.0, e - 3))"),
+    ("e4m3_no_saturation", "if (v > 448.0) return sign | 0x7E;", "if (v > 480.0) return sign | 0x7E;"),
+    ("fp8_value_layout", "layout == PAO_LAYOUT_PRIOR || layout == PAO_LAYOUT_FP8", "layout == PAO_LAYOUT_PRIOR"),
+    ("fp8_v_scale_dropped", "return p->v_scale * pao_load(", "return pao_load("),
+    ("fp8_k_scale_dropped", "double kd = p->k_scale *", "double kd = 1.0 *"),
+    ("fp8_append_value_offset", "v_cache[pao_value_offset_prior(blk, h, off, d, Hkv, B, D)]",
+     "v_cache[pao_offset_ours(blk, h, off, d, Hkv, B, D)]"),
+    ("fp8_append_slot_swapped", "const int64_t blk = sl / B, off = sl % B;", "const int64_t blk = sl % B, off = sl / B;"),
+    ("fp8_append_padding_written", "if (sl < 0) continue; /* padding token */", "if (sl < 0) sl = -sl;"),
+    ("fp8_append_scale_multiplied", "const float rk = xk / k_scale, rv = xv / v_scale;",
+     "const float rk = xk * k_scale, rv = xv / v_scale;"),
 ]
 
 
