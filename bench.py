@@ -45,6 +45,10 @@ WORKLOAD_DESC = {
     "long_bf16_b16": "long bf16 split-KV: 8 seqs x 32768 tokens, 32 q / 8 kv heads, D 128, B 16, 512-token partitions",
     "long_bf16_b32": "long bf16 split-KV: 8 seqs x 32768 tokens, 32 q / 8 kv heads, D 128, B 32, 512-token partitions",
     "long_bf16_b64": "long bf16 split-KV: 8 seqs x 32768 tokens, 32 q / 8 kv heads, D 128, B 64, 512-token partitions",
+    "mha_fp8": "MHA decode over an FP8 E4M3 cache (scales 0.0123 / 0.0117, fp16 q/out): 64 seqs, seq_lens "
+               "U[128,2048], 32 heads, D 128, B 16, pool 8192 shuffled, one quantising append per seq",
+    "gqa_fp8": "GQA decode over an FP8 E4M3 cache (fp16 q/out): 128 seqs, 64 q / 8 kv heads, D 128, B 32, "
+               "lognormal(ln 1200, 0.6) lens in [64, 4096], pool 1.2x needed",
     "prefill_bf16": "chunked prefill bf16: 16 seqs, cached prefix U[0,2048] + chunk U[256,2048] tokens, 32 q / 8 kv "
                     "heads, D 128, B 16, pool 1.2x needed, shuffled; chunk K/V appended, then causal attention",
 }
@@ -196,7 +200,14 @@ class DeviceStep:
         self.alibi = (torch.tensor([2.0 ** (-8.0 * (i + 1) / w.num_q_heads) for i in range(w.num_q_heads)],
                                    dtype=torch.float32, device=device) if alibi else None)
         tdt = getattr(torch, TORCH_DT[w.dtype])
+        self.fp8 = w.info.get("kv_dtype") == "fp8"
+        self.k_scale, self.v_scale = w.info.get("k_scale"), w.info.get("v_scale")
         self.k, self.v = W.device_caches(w, device)
+        if self.fp8:  # E4M3 codes of x / scale (torch's conversion: inputs only); values [blocks][heads][D][B]
+            self.k = (self.k.float() / self.k_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+            self.v = (self.v.float() / self.v_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+            self.v = self.v.transpose(2, 3).contiguous()
+            torch.cuda.empty_cache()
         self.desc = pa.cache_desc(self.k)
 
         def t(a, dtype=None):
@@ -225,18 +236,26 @@ class DeviceStep:
     def launches_per_step(self) -> int:
         return (self.pairs is not None) + (self.slots is not None) + 1 + (self.pmax > 1)
 
+    def append(self, stream, nk, nv, slots):
+        if self.fp8:
+            self.pa.pa_reshape_and_cache_fp8(self.k, self.v, nk, nv, slots, self.k_scale, self.v_scale,
+                                             err_flag=self.err, stream=stream, desc=self.desc)
+        else:
+            self.pa.pa_reshape_and_cache(self.k, self.v, nk, nv, slots, err_flag=self.err, stream=stream,
+                                         desc=self.desc)
+
     def writes(self, stream):
         if self.pairs is not None:
             self.pa.pa_copy_blocks(self.k, self.v, self.pairs, err_flag=self.err, stream=stream, desc=self.desc)
         if self.slots is not None:
-            self.pa.pa_reshape_and_cache(self.k, self.v, self.nk, self.nv, self.slots, err_flag=self.err,
-                                         stream=stream, desc=self.desc)
+            self.append(stream, self.nk, self.nv, self.slots)
 
     def decode(self, stream, q=None, tables=None, lens=None, out=None):
         self.pa.pa_decode(self.out if out is None else out, self.q if q is None else q, self.k, self.v,
                           self.tables if tables is None else tables, self.lens if lens is None else lens,
                           self.w.scale, partition_size=self.w.partition_size, workspace=self.ws,
-                          err_flag=self.err, stream=stream, desc=self.desc, alibi_slopes=self.alibi)
+                          err_flag=self.err, stream=stream, desc=self.desc, alibi_slopes=self.alibi,
+                          k_scale=self.k_scale if self.fp8 else None, v_scale=self.v_scale if self.fp8 else None)
 
     def attend(self, stream):
         self.decode(stream)
@@ -342,8 +361,7 @@ def time_e2e(ds: DeviceStep, steps: int, warmup: int, world: int):
         if ds.pairs is not None:
             ds.pa.pa_copy_blocks(ds.k, ds.v, dev["pairs"], err_flag=ds.err, stream=stream, desc=ds.desc)
         if ds.slots is not None:
-            ds.pa.pa_reshape_and_cache(ds.k, ds.v, dev["nk"], dev["nv"], dev["slots"], err_flag=ds.err,
-                                       stream=stream, desc=ds.desc)
+            ds.append(stream, dev["nk"], dev["nv"], dev["slots"])
         ds.decode(stream, q=dev["q"], tables=dev["tables"], lens=dev["lens"])
         out_host.copy_(ds.out, non_blocking=True)
 
@@ -584,7 +602,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mha_f16", choices=sorted(k for k in W.WORKLOADS if not k.startswith("prefill")))
     ap.add_argument("--extra", nargs="*", default=["gqa_bf16", "gqa_bf16+alibi", "long_bf16_b16", "long_bf16_b32",
-                                                   "long_bf16_b64", "shared_prefix_f16"])
+                                                   "long_bf16_b64", "shared_prefix_f16", "mha_fp8", "gqa_fp8"])
     ap.add_argument("--no-extra", action="store_true", help="time only the headline workload")
     ap.add_argument("--prefill", default="prefill_bf16", help="chunked-prefill workload timed beside decode ('' = none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

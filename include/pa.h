@@ -42,16 +42,32 @@
 extern "C" {
 #endif
 
-typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_FP8_E4M3 = 3 } pa_dtype;
 
 /* Shape of one layer's KV cache pair. */
 typedef struct {
   int32_t num_blocks;   /* physical blocks in the pool */
-  int32_t block_size;   /* tokens per block B: f16/bf16 need a multiple of 16 (<= 256); f32 any B >= 1 */
+  int32_t block_size;   /* tokens per block B: f16/bf16/fp8 need a multiple of 16 (<= 256); f32 any B >= 1 */
   int32_t num_kv_heads; /* Hkv */
-  int32_t head_size;    /* D: 64 or 128 */
-  int32_t dtype;        /* pa_dtype of the cache, of q/out and of new key/value */
+  int32_t head_size;    /* D: 64 or 128 (fp8: 128) */
+  int32_t dtype;        /* pa_dtype of the cache, and of q/out and new key/value except for fp8 (see below) */
 } pa_cache_desc;
+
+/*
+ * FP8 caches (dtype PA_FP8_E4M3).  ["PagedAttention 详解：缓存的存储结构"
+ * "软件地址翻译": cache_t may be FP8, x = 16 / sizeof(cache_t) = 16 elements per
+ * 16-byte access.]  The pages define nothing further; the reading implemented:
+ *   - elements are OCP E4M3 codes (1 sign, 4 exponent bits with bias 7, 3
+ *     mantissa bits; S.1111.111 is NaN; no infinities);
+ *   - one fp32 scale per cache: a key code c stands for k_scale * e4m3(c), a
+ *     value code for v_scale * e4m3(c) (scales > 0, passed per call);
+ *   - keys   [num_blocks][num_kv_heads][block_size][head_size] bytes,
+ *     values [num_blocks][num_kv_heads][head_size][block_size] bytes (the
+ *     pages' value layout: a dimension's tokens are contiguous);
+ *   - q, out and the key/value rows written by pa_reshape_and_cache_fp8 are fp16;
+ *   - written codes are the E4M3 code nearest to x / scale (fp32 division,
+ *     ties to even; magnitudes past 448, infinities included, saturate to 448).
+ */
 
 /* Host-side status codes. */
 enum {
@@ -118,9 +134,12 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
  *                 defining them; the reading implemented is the standard linear
  *                 bias towards the query's own position: score_i of head h gains
  *                 alibi_slopes[h] * (i - (seq_lens[s] - 1)).
+ *   k_scale, v_scale  the dequantisation scales of an FP8 cache (pa_decode uses 1).
  */
 typedef struct {
   const float* alibi_slopes;
+  float k_scale; /* FP8 caches only (> 0); 0 means 1.  Ignored for other dtypes. */
+  float v_scale; /* FP8 caches only (> 0); 0 means 1.  Ignored for other dtypes. */
 } pa_decode_options;
 
 int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
@@ -186,6 +205,17 @@ int pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cach
 int pa_reshape_and_cache(void* k_cache, void* v_cache, const void* key, const void* value,
                          const int64_t* slot_mapping, int32_t num_tokens, const pa_cache_desc* cache,
                          int32_t* err_flag, void* stream);
+
+/*
+ * pa_reshape_and_cache_fp8 - the append for an FP8 cache (dtype PA_FP8_E4M3):
+ *   fp16 key/value [num_tokens][num_kv_heads][head_size] (16-byte aligned) are
+ *   written as E4M3 codes of x / k_scale and x / v_scale (see "FP8 caches"
+ *   above): key[t][h][d] at (block, h, offset, d), value[t][h][d] at (block, h,
+ *   d, offset).  Slots as for pa_reshape_and_cache.  k_scale, v_scale > 0.
+ */
+int pa_reshape_and_cache_fp8(void* k_cache, void* v_cache, const void* key, const void* value,
+                             const int64_t* slot_mapping, int32_t num_tokens, const pa_cache_desc* cache,
+                             float k_scale, float v_scale, int32_t* err_flag, void* stream);
 
 /*
  * pa_copy_blocks - the copy step of copy-on-write [P2 "写时复制是正确性的边界";

@@ -62,6 +62,8 @@ def _load(path: str) -> ctypes.CDLL:
     L.pao_e4m3_to_f64.restype = dbl
     L.pao_f32_to_e4m3_sat.argtypes = [ctypes.c_float]
     L.pao_f32_to_e4m3_sat.restype = ctypes.c_uint8
+    L.pao_f32_to_e4m3_array.argtypes = [vp, vp, i64]
+    L.pao_f32_to_e4m3_array.restype = None
     L.pao_attention_fp8.argtypes = [vp, vp, vp, vp, vp, vp] + [i32] * 7 + [dbl, dbl, dbl, i32, i32, vp]
     L.pao_attention_fp8.restype = i32
     L.pao_reshape_and_cache_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float,
@@ -240,8 +242,9 @@ def e4m3_to_f64(code: int) -> float:
 def quantize_e4m3(r) -> np.ndarray:
     """E4M3 codes nearest to the float32 values r (ties to even, saturating at +-448)."""
     r = np.ascontiguousarray(r, dtype=np.float32)
-    f = lib().pao_f32_to_e4m3_sat
-    return np.array([f(float(x)) for x in r.reshape(-1)], dtype=np.uint8).reshape(r.shape)
+    out = np.empty(r.shape, dtype=np.uint8)
+    lib().pao_f32_to_e4m3_array(_ptr(r), _ptr(out), r.size)
+    return out
 
 
 def quantize_cache_fp8(cache_f16: np.ndarray, scale: float, values: bool) -> np.ndarray:

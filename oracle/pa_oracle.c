@@ -134,6 +134,14 @@ uint8_t pao_f32_to_e4m3_sat(float r) {
   return sign | (uint8_t)((ev + 7) << 3) | (uint8_t)m;
 }
 
+/* pao_f32_to_e4m3_sat over an array (OpenMP): the codes of a whole pool. */
+void pao_f32_to_e4m3_array(const float* r, uint8_t* codes, int64_t n) {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+  for (int64_t i = 0; i < n; ++i) codes[i] = pao_f32_to_e4m3_sat(r[i]);
+}
+
 static size_t elem_size(int dtype) { return dtype == PAO_F32 ? 4 : dtype == PAO_FP8_E4M3 ? 1 : 2; }
 
 double pao_load(const void* base, int64_t i, int dtype) {

@@ -17,17 +17,18 @@ import os
 
 from . import build as _build
 
-PA_F32, PA_F16, PA_BF16 = 0, 1, 2
+PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2, 3
 PA_OK = 0
 PA_DEVERR = {0: "none", 1: "block id out of range", 2: "slot out of range", 3: "copy pair id out of range",
              4: "wait on an asynchronous copy timed out", 5: "prefill chunk inconsistent with q, grid or sequence"}
 
 EXPORTED = ("pa_decode", "pa_decode_ex", "pa_decode_partition_size", "pa_decode_workspace_size", "pa_reshape_and_cache",
-            "pa_copy_blocks", "pa_status_string", "pa_version", "pa_decode_noalloc", "pa_prefill")
+            "pa_copy_blocks", "pa_status_string", "pa_version", "pa_decode_noalloc", "pa_prefill",
+            "pa_reshape_and_cache_fp8")
 
 
 class pa_decode_options(ctypes.Structure):
-    _fields_ = [("alibi_slopes", ctypes.c_void_p)]
+    _fields_ = [("alibi_slopes", ctypes.c_void_p), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
 class pa_cache_desc(ctypes.Structure):
@@ -70,6 +71,8 @@ def lib() -> ctypes.CDLL:
         L.pa_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i32, desc_p, vp, vp]
         L.pa_reshape_and_cache.restype = ctypes.c_int
         L.pa_copy_blocks.argtypes = [vp, vp, vp, i32, desc_p, vp, vp]
+        L.pa_reshape_and_cache_fp8.argtypes = [vp, vp, vp, vp, vp, i32, desc_p, ctypes.c_float, ctypes.c_float, vp, vp]
+        L.pa_reshape_and_cache_fp8.restype = ctypes.c_int
         L.pa_copy_blocks.restype = ctypes.c_int
         L.pa_status_string.argtypes = [ctypes.c_int]
         L.pa_status_string.restype = ctypes.c_char_p
@@ -98,14 +101,18 @@ def version() -> int:
 # ---------------------------------------------------------------- marshalling helpers
 def _dtype_code(t) -> int:
     import torch
-    codes = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
+    codes = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.uint8: PA_FP8_E4M3}
+    if hasattr(torch, "float8_e4m3fn"):
+        codes[torch.float8_e4m3fn] = PA_FP8_E4M3
     if t.dtype not in codes:
         raise TypeError(f"unsupported dtype {t.dtype}")
     return codes[t.dtype]
 
 
 def cache_desc(k_cache) -> pa_cache_desc:
-    """Descriptor of a [num_blocks, num_kv_heads, block_size, head_size] cache tensor."""
+    """Descriptor of a [num_blocks, num_kv_heads, block_size, head_size] key-cache tensor
+    (uint8 or float8_e4m3fn storage means an FP8 E4M3 cache, whose values are
+    [num_blocks, num_kv_heads, head_size, block_size])."""
     if k_cache.dim() != 4:
         raise ValueError("cache must be [num_blocks, num_kv_heads, block_size, head_size]")
     nb, hkv, bs, d = (int(x) for x in k_cache.shape)
@@ -150,14 +157,15 @@ def pa_decode_workspace_size(num_seqs: int, num_q_heads: int, max_blocks_per_seq
 
 def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale: float, partition_size: int = 0,
               workspace=None, err_flag=None, stream=None, desc: pa_cache_desc | None = None,
-              alibi_slopes=None) -> None:
+              alibi_slopes=None, k_scale: float | None = None, v_scale: float | None = None) -> None:
     """out[s, h] = softmax(scale * q[s, h] K_s^T) V_s over seq_lens[s] paged tokens.
 
     out, q: [num_seqs, num_q_heads, head_size] (cache dtype); block_tables: int32
     [num_seqs, max_blocks_per_seq]; seq_lens: int32 [num_seqs].  ``workspace`` is a
     uint8 device tensor of at least pa_decode_workspace_size(...) bytes; when None
     and one is needed, it is allocated with torch.  ``alibi_slopes``: optional
-    float32 device tensor [num_q_heads] (calls pa_decode_ex).
+    float32 device tensor [num_q_heads] (calls pa_decode_ex).  ``k_scale`` /
+    ``v_scale``: dequantisation scales of an FP8 cache (q and out are fp16 then).
     """
     desc = desc or cache_desc(k_cache)
     for t, n in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"),
@@ -173,11 +181,11 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale: float, pa
     args = (_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(seq_lens), num_seqs,
             num_q_heads, max_blocks, ctypes.byref(desc), float(scale), int(partition_size), _ptr(workspace), ws_bytes,
             _ptr(err_flag), _stream(stream))
-    if alibi_slopes is None:
+    if alibi_slopes is None and k_scale is None and v_scale is None:
         _check(lib().pa_decode(*args), "pa_decode")
     else:
         _dense(alibi_slopes, "alibi_slopes")
-        opts = pa_decode_options(_ptr(alibi_slopes))
+        opts = pa_decode_options(_ptr(alibi_slopes), float(k_scale or 0.0), float(v_scale or 0.0))
         _check(lib().pa_decode_ex(*args, ctypes.byref(opts)), "pa_decode_ex")
 
 
@@ -213,6 +221,20 @@ def pa_reshape_and_cache(k_cache, v_cache, key, value, slot_mapping, err_flag=No
                                         int(slot_mapping.shape[0]), ctypes.byref(desc), _ptr(err_flag),
                                         _stream(stream))
     _check(status, "pa_reshape_and_cache")
+
+
+def pa_reshape_and_cache_fp8(k_cache, v_cache, key, value, slot_mapping, k_scale: float, v_scale: float,
+                             err_flag=None, stream=None, desc: pa_cache_desc | None = None) -> None:
+    """Write fp16 key/value [num_tokens, num_kv_heads, head_size] into an FP8 cache as
+    E4M3 codes of x / k_scale and x / v_scale (values transposed per block)."""
+    desc = desc or cache_desc(k_cache)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (key, "key"), (value, "value"),
+                 (slot_mapping, "slot_mapping")):
+        _dense(t, n)
+    status = lib().pa_reshape_and_cache_fp8(_ptr(k_cache), _ptr(v_cache), _ptr(key), _ptr(value), _ptr(slot_mapping),
+                                            int(slot_mapping.shape[0]), ctypes.byref(desc), float(k_scale),
+                                            float(v_scale), _ptr(err_flag), _stream(stream))
+    _check(status, "pa_reshape_and_cache_fp8")
 
 
 def pa_copy_blocks(k_cache, v_cache, block_pairs, err_flag=None, stream=None, desc: pa_cache_desc | None = None) -> None:

@@ -18,18 +18,22 @@ constexpr int32_t kDefaultPartition = 1024;  // tokens per partition when the ca
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-int elem_bytes(int32_t dtype) { return dtype == PA_F32 ? 4 : 2; }
+int elem_bytes(int32_t dtype) { return dtype == PA_F32 ? 4 : dtype == PA_FP8_E4M3 ? 1 : 2; }
 
 // Shape checks common to every call.
 int check_cache(const pa_cache_desc* c) {
   if (c == nullptr) return PA_ERR_NULL_POINTER;
-  if (c->dtype != PA_F32 && c->dtype != PA_F16 && c->dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (c->dtype != PA_F32 && c->dtype != PA_F16 && c->dtype != PA_BF16 && c->dtype != PA_FP8_E4M3)
+    return PA_ERR_UNSUPPORTED;
   if (c->num_blocks < 0 || c->block_size <= 0 || c->num_kv_heads <= 0 || c->head_size <= 0)
     return PA_ERR_INVALID_ARG;
   if (c->head_size != 64 && c->head_size != 128) return PA_ERR_UNSUPPORTED;
+  if (c->dtype == PA_FP8_E4M3 && c->head_size != 128) return PA_ERR_UNSUPPORTED;
   if (c->dtype != PA_F32 && (c->block_size % 16 != 0 || c->block_size > 256)) return PA_ERR_UNSUPPORTED;
-  // row index (block * Hkv + head) * B + slot must fit the kernels' int32 arithmetic
+  // row index (block * Hkv + head) * B + slot (and, for FP8 values, * D + d) must fit the kernels' int32 arithmetic
   if ((int64_t)c->num_blocks * c->num_kv_heads * c->block_size > kInt32Max) return PA_ERR_TOO_LARGE;
+  if (c->dtype == PA_FP8_E4M3 && (int64_t)c->num_blocks * c->num_kv_heads * c->head_size > kInt32Max)
+    return PA_ERR_TOO_LARGE;
   return PA_OK;
 }
 
@@ -83,6 +87,30 @@ bool encode_cache_map(CUtensorMap* map, const void* base, const pa_cache_desc* c
       c->dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// FP8 caches: keys as rows of D bytes (box 16 rows x 128 bytes, 128-byte swizzle); values as rows
+// of B bytes, one per (block, head, dimension) (box 128 rows x 16 bytes, no swizzle)
+bool encode_fp8_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k_cache, const void* v_cache,
+                     const pa_cache_desc* c) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint32_t estr[2] = {1, 1};
+  const cuuint64_t heads = (cuuint64_t)c->num_blocks * c->num_kv_heads;
+  cuuint64_t kdims[2] = {(cuuint64_t)c->head_size, heads * c->block_size};
+  cuuint64_t kstrides[1] = {(cuuint64_t)c->head_size};
+  cuuint32_t kbox[2] = {(cuuint32_t)c->head_size, (cuuint32_t)pa::kTcSlabTokens};
+  CUresult r = enc(tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(k_cache), kdims, kstrides, kbox, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  cuuint64_t vdims[2] = {(cuuint64_t)c->block_size, heads * c->head_size};
+  cuuint64_t vstrides[1] = {(cuuint64_t)c->block_size};
+  cuuint32_t vbox[2] = {(cuuint32_t)pa::kTcSlabTokens, (cuuint32_t)c->head_size};
+  r = enc(tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(v_cache), vdims, vstrides, vbox, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -158,6 +186,11 @@ int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_ca
     return PA_ERR_MISALIGNED;
   const float* alibi = options != nullptr ? options->alibi_slopes : nullptr;
   if (alibi != nullptr && !aligned(alibi, 4)) return PA_ERR_MISALIGNED;
+  float k_scale = options != nullptr ? options->k_scale : 0.f, v_scale = options != nullptr ? options->v_scale : 0.f;
+  if (k_scale == 0.f) k_scale = 1.f;
+  if (v_scale == 0.f) v_scale = 1.f;
+  if (cache->dtype == PA_FP8_E4M3 && (!(k_scale > 0.f) || isinf(k_scale) || !(v_scale > 0.f) || isinf(v_scale)))
+    return PA_ERR_INVALID_ARG;
   const int G = num_q_heads / cache->num_kv_heads;
   const int head_groups = (G + 7) / 8;
   const long long grid = (long long)num_seqs * cache->num_kv_heads * head_groups * pmax;
@@ -194,6 +227,10 @@ int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_ca
   if (cache->dtype == PA_F32) {
     e = pa::launch_decode_f32(cache->head_size, static_cast<const float*>(k_cache),
                               static_cast<const float*>(v_cache), p, st);
+  } else if (cache->dtype == PA_FP8_E4M3) {
+    CUtensorMap tk, tv;
+    if (!encode_fp8_maps(&tk, &tv, k_cache, v_cache, cache)) return PA_ERR_CUDA;
+    e = pa::launch_decode_fp8(cache->head_size, tk, tv, p, k_scale, v_scale, st);
   } else {
     CUtensorMap tk, tv;
     if (!encode_cache_map(&tk, k_cache, cache, pa::kTcSlabTokens) ||
@@ -202,8 +239,8 @@ int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_ca
     e = pa::launch_decode_tc(cache->dtype, cache->head_size, cache->block_size, tk, tv, p, st);
   }
   if (e != cudaSuccess) return PA_ERR_CUDA;
-  if (pmax > 1) {
-    e = pa::launch_merge(cache->dtype, cache->head_size, p, st);
+  if (pmax > 1) {  // partial outputs merge into the output dtype (fp16 for an FP8 cache)
+    e = pa::launch_merge(cache->dtype == PA_FP8_E4M3 ? PA_F16 : cache->dtype, cache->head_size, p, st);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;
@@ -214,6 +251,7 @@ int pa_reshape_and_cache(void* k_cache, void* v_cache, const void* key, const vo
                          int32_t* err_flag, void* stream) {
   int rc = check_cache(cache);
   if (rc != PA_OK) return rc;
+  if (cache->dtype == PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;  // quantising append: pa_reshape_and_cache_fp8
   if (num_tokens < 0) return PA_ERR_INVALID_ARG;
   if (num_tokens == 0) return PA_OK;
   if (k_cache == nullptr || v_cache == nullptr || key == nullptr || value == nullptr || slot_mapping == nullptr)
@@ -225,6 +263,28 @@ int pa_reshape_and_cache(void* k_cache, void* v_cache, const void* key, const vo
   cudaError_t e = pa::launch_reshape_and_cache(k_cache, v_cache, key, value, slot_mapping, num_tokens,
                                                cache->num_blocks, cache->block_size, cache->num_kv_heads, row_bytes,
                                                err_flag, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_reshape_and_cache_fp8(void* k_cache, void* v_cache, const void* key, const void* value,
+                             const int64_t* slot_mapping, int32_t num_tokens, const pa_cache_desc* cache,
+                             float k_scale, float v_scale, int32_t* err_flag, void* stream) {
+  int rc = check_cache(cache);
+  if (rc != PA_OK) return rc;
+  if (cache->dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+  if (num_tokens < 0 || !(k_scale > 0.f) || isinf(k_scale) || !(v_scale > 0.f) || isinf(v_scale))
+    return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (k_cache == nullptr || v_cache == nullptr || key == nullptr || value == nullptr || slot_mapping == nullptr)
+    return PA_ERR_NULL_POINTER;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(key, 16) || !aligned(value, 16) ||
+      !aligned(slot_mapping, 8))
+    return PA_ERR_MISALIGNED;
+  if ((int64_t)num_tokens * cache->num_kv_heads > kInt32Max) return PA_ERR_TOO_LARGE;
+  cudaError_t e = pa::launch_reshape_and_cache_fp8(k_cache, v_cache, key, value, slot_mapping, num_tokens,
+                                                   cache->num_blocks, cache->block_size, cache->num_kv_heads,
+                                                   cache->head_size, k_scale, v_scale, err_flag,
+                                                   static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -20,7 +20,7 @@ int pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cach
                float scale, int32_t* err_flag, void* stream) {
   int rc = check_cache(cache);
   if (rc != PA_OK) return rc;
-  if (cache->dtype == PA_F32 || cache->head_size != 128) return PA_ERR_UNSUPPORTED;
+  if ((cache->dtype != PA_F16 && cache->dtype != PA_BF16) || cache->head_size != 128) return PA_ERR_UNSUPPORTED;
   if (cache->block_size > 128 || 128 % cache->block_size != 0) return PA_ERR_UNSUPPORTED;
   if (num_seqs < 0 || num_query_tokens < 0 || num_q_heads <= 0 || max_blocks_per_seq < 0 || max_query_len < 0)
     return PA_ERR_INVALID_ARG;

@@ -109,6 +109,23 @@ def test_prefill_argument_errors(lib):
     assert call_prefill(lib, desc(), mql=0) == 0
 
 
+def test_fp8_argument_errors(lib):
+    f8 = desc(dtype=pa.PA_FP8_E4M3)
+    assert call_decode(lib, desc(dtype=pa.PA_FP8_E4M3, d=64)) == 2   # FP8 is built for head_size 128
+    opts = pa.pa_decode_options(None, -1.0, 1.0)                     # negative scale
+    assert lib.pa_decode_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 4, ctypes.byref(f8), 0.1, 0, None, 0, None,
+                            None, ctypes.byref(opts)) == 3
+    assert lib.pa_reshape_and_cache(FAKE, FAKE, FAKE, FAKE, FAKE, 4, ctypes.byref(f8), None, None) == 2
+    fp8_append = lib.pa_reshape_and_cache_fp8
+    assert fp8_append(FAKE, FAKE, FAKE, FAKE, FAKE, 4, ctypes.byref(desc()), 1.0, 1.0, None, None) == 2
+    assert fp8_append(FAKE, FAKE, FAKE, FAKE, FAKE, 4, ctypes.byref(f8), 0.0, 1.0, None, None) == 3
+    assert fp8_append(FAKE, FAKE, FAKE, FAKE, FAKE, 4, ctypes.byref(f8), 1.0, float("inf"), None, None) == 3
+    assert fp8_append(FAKE, FAKE, None, FAKE, FAKE, 4, ctypes.byref(f8), 1.0, 1.0, None, None) == 1
+    assert fp8_append(FAKE + 8, FAKE, FAKE, FAKE, FAKE, 4, ctypes.byref(f8), 1.0, 1.0, None, None) == 5
+    assert fp8_append(FAKE, FAKE, FAKE, FAKE, FAKE, 0, ctypes.byref(f8), 1.0, 1.0, None, None) == 0
+    assert call_prefill(lib, f8) == 2                                   # no FP8 prefill
+
+
 def test_write_argument_errors(lib):
     d = desc()
     assert lib.pa_reshape_and_cache(FAKE, FAKE, FAKE, FAKE, FAKE, -1, ctypes.byref(d), None, None) == 3

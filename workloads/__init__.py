@@ -194,9 +194,14 @@ class Workload:
     def max_blocks_per_seq(self) -> int:
         return int(self.block_tables.shape[1])
 
+    @property
+    def cache_elem_bytes(self) -> int:
+        """Bytes per cache element: 1 for an FP8 cache, else those of the dtype."""
+        return 1 if self.info.get("kv_dtype") == "fp8" else ELEM_BYTES[self.dtype]
+
     def kv_bytes(self) -> int:
         """Algorithmic K+V bytes one attention call reads (each token once per KV head)."""
-        return int(self.seq_lens.astype(np.int64).sum()) * 2 * self.num_kv_heads * self.head_size * ELEM_BYTES[self.dtype]
+        return int(self.seq_lens.astype(np.int64).sum()) * 2 * self.num_kv_heads * self.head_size * self.cache_elem_bytes
 
     def unique_kv_bytes(self) -> int:
         """K+V bytes of distinct (block, slot) pairs read: shared prefix blocks count once."""
@@ -432,6 +437,33 @@ def build_prefill(name: str, *, seed: int, dtype: str, prefix_lens, chunk_lens, 
                     query_start=np.concatenate([[0], np.cumsum(chunk_lens)]).astype(np.int32))
 
 
+def mha_fp8(num_seqs: int = 64, max_len: int = 2048, min_len: int = 128, num_heads: int = 32,
+            num_blocks: int = 8192, materialize: bool = True) -> Workload:
+    """The MHA fp16 decode step over an FP8 (E4M3) cache: lens uniform in [128, 2048],
+    32 heads, D = 128, B = 16, pool of 8192 shuffled blocks, one appended token per
+    sequence.  Host arrays are fp16 (q, new K/V and the pools before quantisation);
+    the cache holds E4M3 codes of x / scale with the scales in ``info`` (about
+    max|x| / 448 for N(0,1) pools of this size)."""
+    rng = np.random.default_rng(1006)
+    lens = rng.integers(min_len, max_len, size=num_seqs, endpoint=True)
+    w = build_decode("mha_fp8", seed=1006, dtype="f16", seq_lens=lens, num_q_heads=num_heads,
+                     num_kv_heads=num_heads, head_size=128, block_size=16, num_blocks=num_blocks,
+                     append_last=True, materialize=materialize)
+    w.info.update(kv_dtype="fp8", k_scale=0.0123, v_scale=0.0117)
+    return w
+
+
+def gqa_fp8(num_seqs: int = 128, hi: int = 4096, materialize: bool = True) -> Workload:
+    """The GQA decode shapes (128 seqs, 64 q / 8 kv heads, D = 128, B = 32, lognormal
+    lens) over an FP8 (E4M3) cache with fp16 queries; scales in ``info``."""
+    rng = np.random.default_rng(1007)
+    lens = gqa_lens(num_seqs, rng, hi=hi)
+    w = build_decode("gqa_fp8", seed=1007, dtype="f16", seq_lens=lens, num_q_heads=64, num_kv_heads=8,
+                     head_size=128, block_size=32, pool_factor=1.2, materialize=materialize)
+    w.info.update(kv_dtype="fp8", k_scale=0.0123, v_scale=0.0117)
+    return w
+
+
 def prefill_bf16(num_seqs: int = 16, materialize: bool = True, max_prefix: int = 2048, min_chunk: int = 256,
                  max_chunk: int = 2048) -> Workload:
     """Chunked prefill, bf16: 16 sequences, cached prefix U[0, 2048] tokens, new
@@ -452,6 +484,8 @@ WORKLOADS = {
     "long_bf16_b32": lambda materialize=True: long_bf16(32, materialize=materialize),
     "long_bf16_b64": lambda materialize=True: long_bf16(64, materialize=materialize),
     "prefill_bf16": prefill_bf16,
+    "mha_fp8": mha_fp8,
+    "gqa_fp8": gqa_fp8,
 }
 
 
