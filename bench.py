@@ -70,6 +70,8 @@ KERNEL_SOURCES = ("pa_api.cu", "pa_decode_tc.cu", "pa_device.cuh", "pa_internal.
 
 # sources that define the prefill call's kernel
 PREFILL_SOURCES = ("pa_prefill_api.cu", "pa_prefill_tc.cu", "pa_prefill.h", "pa_device.cuh", "pa_internal.h")
+# sources that define the decode call on an FP8 cache
+FP8_SOURCES = ("pa_api.cu", "pa_decode_fp8.cu", "pa_device.cuh", "pa_internal.h", "pa_merge_and_cache.cu")
 
 
 def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
@@ -91,7 +93,8 @@ def ncu_traffic(workload: str):
     except (OSError, ValueError):
         return None
     entry = rec.get(workload)
-    sources = PREFILL_SOURCES if workload.startswith("prefill") else KERNEL_SOURCES
+    sources = (PREFILL_SOURCES if workload.startswith("prefill") else FP8_SOURCES if "fp8" in workload
+               else KERNEL_SOURCES)
     if not entry or entry.get("source_sha") != kernel_source_hash(sources):
         return None
     return entry.get("dram_bytes_per_launch")
