@@ -198,6 +198,19 @@ def test_fp8_copy_blocks_bit_exact():
     assert np.array_equal(k_dev.cpu().numpy(), kc) and np.array_equal(v_dev.cpu().numpy(), vc)
 
 
+def test_fp8_long_context_split():
+    """Two 8192-token sequences (B = 64) in 512-token partitions merged by the
+    log-sum-exp kernel, GQA 4:1, scores scaled up so the running max moves late."""
+    w = W.build_decode("fp8_long", seed=361, dtype="f16", seq_lens=[8192, 6001], num_q_heads=8, num_kv_heads=2,
+                       head_size=128, block_size=64, pool_factor=1.1, partition_size=512)
+    w.q = (w.q.astype(np.float32) * 3).astype(np.float16)
+    g = Fp8Step(w, 0.0123, 0.0117)
+    k, v = g.host_after_append()
+    got = g.decode()
+    assert int(g.err.item()) == 0
+    assert_close(got, g.oracle(k, v, partition_size=512), "fp8 long context")
+
+
 # ---------------------------------------------------------------- the full-size workloads
 @pytest.mark.parametrize("name", ["mha_fp8", "gqa_fp8"])
 def test_fp8_full_workload(name):
