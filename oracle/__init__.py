@@ -249,17 +249,29 @@ def quantize_e4m3(r) -> np.ndarray:
 
 def quantize_cache_fp8(cache_f16: np.ndarray, scale: float, values: bool) -> np.ndarray:
     """An fp16 pool [blocks][kv_heads][B][D] as E4M3 codes of x / scale (fp32 division),
-    in the FP8 layout: keys [blocks][kv_heads][B][D], values [blocks][kv_heads][D][B]."""
+    in the FP8 layout: keys [blocks][kv_heads][B][D], values [blocks][kv_heads][B/16][D][16]."""
     x = np.ascontiguousarray(cache_f16, dtype=np.float16).astype(np.float32)
     codes = quantize_e4m3(x / np.float32(scale))
-    return np.ascontiguousarray(codes.transpose(0, 1, 3, 2)) if values else codes
+    return values_to_fp8_layout(codes) if values else codes
+
+
+def values_to_fp8_layout(v: np.ndarray) -> np.ndarray:
+    """[blocks][kv_heads][B][D] -> [blocks][kv_heads][B/16][D][16] (the FP8 value layout)."""
+    nb, h, B, D = v.shape
+    return np.ascontiguousarray(v.reshape(nb, h, B // 16, 16, D).transpose(0, 1, 2, 4, 3))
+
+
+def values_from_fp8_layout(v: np.ndarray) -> np.ndarray:
+    """[blocks][kv_heads][B/16][D][16] -> [blocks][kv_heads][B][D]."""
+    nb, h, g, D, _ = v.shape
+    return np.ascontiguousarray(v.transpose(0, 1, 2, 4, 3).reshape(nb, h, g * 16, D))
 
 
 def paged_attention_fp8(q, k_cache, v_cache, block_tables, seq_lens, *, num_kv_heads: int, block_size: int,
                         scale: float, k_scale: float, v_scale: float, partition_size: int = 0, threads: int = 0,
                         alibi_slopes=None) -> np.ndarray:
     """Decode attention over an FP8 (E4M3) cache in float64: fp16 q [N, Hq, D]; key codes
-    [blocks][kv_heads][B][D], value codes [blocks][kv_heads][D][B]; k = k_scale * e4m3(code),
+    [blocks][kv_heads][B][D], value codes [blocks][kv_heads][B/16][D][16]; k = k_scale * e4m3(code),
     v = v_scale * e4m3(code)."""
     q = np.ascontiguousarray(q)
     _check_storage(q, "f16", "q")

@@ -108,7 +108,7 @@ def e4m3_value(code: int) -> float:
 def paged_attention_fp8(q_f16, k_codes, v_codes, block_tables, seq_lens, *, num_kv_heads: int, block_size: int,
                         scale: float, k_scale: float, v_scale: float) -> list:
     """Decode attention over an FP8 cache by brute force: keys [blocks][Hkv][B][D] and values
-    [blocks][Hkv][D][B] of E4M3 codes standing for k_scale (v_scale) times their value."""
+    [blocks][Hkv][B/16][D][16] of E4M3 codes standing for k_scale (v_scale) times their value."""
     N, Hq, D = q_f16.shape
     G = Hq // num_kv_heads
     qf = _flat_values(q_f16, "f16")
@@ -129,7 +129,8 @@ def paged_attention_fp8(q_f16, k_codes, v_codes, block_tables, seq_lens, *, num_
                 blk, off = int(block_tables[s][i // block_size]), i % block_size
                 base = (blk * num_kv_heads + hkv) * block_size * D
                 key = [k_scale * e4m3_value(kc[base + off * D + d]) for d in range(D)]
-                values.append([v_scale * e4m3_value(vc[base + d * block_size + off]) for d in range(D)])
+                vbase = base + (off // 16) * D * 16 + off % 16
+                values.append([v_scale * e4m3_value(vc[vbase + d * 16]) for d in range(D)])
                 scores.append(scale * sum(a * b for a, b in zip(qv, key)))
             mx = max(scores)
             ex = [math.exp(x - mx) for x in scores]

@@ -41,7 +41,9 @@
  * Layout codes: PAO_LAYOUT_OURS is [blocks][kv_heads][B][head_size], dense.
  * PAO_LAYOUT_PRIOR is the [P1] prior-art pair above, kept to pin the address
  * arithmetic against the page's worked example.  PAO_LAYOUT_FP8 pairs our key
- * layout with the [P1] value layout [blocks][kv_heads][head_size][B].
+ * layout with the [P1] value layout [blocks][kv_heads][head_size][B] tiled in
+ * 16-token groups: [blocks][kv_heads][B/16][head_size][16] (the same thing for
+ * B = 16), so that every 16 tokens of one head's values are contiguous.
  *
  * FP8 KV cache: [P1 "软件地址翻译"] allows cache_t to be FP8 (x = 16 /
  * sizeof(cache_t) = 16 elements per 16-byte access) and says nothing more.
@@ -184,6 +186,14 @@ int64_t pao_value_offset_prior(int64_t block, int64_t head, int64_t slot, int64_
   return block * kv_block_stride + head * kv_head_stride + d * B + slot;
 }
 
+/* FP8 value layout: [P1] value layout tiled in 16-token groups,
+ * [blocks][Hkv][B/16][D][16]; B is a multiple of 16. */
+int64_t pao_value_offset_fp8(int64_t block, int64_t head, int64_t slot, int64_t d, int Hkv, int B, int D) {
+  int64_t kv_block_stride = (int64_t)Hkv * D * B;
+  int64_t kv_head_stride = (int64_t)D * B;
+  return block * kv_block_stride + head * kv_head_stride + (slot / 16) * D * 16 + d * 16 + slot % 16;
+}
+
 static int64_t key_index(int layout, int64_t block, int64_t head, int64_t slot, int64_t d, int Hkv, int B, int D,
                          int dtype) {
   if (layout == PAO_LAYOUT_PRIOR) return pao_key_offset_prior(block, head, slot, d, Hkv, B, D, (int)(16 / elem_size(dtype)));
@@ -191,7 +201,8 @@ static int64_t key_index(int layout, int64_t block, int64_t head, int64_t slot, 
 }
 
 static int64_t value_index(int layout, int64_t block, int64_t head, int64_t slot, int64_t d, int Hkv, int B, int D) {
-  if (layout == PAO_LAYOUT_PRIOR || layout == PAO_LAYOUT_FP8) return pao_value_offset_prior(block, head, slot, d, Hkv, B, D);
+  if (layout == PAO_LAYOUT_PRIOR) return pao_value_offset_prior(block, head, slot, d, Hkv, B, D);
+  if (layout == PAO_LAYOUT_FP8) return pao_value_offset_fp8(block, head, slot, d, Hkv, B, D);
   return pao_offset_ours(block, head, slot, d, Hkv, B, D);
 }
 
@@ -325,6 +336,7 @@ static int check_problem(const pao_problem* p) {
   if (p->Hq % p->Hkv != 0) return PAO_BAD_ARG;
   if (p->dtype < PAO_F32 || p->dtype > PAO_FP8_E4M3) return PAO_BAD_ARG;
   if ((p->dtype == PAO_FP8_E4M3) != (p->layout == PAO_LAYOUT_FP8)) return PAO_BAD_ARG;
+  if (p->layout == PAO_LAYOUT_FP8 && p->B % 16 != 0) return PAO_BAD_ARG;
   if (p->layout == PAO_LAYOUT_PRIOR && p->D % (int)(16 / elem_size(p->dtype)) != 0) return PAO_BAD_ARG;
   for (int s = 0; s < p->N; ++s) {
     if (p->seq_lens[s] < 0) return PAO_BAD_ARG;
@@ -362,7 +374,7 @@ int pao_attention(double* out, const void* q, const void* k_cache, const void* v
   return err;
 }
 
-/* FP8 (E4M3) cache: keys [blocks][kv_heads][B][D] and values [blocks][kv_heads][D][B]
+/* FP8 (E4M3) cache: keys [blocks][kv_heads][B][D] and values [blocks][kv_heads][B/16][D][16]
  * of E4M3 codes, fp16 queries; the definition above with k = k_scale * e4m3(code),
  * v = v_scale * e4m3(code). */
 int pao_attention_fp8(double* out, const void* q_f16, const uint8_t* k_cache, const uint8_t* v_cache,
@@ -473,12 +485,12 @@ int pao_reshape_and_cache(void* k_cache, void* v_cache, const void* key, const v
 
 /* The FP8 append: as above, but each element of the fp16 key (value) row is
  * written as the E4M3 code of x / k_scale (x / v_scale), the division in fp32;
- * keys go to [block][head][offset][d], values to [block][head][d][offset]. */
+ * keys go to [block][head][offset][d], values to [block][head][offset/16][d][offset%16]. */
 int pao_reshape_and_cache_fp8(uint8_t* k_cache, uint8_t* v_cache, const uint16_t* key_f16, const uint16_t* value_f16,
                               const int64_t* slot_mapping, int T, int Hkv, int D, int B, int num_blocks,
                               float k_scale, float v_scale) {
   if (!k_cache || !v_cache || !key_f16 || !value_f16 || !slot_mapping || T < 0) return PAO_BAD_ARG;
-  if (!(k_scale > 0.0f) || !(v_scale > 0.0f)) return PAO_BAD_ARG;
+  if (!(k_scale > 0.0f) || !(v_scale > 0.0f) || B % 16 != 0) return PAO_BAD_ARG;
   for (int t = 0; t < T; ++t) {
     int64_t sl = slot_mapping[t];
     if (sl < 0) continue; /* padding token */
@@ -491,7 +503,7 @@ int pao_reshape_and_cache_fp8(uint8_t* k_cache, uint8_t* v_cache, const uint16_t
         const float xv = (float)pao_f16_to_f64(value_f16[src]);
         const float rk = xk / k_scale, rv = xv / v_scale;
         k_cache[pao_offset_ours(blk, h, off, d, Hkv, B, D)] = pao_f32_to_e4m3_sat(rk);
-        v_cache[pao_value_offset_prior(blk, h, off, d, Hkv, B, D)] = pao_f32_to_e4m3_sat(rv);
+        v_cache[pao_value_offset_fp8(blk, h, off, d, Hkv, B, D)] = pao_f32_to_e4m3_sat(rv);
       }
     }
   }

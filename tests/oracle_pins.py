@@ -469,7 +469,7 @@ def pin_e4m3_rounding():
     assert np.array_equal(O.quantize_e4m3(vals.astype(np.float32)), finite)
 
 
-def _fp8_case(seed, k_scale, v_scale, lens=None, Hq=4, Hkv=2, D=8, B=4):
+def _fp8_case(seed, k_scale, v_scale, lens=None, Hq=4, Hkv=2, D=8, B=16):
     w = small_case(seed, "f16", Hq=Hq, Hkv=Hkv, D=D, B=B, lens=lens)
     kc = O.quantize_cache_fp8(w.k_cache, k_scale, values=False)
     vc = O.quantize_cache_fp8(w.v_cache, v_scale, values=True)
@@ -479,20 +479,21 @@ def _fp8_case(seed, k_scale, v_scale, lens=None, Hq=4, Hkv=2, D=8, B=4):
 def pin_fp8_attention():
     """FP8 attention is the definition on the dequantised caches: with power-of-two
     scales it equals, bit for bit, the float32 evaluation of k_scale * e4m3(code)
-    (the value pool transposed back to [B][D] with numpy); with any scales it
+    (the value pool taken back to [B][D] with numpy); with any scales it
     agrees with the pure-Python brute force to 1e-12, and its split form with the
     unsplit one."""
     ks, vs = 2.0 ** -5, 2.0 ** -3
-    w, kc, vc = _fp8_case(181, ks, vs)
+    w, kc, vc = _fp8_case(181, ks, vs, B=16)
+    assert vc.shape[2:] == (1, w.head_size, 16)
     got = O.paged_attention_fp8(w.q, kc, vc, w.block_tables, w.seq_lens, num_kv_heads=w.num_kv_heads,
                                 block_size=w.block_size, scale=w.scale, k_scale=ks, v_scale=vs)
     kd = (O.to_f64(kc, "fp8") * ks).astype(np.float32)
-    vd = np.ascontiguousarray((O.to_f64(vc, "fp8") * vs).astype(np.float32).transpose(0, 1, 3, 2))
+    vd = O.values_from_fp8_layout((O.to_f64(vc, "fp8") * vs).astype(np.float32))
     ref = O.paged_attention(w.q.astype(np.float32), kd, vd, w.block_tables, w.seq_lens, dtype="f32",
                             num_kv_heads=w.num_kv_heads, block_size=w.block_size, scale=w.scale)
     assert np.array_equal(got, ref)
     ks, vs = 0.0113, 0.0371
-    w, kc, vc = _fp8_case(182, ks, vs, lens=[1, 6, 9])
+    w, kc, vc = _fp8_case(182, ks, vs, lens=[1, 6, 19, 40], B=32)
     kw = dict(num_kv_heads=w.num_kv_heads, block_size=w.block_size, scale=w.scale, k_scale=ks, v_scale=vs)
     got = O.paged_attention_fp8(w.q, kc, vc, w.block_tables, w.seq_lens, **kw)
     bf = np.array(brute.paged_attention_fp8(w.q, kc, vc, w.block_tables, w.seq_lens, **kw))
@@ -504,17 +505,17 @@ def pin_fp8_attention():
 def pin_fp8_append():
     """The FP8 append writes the code of x / scale (fp32 division; torch's
     conversion for in-range values) of token t's key at [block][head][offset][d]
-    and of its value at [block][head][d][offset]; padding slots are skipped and
-    every other byte is left as it was."""
+    and of its value at [block][head][offset / 16][d][offset % 16]; padding slots
+    are skipped and every other byte is left as it was."""
     import torch
     rng = np.random.default_rng(191)
-    Hkv, D, B, nb = 2, 16, 4, 6
+    Hkv, D, B, nb = 2, 16, 32, 3
     kc = rng.integers(0, 256, size=(nb, Hkv, B, D), dtype=np.uint8)
-    vc = rng.integers(0, 256, size=(nb, Hkv, D, B), dtype=np.uint8)
+    vc = rng.integers(0, 256, size=(nb, Hkv, B // 16, D, 16), dtype=np.uint8)
     k0, v0 = kc.copy(), vc.copy()
     key = (rng.standard_normal((5, Hkv, D)) * 2).astype(np.float16)
     val = (rng.standard_normal((5, Hkv, D)) * 2).astype(np.float16)
-    slots = np.array([7, -1, 0, 23, 13], dtype=np.int64)
+    slots = np.array([7, -1, 0, 53, 90], dtype=np.int64)
     ks, vs = 0.0231, 2.0 ** -4
     assert np.abs(key.astype(np.float32) / np.float32(ks)).max() < 448  # torch's conversion saturates nowhere here
     O.reshape_and_cache_fp8(kc, vc, key, val, slots, num_kv_heads=Hkv, block_size=B, k_scale=ks, v_scale=vs)
@@ -525,7 +526,7 @@ def pin_fp8_append():
             continue
         b, off = sl // B, sl % B
         k0[b, :, off, :] = kq[t]
-        v0[b, :, :, off] = vq[t]
+        v0[b, :, off // 16, :, off % 16] = vq[t]
     assert np.array_equal(kc, k0) and np.array_equal(vc, v0)
 
 

@@ -42,10 +42,12 @@ MUTANTS = [
     ("e4m3_subnormal", "v = ldexp((double)m, -9);", "v = ldexp((double)m, -8);"),
     ("e4m3_round_down", "nearbyint(a / ldexp(1.0, e - 3))", "floor(a / ldexp(1.0, e - 3))"),
     ("e4m3_no_saturation", "if (v > 448.0) return sign | 0x7E;", "if (v > 480.0) return sign | 0x7E;"),
-    ("fp8_value_layout", "layout == PAO_LAYOUT_PRIOR || layout == PAO_LAYOUT_FP8", "layout == PAO_LAYOUT_PRIOR"),
+    ("fp8_value_layout", "if (layout == PAO_LAYOUT_FP8) return pao_value_offset_fp8(",
+     "if (layout == PAO_LAYOUT_FP8) return pao_value_offset_prior("),
+    ("fp8_value_tile", "(slot / 16) * D * 16 + d * 16 + slot % 16", "(slot / 16) * D * 16 + d * 16 + slot % 8"),
     ("fp8_v_scale_dropped", "return p->v_scale * pao_load(", "return pao_load("),
     ("fp8_k_scale_dropped", "double kd = p->k_scale *", "double kd = 1.0 *"),
-    ("fp8_append_value_offset", "v_cache[pao_value_offset_prior(blk, h, off, d, Hkv, B, D)]",
+    ("fp8_append_value_offset", "v_cache[pao_value_offset_fp8(blk, h, off, d, Hkv, B, D)]",
      "v_cache[pao_offset_ours(blk, h, off, d, Hkv, B, D)]"),
     ("fp8_append_slot_swapped", "const int64_t blk = sl / B, off = sl % B;", "const int64_t blk = sl % B, off = sl / B;"),
     ("fp8_append_padding_written", "if (sl < 0) continue; /* padding token */", "if (sl < 0) sl = -sl;"),
