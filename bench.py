@@ -206,10 +206,11 @@ class DeviceStep:
         self.fp8 = w.info.get("kv_dtype") == "fp8"
         self.k_scale, self.v_scale = w.info.get("k_scale"), w.info.get("v_scale")
         self.k, self.v = W.device_caches(w, device)
-        if self.fp8:  # E4M3 codes of x / scale (torch's conversion: inputs only); values [blocks][heads][D][B]
+        if self.fp8:  # E4M3 codes of x / scale (torch's conversion: inputs only); values [blocks][heads][B/16][D][16]
             self.k = (self.k.float() / self.k_scale).to(torch.float8_e4m3fn).view(torch.uint8)
             self.v = (self.v.float() / self.v_scale).to(torch.float8_e4m3fn).view(torch.uint8)
-            self.v = self.v.transpose(2, 3).contiguous()
+            nb, hkv, bs, d = self.v.shape
+            self.v = self.v.view(nb, hkv, bs // 16, 16, d).transpose(3, 4).contiguous()
             torch.cuda.empty_cache()
         self.desc = pa.cache_desc(self.k)
 

@@ -62,8 +62,10 @@ typedef struct {
  *   - one fp32 scale per cache: a key code c stands for k_scale * e4m3(c), a
  *     value code for v_scale * e4m3(c) (scales > 0, passed per call);
  *   - keys   [num_blocks][num_kv_heads][block_size][head_size] bytes,
- *     values [num_blocks][num_kv_heads][head_size][block_size] bytes (the
- *     pages' value layout: a dimension's tokens are contiguous);
+ *     values [num_blocks][num_kv_heads][block_size/16][head_size][16] bytes:
+ *     the pages' value layout ([head_size][block_size], a dimension's tokens
+ *     contiguous) tiled in 16-token groups, identical to it for block_size 16,
+ *     so that the values of every 16 tokens of one head are contiguous;
  *   - q, out and the key/value rows written by pa_reshape_and_cache_fp8 are fp16;
  *   - written codes are the E4M3 code nearest to x / scale (fp32 division,
  *     ties to even; magnitudes past 448, infinities included, saturate to 448).
@@ -211,7 +213,8 @@ int pa_reshape_and_cache(void* k_cache, void* v_cache, const void* key, const vo
  *   fp16 key/value [num_tokens][num_kv_heads][head_size] (16-byte aligned) are
  *   written as E4M3 codes of x / k_scale and x / v_scale (see "FP8 caches"
  *   above): key[t][h][d] at (block, h, offset, d), value[t][h][d] at (block, h,
- *   d, offset).  Slots as for pa_reshape_and_cache.  k_scale, v_scale > 0.
+ *   offset / 16, d, offset % 16).  Slots as for pa_reshape_and_cache.
+ *   k_scale, v_scale > 0.
  */
 int pa_reshape_and_cache_fp8(void* k_cache, void* v_cache, const void* key, const void* value,
                              const int64_t* slot_mapping, int32_t num_tokens, const pa_cache_desc* cache,

@@ -112,7 +112,7 @@ def _dtype_code(t) -> int:
 def cache_desc(k_cache) -> pa_cache_desc:
     """Descriptor of a [num_blocks, num_kv_heads, block_size, head_size] key-cache tensor
     (uint8 or float8_e4m3fn storage means an FP8 E4M3 cache, whose values are
-    [num_blocks, num_kv_heads, head_size, block_size])."""
+    [num_blocks, num_kv_heads, block_size / 16, head_size, 16])."""
     if k_cache.dim() != 4:
         raise ValueError("cache must be [num_blocks, num_kv_heads, block_size, head_size]")
     nb, hkv, bs, d = (int(x) for x in k_cache.shape)
@@ -226,7 +226,7 @@ def pa_reshape_and_cache(k_cache, v_cache, key, value, slot_mapping, err_flag=No
 def pa_reshape_and_cache_fp8(k_cache, v_cache, key, value, slot_mapping, k_scale: float, v_scale: float,
                              err_flag=None, stream=None, desc: pa_cache_desc | None = None) -> None:
     """Write fp16 key/value [num_tokens, num_kv_heads, head_size] into an FP8 cache as
-    E4M3 codes of x / k_scale and x / v_scale (values transposed per block)."""
+    E4M3 codes of x / k_scale and x / v_scale (values at [block, head, offset / 16, d, offset % 16])."""
     desc = desc or cache_desc(k_cache)
     for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (key, "key"), (value, "value"),
                  (slot_mapping, "slot_mapping")):

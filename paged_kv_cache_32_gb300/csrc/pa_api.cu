@@ -30,10 +30,8 @@ int check_cache(const pa_cache_desc* c) {
   if (c->head_size != 64 && c->head_size != 128) return PA_ERR_UNSUPPORTED;
   if (c->dtype == PA_FP8_E4M3 && c->head_size != 128) return PA_ERR_UNSUPPORTED;
   if (c->dtype != PA_F32 && (c->block_size % 16 != 0 || c->block_size > 256)) return PA_ERR_UNSUPPORTED;
-  // row index (block * Hkv + head) * B + slot (and, for FP8 values, * D + d) must fit the kernels' int32 arithmetic
+  // row index (block * Hkv + head) * B + slot must fit the kernels' int32 arithmetic
   if ((int64_t)c->num_blocks * c->num_kv_heads * c->block_size > kInt32Max) return PA_ERR_TOO_LARGE;
-  if (c->dtype == PA_FP8_E4M3 && (int64_t)c->num_blocks * c->num_kv_heads * c->head_size > kInt32Max)
-    return PA_ERR_TOO_LARGE;
   return PA_OK;
 }
 
@@ -90,10 +88,9 @@ bool encode_cache_map(CUtensorMap* map, const void* base, const pa_cache_desc* c
   return r == CUDA_SUCCESS;
 }
 
-// FP8 caches: keys as rows of D bytes (box 16 rows x 128 bytes, 128-byte swizzle); values as rows
-// of B bytes, one per (block, head, dimension) (box 128 rows x 16 bytes, no swizzle)
-bool encode_fp8_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k_cache, const void* v_cache,
-                     const pa_cache_desc* c) {
+// FP8 keys as rows of D bytes (box 16 rows x 128 bytes, 128-byte swizzle); FP8 values need no map
+// (every 16 tokens of one head are one contiguous run, read by 1-D bulk copies)
+bool encode_fp8_key_map(CUtensorMap* tk, const void* k_cache, const pa_cache_desc* c) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   cuuint32_t estr[2] = {1, 1};
@@ -104,13 +101,6 @@ bool encode_fp8_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k_cache, cons
   CUresult r = enc(tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(k_cache), kdims, kstrides, kbox, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return false;
-  cuuint64_t vdims[2] = {(cuuint64_t)c->block_size, heads * c->head_size};
-  cuuint64_t vstrides[1] = {(cuuint64_t)c->block_size};
-  cuuint32_t vbox[2] = {(cuuint32_t)pa::kTcSlabTokens, (cuuint32_t)c->head_size};
-  r = enc(tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(v_cache), vdims, vstrides, vbox, estr,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -228,9 +218,9 @@ int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_ca
     e = pa::launch_decode_f32(cache->head_size, static_cast<const float*>(k_cache),
                               static_cast<const float*>(v_cache), p, st);
   } else if (cache->dtype == PA_FP8_E4M3) {
-    CUtensorMap tk, tv;
-    if (!encode_fp8_maps(&tk, &tv, k_cache, v_cache, cache)) return PA_ERR_CUDA;
-    e = pa::launch_decode_fp8(cache->head_size, tk, tv, p, k_scale, v_scale, st);
+    CUtensorMap tk;
+    if (!encode_fp8_key_map(&tk, k_cache, cache)) return PA_ERR_CUDA;
+    e = pa::launch_decode_fp8(cache->head_size, tk, v_cache, p, k_scale, v_scale, st);
   } else {
     CUtensorMap tk, tv;
     if (!encode_cache_map(&tk, k_cache, cache, pa::kTcSlabTokens) ||

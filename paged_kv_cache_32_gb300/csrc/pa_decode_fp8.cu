@@ -11,14 +11,18 @@
 // ties to even, saturating at +-448).
 //
 // Layout: keys [blocks][kv_heads][B][D] (a token's key is one D-byte row),
-// values [blocks][kv_heads][D][B] (the value layout of "软件地址翻译": a
-// dimension's B tokens are contiguous).
+// values [blocks][kv_heads][B/16][D][16]: the value layout of "软件地址翻译"
+// ([D][B], a dimension's tokens contiguous) tiled in groups of 16 tokens, the
+// same thing for B = 16, so that the values of every 16 tokens of one head are
+// one contiguous 2 KB run for any block size.
 //
 // How: the structure of the fp16/bf16 kernel (one CTA per (sequence, kv head,
 // head group, partition), four warps each streaming slabs through a private
-// ring filled by tensor-map copies).  A slab is 32 tokens: two 16-token
-// sub-slabs, each inside one block, each one 2 KB box of keys (16 rows x 128
-// bytes, 128-byte swizzle) and one 2 KB box of values (128 rows of 16 bytes);
+// ring filled by asynchronous bulk copies).  A slab is 32 tokens: two 16-token
+// sub-slabs, each inside one block, each one 2 KB tensor-map box of keys (16
+// rows x 128 bytes, 128-byte swizzle) and one 2 KB 1-D bulk copy of values
+// (D rows of 16 bytes; a tensor-map box of 128 rows x 16 bytes moves the same
+// bytes measurably slower);
 // 32 tokens per slab halve the fixed per-slab work (barrier wait, block-table
 // shuffle, row-max shuffles) per byte against 16.  The output rescale is
 // skipped when no running max of the warp moved.  E4M3 values convert exactly to fp16 (cvt e4m3x2 -> f16x2), so
@@ -52,7 +56,7 @@ struct Fp8Shape {
   static constexpr int NSUB = 2;                          // sub-slabs per slab
   static constexpr int SB = SUB * NSUB;                   // tokens per slab
   static constexpr int KBOX = SUB * D;                    // key box: 16 rows x D bytes
-  static constexpr int VBOX = D * SUB;                    // value box: D rows x 16 bytes
+  static constexpr int VBOX = D * SUB;                    // value run: D rows x 16 bytes, contiguous
   static constexpr int SLAB_BYTES = NSUB * (KBOX + VBOX); // keys of both sub-slabs, then their values
   static constexpr int RING_BYTES = NS * SLAB_BYTES;      // per warp
   static constexpr int OROW = D + 4;                      // merge row stride (floats)
@@ -253,7 +257,7 @@ __device__ __forceinline__ void fp8_slab(const uint8_t* kst, const uint8_t* vst,
 
 template <int D, int NW, int NS>
 __global__ void __launch_bounds__(Fp8Shape<D, NW, NS>::THREADS)
-    decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+    decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k, const uint8_t* __restrict__ v_cache,
                       const DecodeParams p, const float k_scale, const float v_scale) {
   using S = Fp8Shape<D, NW, NS>;
   Fp8Item it;
@@ -337,7 +341,9 @@ __global__ void __launch_bounds__(Fp8Shape<D, NW, NS>::THREADS)
           const int slot0 = sub_tok(k, u) % B;  // first token of the sub-slab in its block
           const int head_row = pb * p.num_kv_heads + it.hkv;
           tma_load_2d(dst + u * S::KBOX, &tmap_k, 0, head_row * B + slot0, bar);
-          tma_load_2d(dst + S::NSUB * S::KBOX + u * S::VBOX, &tmap_v, slot0, head_row * D, bar);
+          // values of tokens slot0 .. slot0 + 15 (slot0 a multiple of 16): [D][16] at (head_row * B + slot0) * D
+          bulk_load_1d(dst + S::NSUB * S::KBOX + u * S::VBOX, v_cache + (size_t)(head_row * B + slot0) * D, S::VBOX,
+                       bar);
         }
       } else {
         report_error(p.err_flag, PA_DEVERR_BLOCK_ID);
@@ -431,7 +437,7 @@ __global__ void __launch_bounds__(Fp8Shape<D, NW, NS>::THREADS)
 
 // The quantising append: block (token, kv head); thread d handles element d.
 // Keys go to [block][head][offset][d] (one coalesced row), values to
-// [block][head][d][offset].
+// [block][head][offset / 16][d][offset % 16].
 __global__ void __launch_bounds__(128)
     reshape_and_cache_fp8_kernel(uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
                                  const __half* __restrict__ key, const __half* __restrict__ value,
@@ -448,6 +454,7 @@ __global__ void __launch_bounds__(128)
   }
   const size_t src = ((size_t)t * num_kv_heads + h) * head_size;
   const size_t head_base = ((size_t)blk * num_kv_heads + h) * (size_t)block_size * head_size;
+  const size_t vtile = head_base + (size_t)(off / 16) * head_size * 16 + off % 16;  // + 16 d
   for (int d = 2 * threadIdx.x; d < head_size; d += 2 * blockDim.x) {
     const __half2 kx = *reinterpret_cast<const __half2*>(key + src + d);
     const __half2 vx = *reinterpret_cast<const __half2*>(value + src + d);
@@ -456,14 +463,14 @@ __global__ void __launch_bounds__(128)
     const __nv_fp8x2_storage_t kc = __nv_cvt_float2_to_fp8x2(kr, __NV_SATFINITE, __NV_E4M3);
     const __nv_fp8x2_storage_t vc = __nv_cvt_float2_to_fp8x2(vr, __NV_SATFINITE, __NV_E4M3);
     *reinterpret_cast<__nv_fp8x2_storage_t*>(k_cache + head_base + (size_t)off * head_size + d) = kc;
-    v_cache[head_base + (size_t)d * block_size + off] = (uint8_t)(vc & 0xff);  // element d: the low byte
-    v_cache[head_base + (size_t)(d + 1) * block_size + off] = (uint8_t)(vc >> 8);
+    v_cache[vtile + (size_t)d * 16] = (uint8_t)(vc & 0xff);  // element d: the low byte
+    v_cache[vtile + (size_t)(d + 1) * 16] = (uint8_t)(vc >> 8);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_decode_fp8(int head_size, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+cudaError_t launch_decode_fp8(int head_size, const CUtensorMap& tk, const void* v_cache, const DecodeParams& p,
                               float k_scale, float v_scale, cudaStream_t stream) {
   if (head_size != 128) return cudaErrorInvalidValue;
   using S = Fp8Shape<128, 4, 2>;
@@ -472,7 +479,8 @@ cudaError_t launch_decode_fp8(int head_size, const CUtensorMap& tk, const CUtens
   if (e != cudaSuccess) return e;
   const long long items = (long long)p.num_seqs * p.num_kv_heads * p.head_groups * p.pmax;
   if (items == 0) return cudaSuccess;
-  kernel<<<(unsigned)items, S::THREADS, S::SMEM_BYTES, stream>>>(tk, tv, p, k_scale, v_scale);
+  kernel<<<(unsigned)items, S::THREADS, S::SMEM_BYTES, stream>>>(tk, static_cast<const uint8_t*>(v_cache), p,
+                                                                  k_scale, v_scale);
   return cudaGetLastError();
 }
 

@@ -2,8 +2,8 @@
 
 Reading ("PagedAttention 详解：缓存的存储结构", section "软件地址翻译": cache_t may be
 FP8): a key code c stands for k_scale * e4m3(c), a value code for v_scale *
-e4m3(c); values are stored [blocks][kv_heads][D][B]; queries and outputs are
-fp16.  Both sides quantise nothing on their own for the attention tests: the
+e4m3(c); values are stored [blocks][kv_heads][B/16][D][16] (the pages' [D][B]
+value layout tiled in 16-token groups); queries and outputs are fp16.  Both sides quantise nothing on their own for the attention tests: the
 host pools are turned into codes once by the oracle's quantiser and the same
 bytes go to the GPU.
 
@@ -104,7 +104,7 @@ def test_fp8_append_bit_exact():
     rng = np.random.default_rng(301)
     nb, hkv, B, D, T = 12, 4, 32, 128, 40
     kc = rng.integers(0, 256, size=(nb, hkv, B, D), dtype=np.uint8)
-    vc = rng.integers(0, 256, size=(nb, hkv, D, B), dtype=np.uint8)
+    vc = rng.integers(0, 256, size=(nb, hkv, B // 16, D, 16), dtype=np.uint8)
     key = (rng.standard_normal((T, hkv, D)) * np.exp(rng.uniform(-9, 3, (T, hkv, D)))).astype(np.float16)
     val = (rng.standard_normal((T, hkv, D)) * 4).astype(np.float16)
     key[0, 0, :4] = [np.inf, -np.inf, 60000.0, -6.0]          # saturate with k_scale below
@@ -127,14 +127,14 @@ def test_fp8_append_bad_slot_reported():
     import torch
     import paged_kv_cache_32_gb300 as pa
     k_dev = torch.zeros((2, 1, 16, 128), dtype=torch.uint8, device="cuda")
-    v_dev = torch.zeros((2, 1, 128, 16), dtype=torch.uint8, device="cuda")
+    v_dev = torch.zeros((2, 1, 1, 128, 16), dtype=torch.uint8, device="cuda")
     key = torch.ones((2, 1, 128), dtype=torch.float16, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     slots = torch.tensor([5, 2 * 16 + 3], dtype=torch.int64, device="cuda")
     pa.pa_reshape_and_cache_fp8(k_dev, v_dev, key, key, slots, 1.0, 1.0, err_flag=err, desc=pa.cache_desc(k_dev))
     torch.cuda.synchronize()
     assert int(err.item()) == 2
-    assert int(k_dev[0, 0, 5, 0].item()) == 0x38 and int(v_dev[0, 0, 7, 5].item()) == 0x38  # 1.0 written
+    assert int(k_dev[0, 0, 5, 0].item()) == 0x38 and int(v_dev[0, 0, 0, 7, 5].item()) == 0x38  # 1.0 written
     assert int(k_dev.sum().item()) == 0x38 * 128 and int(v_dev.sum().item()) == 0x38 * 128
 
 
@@ -182,12 +182,12 @@ def test_fp8_bad_block_id_reported():
 
 
 def test_fp8_copy_blocks_bit_exact():
-    """Copy-on-write of whole blocks moves the FP8 bytes of both pools (values transposed) unchanged."""
+    """Copy-on-write of whole blocks moves the FP8 bytes of both pools (values tiled) unchanged."""
     import torch
     import paged_kv_cache_32_gb300 as pa
     rng = np.random.default_rng(351)
-    kc = rng.integers(0, 256, size=(10, 2, 16, 128), dtype=np.uint8)
-    vc = rng.integers(0, 256, size=(10, 2, 128, 16), dtype=np.uint8)
+    kc = rng.integers(0, 256, size=(10, 2, 32, 128), dtype=np.uint8)
+    vc = rng.integers(0, 256, size=(10, 2, 2, 128, 16), dtype=np.uint8)
     pairs = np.array([[1, 7], [4, 2], [9, 0]], dtype=np.int32)
     k_dev, v_dev = u8(kc), u8(vc)
     pa.pa_copy_blocks(k_dev, v_dev, u8(pairs), desc=pa.cache_desc(k_dev))
