@@ -10,7 +10,7 @@
 // 0..p: out = softmax_i(scale * q . k_i) v_i.  Keys and values of token i come
 // from offset i % B of block block_tables[s][i / B] (section "软件地址翻译").
 //
-// How (one CTA per sequence, query head and tile of 128 queries; 12 warps):
+// How (one CTA per sequence, query head and tile of 128 queries; 14 warps):
 //  * Tensor memory (512 columns): two S buffers (0..127, 128..255), the
 //    output accumulator O (256..383) and the query tile Q (384..447, two
 //    16-bit elements per column).  Q is written there once by the first four
@@ -19,16 +19,18 @@
 //    MMA with both operands in shared memory runs at about half rate at this
 //    shape, limited by the shared-memory read bandwidth).
 //  * Data: key and value tiles of 128 tokens are gathered block by block
-//    through the block table by two producer warps (one for K, one for V)
-//    with 2-D tensor-map copies (one per block and 64-column half, 128-byte
-//    swizzle) into two-stage rings; each copy's lane arrives on the stage
-//    barrier with its bytes.  A producer refills a stage as soon as the MMA
-//    that read it has finished.  Value rows past the sequence must read as
-//    zeros (P is 0 there, but 0 * NaN is not): the V producer copies the
-//    last, partial block row by row with cp.async and zero-fills the rest,
-//    then fences those generic-proxy writes before its extra arrival.
+//    through the block table by four producer warps (K and V, one warp per
+//    64-column half: a single thread issues a copy in about 200 cycles and
+//    the lanes of one warp largely serialise, so the copies of a tile are
+//    spread over warps) with 2-D tensor-map copies (one per block and half,
+//    128-byte swizzle) into two-stage rings; each copy's lane arrives on the
+//    stage barrier with its bytes.  A producer refills a stage as soon as the
+//    MMA that read it has finished.  Value rows past the sequence must read as
+//    zeros (P is 0 there, but 0 * NaN is not): each V producer copies its half
+//    of the last, partial block row by row with cp.async and zero-fills the
+//    rest, then fences those generic-proxy writes before its extra arrival.
 //  * Two threads in different warps issue the MMAs (kind::f16, fp32
-//    accumulation): warp 11 S = Q K^T (M = 128 queries, N = 128 keys, K = D),
+//    accumulation): warp 9 S = Q K^T (M = 128 queries, N = 128 keys, K = D),
 //    warp 8 O += P V (M = 128, N = D, K = 128 keys; P from tensor memory).
 //    S of tile kt + 2 goes into the buffer of tile kt once P V of tile kt has
 //    finished; with separate issuers that wait never delays the next P V, and
@@ -70,11 +72,10 @@ constexpr int kSmemBytes = kBarOff + 128 + 2 * 2 * kTile * 4 + 2 * kTile * 4 + 1
 constexpr uint32_t kOCol = 256;       // tensor-memory column of O
 constexpr uint32_t kQCol = 384;       // tensor-memory column of Q
 constexpr int kSoftmaxWarps = 8;
-constexpr int kPVWarp = kSoftmaxWarps;     // issues O += P V
-constexpr int kKLoadWarp = kSoftmaxWarps + 1;
-constexpr int kVLoadWarp = kSoftmaxWarps + 2;
-constexpr int kSWarp = kSoftmaxWarps + 3;  // issues S = Q K^T
-constexpr int kThreads = (kSoftmaxWarps + 4) * 32;
+constexpr int kPVWarp = kSoftmaxWarps;         // issues O += P V
+constexpr int kSWarp = kSoftmaxWarps + 1;      // issues S = Q K^T
+constexpr int kLoadWarp0 = kSoftmaxWarps + 2;  // four producers: K half 0, K half 1, V half 0, V half 1
+constexpr int kThreads = (kSoftmaxWarps + 6) * 32;
 constexpr float kRescaleThreshold = 8.f;  // log2 units: P <= 2^8 between rescales
 constexpr long long kWaitCyclesPf = 500ll * 1000 * 1000;
 
@@ -113,6 +114,20 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   return true;
 }
 
+// the same, spinning: for the waits on the critical path (the MMA issuers, and the softmax waiting
+// for S), where waking a parked thread costs a few hundred cycles
+__device__ __forceinline__ bool wait_bar_spin(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCyclesPf) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+  return true;
+}
 // drain wait: bounded, ignores the abort flag
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   const long long t0 = clock64();
@@ -308,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_q, 4);  // the four warps that write Q
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bar_k[b], slots);      // each copy slot arrives once per tile (with its bytes, or none)
-      mbar_init(&bar_v[b], slots + 1);  // + the partial-block / zero-fill arrival
+      mbar_init(&bar_v[b], slots + 2);  // + each V producer's partial-block / zero-fill arrival
       mbar_init(&bar_s[b], 1);
       mbar_init(&bar_p[b], kSoftmaxWarps);
       mbar_init(&bar_o[b], 1);
@@ -332,18 +347,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag));
   };
 
-  if (warp == kKLoadWarp || warp == kVLoadWarp) {
-    // =================================================================== producers: K or V tiles
-    const bool is_v = warp == kVLoadWarp;
+  if (warp >= kLoadWarp0) {
+    // =================================================================== producers: one half of K or V tiles
+    const bool is_v = warp >= kLoadWarp0 + 2;
+    const int half = (warp - kLoadWarp0) & 1;  // columns 64 half .. 64 half + 63
     const T* cache = static_cast<const T*>(is_v ? p.v_cache : p.k_cache);
     const CUtensorMap* tmap = is_v ? &tmap_v : &tmap_k;
     uint8_t* ring = smem + (is_v ? kVOff : kKOff);
     constexpr int kPastEnd = INT_MIN;
-    // lane c < slots copies block c / 2, column half c % 2 of every tile; its table entry is read one tile ahead
-    const int blk = lane >> 1, half = lane & 1;
+    // lane b < blocks_per_tile copies this half of block b of every tile; its table entry is read one tile ahead
+    const int blk = lane;
     auto fetch = [&](int kt) -> int {
       const int bi = kt * blocks_per_tile + blk;
-      return (lane < slots && kt < key_tiles && bi < nblocks_seq) ? __ldg(table + bi) : kPastEnd;
+      return (blk < blocks_per_tile && kt < key_tiles && bi < nblocks_seq) ? __ldg(table + bi) : kPastEnd;
     };
     if (lane == 0) tma_prefetch_descriptor(tmap);
     int entry_next = fetch(0);
@@ -354,31 +370,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int entry = entry_next;
       entry_next = fetch(t + 1);
       uint64_t* bar = is_v ? &bar_v[t & 1] : &bar_k[t & 1];
-      uint8_t* st = ring + (t & 1) * 2 * kHalf;
+      uint8_t* st = ring + (t & 1) * 2 * kHalf + half * kHalf;
       const bool in_pool = entry >= 0 && entry < p.num_blocks;
       if (!is_v && half == 0 && entry != kPastEnd && !in_pool) report_error(p.err_flag, PA_DEVERR_BLOCK_ID);
       // V: only blocks entirely inside the sequence go by tensor-map copy
       const bool whole = in_pool && (!is_v || (t * blocks_per_tile + blk + 1) * B <= L);
-      if (lane < slots) {
+      if (blk < blocks_per_tile) {
         if (whole) {
           mbar_arrive_expect_tx(bar, (uint32_t)B * 128);
-          tma_load_2d(st + half * kHalf + blk * B * 128, tmap, half * 64, (entry * p.num_kv_heads + hkv) * B, bar);
+          tma_load_2d(st + blk * B * 128, tmap, half * 64, (entry * p.num_kv_heads + hkv) * B, bar);
         } else {
           mbar_arrive(bar);
         }
       }
       if (is_v) {
-        // blocks not copied above: rows inside the sequence of an in-pool block by cp.async, the rest zeros
-        const unsigned partial = __ballot_sync(0xffffffffu, lane < slots && half == 0 && !whole);
+        // this half of the blocks not copied above: rows inside the sequence of an in-pool block by
+        // cp.async, the rest zeros.  Four rows of eight 16-byte chunks per step; the four rows lie in
+        // one block (B is a multiple of 16), so every branch below is uniform across the warp.
+        const unsigned partial = __ballot_sync(0xffffffffu, blk < blocks_per_tile && !whole);
         if (partial) {
-          for (int r = lane >> 4; r < kTile; r += 2) {  // 16 chunks of 16 bytes per row, two rows per step
-            const int b = r / B;
-            if (!((partial >> (2 * b)) & 1)) continue;
-            const int e = __shfl_sync(__activemask(), entry, 2 * b);
-            const int pos = t * kTile + r, chunk = lane & 15;
-            uint8_t* dst = st + (chunk >> 3) * kHalf + swz128(r, chunk & 7);
+          const int first = (__ffs(partial) - 1) * B;  // rows before the first such block are all copied
+          for (int r0 = first; r0 < kTile; r0 += 4) {
+            const int b = r0 / B;
+            const int e = __shfl_sync(0xffffffffu, entry, b);
+            if (!((partial >> b) & 1)) continue;
+            const int r = r0 + (lane >> 3), chunk = lane & 7;
+            const int pos = t * kTile + r;
+            uint8_t* dst = st + swz128(r, chunk);
             if (pos < L && e >= 0 && e < p.num_blocks)
-              cp_async16(dst, cache + (((size_t)e * p.num_kv_heads + hkv) * B + (pos % B)) * kD + chunk * 8);
+              cp_async16(dst, cache + (((size_t)e * p.num_kv_heads + hkv) * B + (pos % B)) * kD + half * 64 +
+                                  chunk * 8);
             else
               *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
           }
@@ -398,8 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; ok && t < key_tiles; ++t) {
         // buffer t % 2 held P of tile t - 2 (its P V must have finished; the barrier's next phase,
         // tile t, needs this S, so the wait is exact) and K stage t % 2 must hold key tile t
-        if (t >= 2) ok = wait_bar(&bar_o[t & 1], ((t - 2) >> 1) & 1, abort_flag);
-        ok = ok && wait_bar(&bar_k[t & 1], (t >> 1) & 1, abort_flag);
+        if (t >= 2) ok = wait_bar_spin(&bar_o[t & 1], ((t - 2) >> 1) & 1, abort_flag);
+        ok = ok && wait_bar_spin(&bar_k[t & 1], (t >> 1) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
         const uint32_t kb = smem_u32(smem + kKOff + (t & 1) * 2 * kHalf);
@@ -420,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kt = 0; ok && kt < key_tiles; ++kt) {
         const int buf = kt & 1;
         // once every softmax warp has written P of tile kt and V of tile kt is in place
-        ok = wait_bar(&bar_p[buf], (kt >> 1) & 1, abort_flag) && wait_bar(&bar_v[buf], (kt >> 1) & 1, abort_flag);
+        ok = wait_bar_spin(&bar_p[buf], (kt >> 1) & 1, abort_flag) && wait_bar_spin(&bar_v[buf], (kt >> 1) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
         const uint32_t vb = smem_u32(smem + kVOff + buf * 2 * kHalf);
@@ -477,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // so no warp can be left waiting on a barrier that another warp has stopped visiting.
     for (int kt = 0; kt < key_tiles; ++kt) {
       const int buf = kt & 1;
-      ok = warp_wait(&bar_s[buf], (kt >> 1) & 1) && ok;
+      ok = __all_sync(0xffffffffu, wait_bar_spin(&bar_s[buf], (kt >> 1) & 1, abort_flag)) && ok;
       tc_fence_after();
       const uint32_t s_addr = tmem + lane_base + buf * 128 + 64 * g;
       float v[64];
@@ -566,8 +587,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // a wait expired (the flag is stable: every thread has left its loop): record it, and let the
     // copies and MMAs this CTA started finish, each wait bounded, before its memory is released
     if (threadIdx.x == 0) report_error(p.err_flag, PA_DEVERR_TIMEOUT);
-    if ((warp == kKLoadWarp || warp == kVLoadWarp) && lane == 0) {  // copies still landing
-      uint64_t* ring_bar = warp == kVLoadWarp ? bar_v : bar_k;
+    if (warp >= kLoadWarp0 && lane == 0) {  // copies still landing
+      uint64_t* ring_bar = warp >= kLoadWarp0 + 2 ? bar_v : bar_k;
       for (int t = max(0, n_issued - 2); t < n_issued; ++t) drain_wait(&ring_bar[t & 1], (t >> 1) & 1);
     }
     if (warp == kSWarp && lane == 0)
