@@ -35,17 +35,19 @@
 //    S of tile kt + 2 goes into the buffer of tile kt once P V of tile kt has
 //    finished; with separate issuers that wait never delays the next P V, and
 //    the softmax of tile kt + 1 overlaps P V of tile kt and S of tile kt + 2.
-//  * Warps 0..7 run the softmax as two groups: group g owns keys
-//    64g .. 64g + 63 of every key tile (columns of S); thread = query row in
-//    the 32x32b tensor-memory layout.  The groups exchange their tile row
-//    maxima through shared memory, so both use one reference max per row and
-//    accumulate into the same O.  P is written back into the S columns it
-//    came from (tcgen05.st); bf16 P is written as two terms hi + lo (two
-//    MMAs), since 8 significant bits alone would cost up to 2^-8 of a weight.
+//  * Warps 0..7 run the softmax.  Each owns 16 query rows (tensor-memory
+//    lanes) and all 128 keys of a tile, read with the 16-lane 16x256b shape:
+//    a thread holds two rows, 32 keys of each, so a row's maximum and sum
+//    take two shuffles among its four threads and no warp waits for another.
+//    P is written back into the S buffer it came from (16x128b shape, two
+//    keys per 32-bit column: hi words in columns 0..63, lo words in
+//    64..127); bf16 P is written as two terms hi + lo (two MMAs), since 8
+//    significant bits alone would cost up to 2^-8 of a weight.
 //  * Rescaling: a row's reference max moves only when the tile max exceeds it
 //    by more than 8 (log2 units), so P <= 2^8 and O is rescaled in place
-//    (tcgen05.ld / st, each group its 64 columns) on few tiles.
-//  * Epilogue: out = O / (l0 + l1), each group writing its 64 columns.
+//    (tcgen05.ld / st of the warp's 16 rows) on few tiles.
+//  * Epilogue: the row sums go through shared memory once; out = O / l, two
+//    warps per lane quarter each writing 64 columns of its 32 rows.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -199,6 +201,41 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// The 16-lane shapes: a warp addresses one half (16 lanes) of its lane quarter.  Thread t holds
+// lanes t / 4 and t / 4 + 8 of that half.
+//  16x256b.x8 (64 columns): v[4j], v[4j + 1] = lane t / 4, columns 8j + 2 (t % 4) and + 1;
+//                           v[4j + 2], v[4j + 3] = lane t / 4 + 8, the same columns.
+//  16x128b.x8 (32 columns): r[2j] = lane t / 4, column 4j + t % 4; r[2j + 1] = lane t / 4 + 8.
+__device__ __forceinline__ void tmem_ld16x256_x8(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st16x256_x8(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16x128_x8(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -237,37 +274,51 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
 // all of this thread's cp.async copies have landed (commits the pending ones first)
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// P of one row's 64 keys (two per 32-bit column, lower key in the low half) from
-// the scores v (raw q . k), the scale in log2 units and the reference max; keys
-// i > lim are masked.  Writes hi (and for bf16 lo) words; returns the row sum
-// of the unrounded weights.
+// P of 8 of the 16 key pairs this thread holds in each of its two rows, pairs j0 .. j0 + 7 (v in
+// the 16x256b layout over the tile's 128 columns: pair j = keys 8j + 2c, 8j + 2c + 1, c = thread % 4;
+// v[4j], v[4j + 1] row 0, v[4j + 2], v[4j + 3] row 1) from the raw scores, the scale in log2 units
+// and the rows' reference maxima; a pair's keys past e0 (e1) of row 0 (1), counted from key 2c, are
+// masked.  Writes the packed words of those pairs in the 16x128b layout (hi[2i] row 0, hi[2i + 1]
+// row 1 for pair j0 + i; for bf16 also lo) and adds the rows' sums of the unrounded weights to s0, s1.
 template <typename T, bool kMasked>
-__device__ __forceinline__ float make_p(const float* v, float sl2, float m_ref, int lim, uint32_t* hi,
-                                        uint32_t* lo) {
-  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-  const float2 s2 = make_float2(sl2, sl2), nm2 = make_float2(-m_ref, -m_ref);
+__device__ __forceinline__ void make_p(const float* v, int j0, float sl2, float mr0, float mr1, int e0, int e1,
+                                       uint32_t* hi, uint32_t* lo, float& s0, float& s1) {
+  float2 acc0[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  float2 acc1[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  const float2 sc2 = make_float2(sl2, sl2), n0 = make_float2(-mr0, -mr0), n1 = make_float2(-mr1, -mr1);
 #pragma unroll
-  for (int i = 0; i < 64; i += 2) {
-    const float2 x = fma2(make_float2(v[i], v[i + 1]), s2, nm2);
-    float e0 = fast_exp2(x.x), e1 = fast_exp2(x.y);
+  for (int j = j0; j < j0 + 8; ++j) {
+    const float2 x = fma2(make_float2(v[4 * j], v[4 * j + 1]), sc2, n0);
+    const float2 y = fma2(make_float2(v[4 * j + 2], v[4 * j + 3]), sc2, n1);
+    float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y), p2 = fast_exp2(y.x), p3 = fast_exp2(y.y);
     if (kMasked) {
-      e0 = i <= lim ? e0 : 0.f;
-      e1 = i + 1 <= lim ? e1 : 0.f;
+      p0 = 8 * j <= e0 ? p0 : 0.f;
+      p1 = 8 * j + 1 <= e0 ? p1 : 0.f;
+      p2 = 8 * j <= e1 ? p2 : 0.f;
+      p3 = 8 * j + 1 <= e1 ? p3 : 0.f;
     }
-    acc[(i >> 1) & 3] = add2(acc[(i >> 1) & 3], make_float2(e0, e1));
+    acc0[j & 1] = add2(acc0[j & 1], make_float2(p0, p1));
+    acc1[j & 1] = add2(acc1[j & 1], make_float2(p2, p3));
     if constexpr (split_p<T>()) {
-      // hi = e truncated to bf16 (exact as a float), lo = the remainder rounded to bf16
-      const uint32_t b0 = __float_as_uint(e0), b1 = __float_as_uint(e1);
-      hi[i / 2] = __byte_perm(b0, b1, 0x7632);
-      const float2 r = sub2(make_float2(e0, e1), make_float2(__uint_as_float(b0 & 0xffff0000u),
-                                                            __uint_as_float(b1 & 0xffff0000u)));
-      lo[i / 2] = Mma<T>::pack(r.x, r.y);
+      // hi = p truncated to bf16 (exact as a float), lo = the remainder rounded to bf16
+      const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+      const uint32_t b2 = __float_as_uint(p2), b3 = __float_as_uint(p3);
+      hi[2 * (j - j0)] = __byte_perm(b0, b1, 0x7632);
+      hi[2 * (j - j0) + 1] = __byte_perm(b2, b3, 0x7632);
+      const float2 r0 = sub2(make_float2(p0, p1), make_float2(__uint_as_float(b0 & 0xffff0000u),
+                                                              __uint_as_float(b1 & 0xffff0000u)));
+      const float2 r1 = sub2(make_float2(p2, p3), make_float2(__uint_as_float(b2 & 0xffff0000u),
+                                                              __uint_as_float(b3 & 0xffff0000u)));
+      lo[2 * (j - j0)] = Mma<T>::pack(r0.x, r0.y);
+      lo[2 * (j - j0) + 1] = Mma<T>::pack(r1.x, r1.y);
     } else {
-      hi[i / 2] = Mma<T>::pack(e0, e1);
+      hi[2 * (j - j0)] = Mma<T>::pack(p0, p1);
+      hi[2 * (j - j0) + 1] = Mma<T>::pack(p2, p3);
     }
   }
-  const float2 t = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
-  return t.x + t.y;
+  const float2 t0 = add2(acc0[0], acc0[1]), t1 = add2(acc1[0], acc1[1]);
+  s0 += t0.x + t0.y;
+  s1 += t1.x + t1.y;
 }
 
 }  // namespace
@@ -313,8 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_done = bar_q + 11; // every P V done
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 112);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 120);
-  float* xmax = reinterpret_cast<float*>(smem + kBarOff + 128);  // [2 tiles][2 groups][128] row maxima
-  float* xsum = xmax + 2 * 2 * kTile;                             // [2 groups][128] row sums
+  float* xsum = reinterpret_cast<float*>(smem + kBarOff + 128);  // [128] row sums, exchanged once at the end
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int n_s = 0, n_o = 0;  // S / P V commits (control thread)
   int n_issued = 0;      // tiles whose copies this producer warp has issued
@@ -445,13 +495,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         const uint32_t vb = smem_u32(smem + kVOff + buf * 2 * kHalf);
-        // keys 64g + 16kk' of the tile: P hi (lo) of group g in columns 64g (+ 32) + 8kk' of the buffer
+        // keys 16kk .. 16kk + 15 of the tile: P hi (lo) in columns 8kk (64 + 8kk) of the buffer
 #pragma unroll
         for (int part = 0; part < (split_p<T>() ? 2 : 1); ++part) {
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tmem + kOCol, tmem + buf * 128 + 64 * (kk >> 2) + part * 32 + (kk & 3) * 8,
-                   sw128_desc(vb + kk * 2048, kHalf, 1024), id_o, kt > 0 || part > 0 || kk > 0);
+            mma_ts(tmem + kOCol, tmem + buf * 128 + part * 64 + kk * 8, sw128_desc(vb + kk * 2048, kHalf, 1024), id_o,
+                   kt > 0 || part > 0 || kk > 0);
         }
         mma_commit(&bar_o[buf]);
         ++n_o;
@@ -463,12 +513,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // =================================================================== softmax warps
-    const int g = warp >> 2;                         // key columns 64g .. 64g + 63 of every tile
-    const int row = (warp & 3) * 32 + lane;          // query row = tensor-memory lane
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t o_addr = tmem + lane_base + kOCol + 64 * g;  // this group's 64 columns of O
-    if (g == 0) {
+    // Warp w owns the 16 query rows (tensor-memory lanes) 32 (w % 4) + 16 (w / 4) .. + 15 of the tile,
+    // all 128 key columns: thread t holds rows r0 = base + t / 4 and r1 = r0 + 8, keys 8j + 2 (t % 4)
+    // and + 1 (j = 0..15), so a row's maximum and sum take two shuffles among its four threads.
+    const int q4 = warp & 3, hh = warp >> 2, c4 = lane & 3;
+    const uint32_t half_base = (uint32_t)(q4 * 32 + hh * 16) << 16;  // first lane of this warp's rows
+    const int r0 = q4 * 32 + hh * 16 + (lane >> 2), r1 = r0 + 8;
+    if (hh == 0) {
       // Q row -> tensor memory columns kQCol.. (two elements per column, lower index in the low half)
+      const int row = q4 * 32 + lane;
+      const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
       uint32_t qw[64];
       if (row < rows) {
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
@@ -490,76 +544,108 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar_q);
     }
     const float sl2 = p.scale_log2;
-    const int lim_base = min(pos0 + row, L - 1);     // last key position this row sees
-    float m_ref = -INFINITY, l_run = 0.f;
+    const int lim0 = min(pos0 + r0, L - 1), lim1 = min(pos0 + r1, L - 1);  // last key position each row sees
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // reference maxima (log2 units), partial sums
     bool ok = true;
-    // Every softmax warp runs all key_tiles iterations and passes the named barrier of each: after a
-    // failure the waits return at once (the abort flag is set) and the arithmetic is just discarded,
-    // so no warp can be left waiting on a barrier that another warp has stopped visiting.
+    // Every softmax warp runs all key_tiles iterations: after a failure the waits return at once (the
+    // abort flag is set) and the arithmetic is just discarded.
     for (int kt = 0; kt < key_tiles; ++kt) {
       const int buf = kt & 1;
       ok = __all_sync(0xffffffffu, wait_bar_spin(&bar_s[buf], (kt >> 1) & 1, abort_flag)) && ok;
       tc_fence_after();
-      const uint32_t s_addr = tmem + lane_base + buf * 128 + 64 * g;
+      const uint32_t s_addr = tmem + half_base + buf * 128;
       float v[64];
-      tmem_ld32(s_addr, v);
-      tmem_ld32(s_addr + 32, v + 32);
+      tmem_ld16x256_x8(s_addr, v);
+      tmem_ld16x256_x8(s_addr + 64, v + 32);
       tmem_wait_ld<64>(v);
-      const int lim = lim_base - (kt * kTile + 64 * g);  // keys 0..lim of these 64 are visible
-      const bool unmasked = __all_sync(0xffffffffu, lim >= 63);
-      // ---- the tile's row max over both groups, and the reference max it implies
-      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
+      const int key0 = kt * kTile + 2 * c4;      // key of this thread's pair 0
+      const int e0 = lim0 - key0, e1 = lim1 - key0;  // pair j's keys 8j, 8j + 1 are visible up to e
+      const bool unmasked = __all_sync(0xffffffffu, min(lim0, lim1) >= kt * kTile + kTile - 1);
+      // ---- the rows' tile maxima, and the reference maxima they imply
+      float a0 = -INFINITY, b0 = -INFINITY, a1 = -INFINITY, b1 = -INFINITY;  // two chains per row
       if (unmasked) {
 #pragma unroll
-        for (int i = 0; i < 64; i += 2) mq[(i >> 1) & 3] = max3(mq[(i >> 1) & 3], v[i], v[i + 1]);
+        for (int j = 0; j < 16; j += 2) {
+          a0 = max3(a0, v[4 * j], v[4 * j + 1]);
+          a1 = max3(a1, v[4 * j + 2], v[4 * j + 3]);
+          b0 = max3(b0, v[4 * j + 4], v[4 * j + 5]);
+          b1 = max3(b1, v[4 * j + 6], v[4 * j + 7]);
+        }
       } else {
 #pragma unroll
-        for (int i = 0; i < 64; i += 2)
-          mq[(i >> 1) & 3] = max3(mq[(i >> 1) & 3], i <= lim ? v[i] : -INFINITY, i + 1 <= lim ? v[i + 1] : -INFINITY);
+        for (int j = 0; j < 16; ++j) {
+          a0 = max3(a0, 8 * j <= e0 ? v[4 * j] : -INFINITY, 8 * j + 1 <= e0 ? v[4 * j + 1] : -INFINITY);
+          a1 = max3(a1, 8 * j <= e1 ? v[4 * j + 2] : -INFINITY, 8 * j + 1 <= e1 ? v[4 * j + 3] : -INFINITY);
+        }
       }
-      float* xm = xmax + buf * 2 * kTile;  // two buffers: tile kt + 2 writes after tile kt + 1's exchange
-      xm[g * kTile + row] = fmaxf(max3(mq[0], mq[1], mq[2]), mq[3]);
-      asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxWarps * 32) : "memory");
-      const float mx_s = fmaxf(xm[row], xm[kTile + row]) * sl2;  // scale > 0; the same in both groups
-      const bool upd = mx_s > m_ref + kRescaleThreshold;
-      const float alpha = upd ? fast_exp2(m_ref - mx_s) : 1.f;
-      if (__any_sync(0xffffffffu, upd) && kt > 0 && ok) {
-        // O of these rows (this group's columns) is rescaled between P V of tile kt - 1 and that of
-        // tile kt.  The barrier of its V stage finished tile kt - 3 before S(kt - 1) was issued and its
-        // next phase (tile kt + 1) needs this warp's P, so the parity wait below is exact.
+      a0 = fmaxf(a0, b0);
+      a1 = fmaxf(a1, b1);
+      a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, 1));
+      a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
+      a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, 2));
+      a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 2));
+      const float mx0 = a0 * sl2, mx1 = a1 * sl2;  // scale > 0
+      const bool upd0 = mx0 > m0 + kRescaleThreshold, upd1 = mx1 > m1 + kRescaleThreshold;
+      const float al0 = upd0 ? fast_exp2(m0 - mx0) : 1.f, al1 = upd1 ? fast_exp2(m1 - mx1) : 1.f;
+      if (__any_sync(0xffffffffu, upd0 || upd1) && kt > 0 && ok) {
+        // O of these rows is rescaled between P V of tile kt - 1 and that of tile kt.  The barrier of
+        // its V stage finished tile kt - 3 before S(kt - 1) was issued and its next phase (tile kt + 1)
+        // needs this warp's P, so the parity wait below is exact.
         ok = warp_wait(&bar_o[(kt - 1) & 1], ((kt - 1) >> 1) & 1);
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
           float o[32];
-          tmem_ld32(o_addr + c * 32, o);
+          tmem_ld16x256_x8(tmem + half_base + kOCol + 64 * c, o);
           tmem_wait_ld<32>(o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32(o_addr + c * 32, reinterpret_cast<const uint32_t*>(o));
+          for (int i = 0; i < 32; i += 4) {
+            o[i] *= al0, o[i + 1] *= al0;
+            o[i + 2] *= al1, o[i + 3] *= al1;
+          }
+          tmem_st16x256_x8(tmem + half_base + kOCol + 64 * c, reinterpret_cast<const uint32_t*>(o));
         }
         tmem_wait_st();
       }
-      if (upd) m_ref = mx_s;
-      // ---- P into the S columns it came from
-      uint32_t hi[32], lo[32];
-      const float lsum = unmasked ? make_p<T, false>(v, sl2, m_ref, lim, hi, lo)
-                                  : make_p<T, true>(v, sl2, m_ref, lim, hi, lo);
-      l_run = l_run * alpha + lsum;
-      tmem_st32(s_addr, hi);
-      if constexpr (split_p<T>()) tmem_st32(s_addr + 32, lo);
+      if (upd0) m0 = mx0;
+      if (upd1) m1 = mx1;
+      // ---- P into the buffer, 8 pairs (32 columns of packed words) at a time: hi words in columns
+      //      0..63, lo words in 64..127
+      l0 *= al0;
+      l1 *= al1;
+#pragma unroll
+      for (int j0 = 0; j0 < 16; j0 += 8) {
+        uint32_t hi[16], lo[16];
+        if (unmasked)
+          make_p<T, false>(v, j0, sl2, m0, m1, e0, e1, hi, lo, l0, l1);
+        else
+          make_p<T, true>(v, j0, sl2, m0, m1, e0, e1, hi, lo, l0, l1);
+        tmem_st16x128_x8(s_addr + 4 * j0, hi);
+        if constexpr (split_p<T>()) tmem_st16x128_x8(s_addr + 64 + 4 * j0, lo);
+      }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_p[buf]);
     }
-    // ---- epilogue: out = O / (l0 + l1), this group's 64 columns
+    // ---- row sums over each row's four threads, then to shared memory for the epilogue's layout
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    if (c4 == 0) {
+      xsum[r0] = l0;
+      xsum[r1] = l1;
+    }
+    const int g = hh;                                // epilogue: columns 64g .. 64g + 63 of O
+    const int row = q4 * 32 + lane;                  // query row = tensor-memory lane (32x32b shape)
+    const uint32_t o_addr = tmem + ((uint32_t)(q4 * 32) << 16) + kOCol + 64 * g;
+    // ---- epilogue: out = O / l, this warp's 64 columns of its quarter's 32 rows
     if (ok) ok = warp_wait(bar_done, 0);
-    xsum[g * kTile + row] = l_run;
     asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxWarps * 32) : "memory");
     if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
       tc_fence_after();
-      const float den = xsum[row] + xsum[kTile + row];
+      const float den = xsum[row];
       const float inv = den > 0.f ? 1.f / den : 0.f;
       T* out = reinterpret_cast<T*>(p.out) + ((size_t)(q0 + tile0 + row) * p.num_q_heads + h) * kD + 64 * g;
 #pragma unroll 1
