@@ -33,7 +33,8 @@ int pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cach
   if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 16))
     return PA_ERR_MISALIGNED;
   const long long q_tiles = (max_query_len + 127) / 128;
-  if ((long long)num_seqs * num_q_heads * q_tiles > kInt32Max) return PA_ERR_TOO_LARGE;
+  // work items (sequence, head, query tile) are counted in int32, with room for one grid stride past the end
+  if ((long long)num_seqs * num_q_heads * q_tiles > kInt32Max - 4096) return PA_ERR_TOO_LARGE;
   if ((long long)max_blocks_per_seq * cache->block_size > kInt32Max) return PA_ERR_TOO_LARGE;
   if ((long long)num_query_tokens * num_q_heads * 128 > ((long long)1 << 40)) return PA_ERR_TOO_LARGE;
 

@@ -323,48 +323,68 @@ __device__ __forceinline__ void make_p(const float* v, int j0, float sl2, float 
 
 }  // namespace
 
+// One work item: query tile qt of (sequence s, query head h).
+struct PfItem {
+  int s, h, hkv, q0, n, L, tile0, rows, pos0, key_tiles, nblocks_seq;
+};
+
+// The idx-th work item in schedule order: the last query tile of every (sequence, head) first (it
+// sees the most keys), then the next-to-last ones, and so on, so that a CTA taking every
+// gridDim.x-th item gets a mix of long and short ones.  False when the item has no queries, or when
+// its sequence's chunk is inconsistent (reported once per sequence, by the item of its first tile
+// and head, when `report`).
+__device__ __forceinline__ bool pf_item(const PrefillParams& p, int idx, PfItem& it, bool report) {
+  const int per_level = p.num_seqs * p.num_q_heads;
+  const int qt = p.q_tiles - 1 - idx / per_level;
+  const int rem = idx % per_level;
+  it.s = rem / p.num_q_heads;
+  it.h = rem % p.num_q_heads;
+  it.q0 = __ldg(p.query_start + it.s);
+  it.n = __ldg(p.query_start + it.s + 1) - it.q0;
+  it.L = __ldg(p.seq_lens + it.s);
+  const int B = p.block_size;
+  // a chunk must lie inside q / out, fit the tiles, and be part of its sequence's cached tokens
+  if (it.q0 < 0 || it.n < 0 || (long long)it.q0 + it.n > p.num_query_tokens || it.n > p.q_tiles * kTile ||
+      it.L < it.n || (long long)it.L > (long long)p.max_blocks * B) {
+    if (report && qt == 0 && it.h == 0) report_error(p.err_flag, PA_DEVERR_QUERY);
+    return false;
+  }
+  it.tile0 = qt * kTile;
+  if (it.tile0 >= it.n) return false;
+  it.hkv = it.h / (p.num_q_heads / p.num_kv_heads);
+  it.rows = min(kTile, it.n - it.tile0);               // valid query rows of this tile
+  it.pos0 = it.L - it.n + it.tile0;                    // position of query row 0
+  it.key_tiles = (it.pos0 + it.rows - 1) / kTile + 1;  // key tiles reaching the last row's position
+  it.nblocks_seq = (it.L + B - 1) / B;                 // <= max_blocks (checked above)
+  return true;
+}
+
+// Persistent: each CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ...  Every role walks the same
+// items; the K/V rings, the S buffers and their barriers run on across items (tg counts this CTA's
+// key tiles so far), so the next item's Q, K/V copies and first S MMAs overlap this item's last
+// P V and epilogue.
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                       const PrefillParams p) {
-  // ---- work item
-  const int tiles = p.q_tiles;
-  const int qt = tiles - 1 - (int)(blockIdx.x % tiles);  // the longest (last) query tiles start first
-  const int h = (blockIdx.x / tiles) % p.num_q_heads;
-  const int s = blockIdx.x / (tiles * p.num_q_heads);
-  const int q0 = __ldg(p.query_start + s);
-  const int n = __ldg(p.query_start + s + 1) - q0;
+  const int n_items = p.num_seqs * p.num_q_heads * p.q_tiles;
   const int B = p.block_size;
-  const int L = __ldg(p.seq_lens + s);
-  // a chunk must lie inside q / out, fit the grid, and be part of its sequence's cached tokens
-  if (q0 < 0 || n < 0 || (long long)q0 + n > p.num_query_tokens || n > tiles * kTile || L < n ||
-      (long long)L > (long long)p.max_blocks * B) {
-    if (threadIdx.x == 0 && qt == 0 && h == 0) report_error(p.err_flag, PA_DEVERR_QUERY);
-    return;
-  }
-  const int tile0 = qt * kTile;
-  if (tile0 >= n) return;
-  const int hkv = h / (p.num_q_heads / p.num_kv_heads);
-  const int rows = min(kTile, n - tile0);               // valid query rows of this tile
-  const int pos0 = L - n + tile0;                       // position of query row 0
-  const int key_tiles = (pos0 + rows - 1) / kTile + 1;  // key tiles reaching the last row's position
   const int blocks_per_tile = kTile / B;
-  const int slots = 2 * blocks_per_tile;                // tensor-map copies per tile: one per block and half
-  const int32_t* table = p.block_tables + (size_t)s * p.max_blocks;
-  const int nblocks_seq = (L + B - 1) / B;              // <= max_blocks (checked above)
+  const int slots = 2 * blocks_per_tile;  // tensor-map copies per tile: one per block and half
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bar_q = reinterpret_cast<uint64_t*>(smem + kBarOff);  // Q written into tensor memory
-  uint64_t* bar_k = bar_q + 1;     // [2] K stage filled
-  uint64_t* bar_v = bar_q + 3;     // [2] V stage filled
-  uint64_t* bar_s = bar_q + 5;     // [2] S buffer computed
-  uint64_t* bar_p = bar_q + 7;     // [2] P of the buffer written by all softmax warps
-  uint64_t* bar_o = bar_q + 9;     // [2] O += P V of the tile in V stage b done (one phase per tile held)
-  uint64_t* bar_done = bar_q + 11; // every P V done
+  uint64_t* bar_q = reinterpret_cast<uint64_t*>(smem + kBarOff);  // Q of the next item written into tensor memory
+  uint64_t* bar_k = bar_q + 1;      // [2] K stage filled
+  uint64_t* bar_v = bar_q + 3;      // [2] V stage filled
+  uint64_t* bar_s = bar_q + 5;      // [2] S buffer computed
+  uint64_t* bar_p = bar_q + 7;      // [2] P of the buffer written by all softmax warps
+  uint64_t* bar_o = bar_q + 9;      // [2] O += P V of the tile in V stage b done (one phase per tile held)
+  uint64_t* bar_done = bar_q + 11;  // every P V of the item done (one phase per item)
+  uint64_t* bar_ofree = bar_q + 12; // the item's epilogue has read O (one phase per item)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 112);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 120);
-  float* xsum = reinterpret_cast<float*>(smem + kBarOff + 128);  // [128] row sums, exchanged once at the end
+  float* xsum = reinterpret_cast<float*>(smem + kBarOff + 128);  // [2 items][128] row sums for the epilogue
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int n_s = 0, n_o = 0;  // S / P V commits (control thread)
   int n_issued = 0;      // tiles whose copies this producer warp has issued
@@ -379,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_o[b], 1);
     }
     mbar_init(bar_done, 1);
+    mbar_init(bar_ofree, kSoftmaxWarps);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -405,81 +426,100 @@ __global__ void __launch_bounds__(kThreads, 1)
     const CUtensorMap* tmap = is_v ? &tmap_v : &tmap_k;
     uint8_t* ring = smem + (is_v ? kVOff : kKOff);
     constexpr int kPastEnd = INT_MIN;
-    // lane b < blocks_per_tile copies this half of block b of every tile; its table entry is read one tile ahead
-    const int blk = lane;
-    auto fetch = [&](int kt) -> int {
-      const int bi = kt * blocks_per_tile + blk;
-      return (blk < blocks_per_tile && kt < key_tiles && bi < nblocks_seq) ? __ldg(table + bi) : kPastEnd;
-    };
+    const int blk = lane;  // lane b < blocks_per_tile copies this half of block b of every tile
     if (lane == 0) tma_prefetch_descriptor(tmap);
-    int entry_next = fetch(0);
-    for (int t = 0; t < key_tiles; ++t) {
-      // the stage of tile t held tile t - 2: wait until the MMA that read it has finished (the
-      // stage's barrier has one phase per tile held; its next phase needs this tile, so the wait is exact)
-      if (t >= 2 && !warp_wait(is_v ? &bar_o[t & 1] : &bar_s[t & 1], ((t - 2) >> 1) & 1)) break;
-      const int entry = entry_next;
-      entry_next = fetch(t + 1);
-      uint64_t* bar = is_v ? &bar_v[t & 1] : &bar_k[t & 1];
-      uint8_t* st = ring + (t & 1) * 2 * kHalf + half * kHalf;
-      const bool in_pool = entry >= 0 && entry < p.num_blocks;
-      if (!is_v && half == 0 && entry != kPastEnd && !in_pool) report_error(p.err_flag, PA_DEVERR_BLOCK_ID);
-      // V: only blocks entirely inside the sequence go by tensor-map copy
-      const bool whole = in_pool && (!is_v || (t * blocks_per_tile + blk + 1) * B <= L);
-      if (blk < blocks_per_tile) {
-        if (whole) {
-          mbar_arrive_expect_tx(bar, (uint32_t)B * 128);
-          tma_load_2d(st + blk * B * 128, tmap, half * 64, (entry * p.num_kv_heads + hkv) * B, bar);
-        } else {
-          mbar_arrive(bar);
+    bool ok = true;
+    int tg = 0;
+    for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+      PfItem it;
+      if (!pf_item(p, idx, it, false)) continue;
+      const int32_t* table = p.block_tables + (size_t)it.s * p.max_blocks;
+      // the table entry of this lane's block, read one tile ahead
+      auto fetch = [&](int kt) -> int {
+        const int bi = kt * blocks_per_tile + blk;
+        return (blk < blocks_per_tile && kt < it.key_tiles && bi < it.nblocks_seq) ? __ldg(table + bi) : kPastEnd;
+      };
+      int entry_next = fetch(0);
+      for (int t = 0; t < it.key_tiles; ++t, ++tg) {
+        // the stage of tile tg held tile tg - 2: wait until the MMA that read it has finished (the
+        // stage's barrier has one phase per tile held; its next phase needs this tile, so the wait is exact)
+        if (tg >= 2 && !warp_wait(is_v ? &bar_o[tg & 1] : &bar_s[tg & 1], ((tg - 2) >> 1) & 1)) {
+          ok = false;
+          break;
         }
-      }
-      if (is_v) {
-        // this half of the blocks not copied above: rows inside the sequence of an in-pool block by
-        // cp.async, the rest zeros.  Four rows of eight 16-byte chunks per step; the four rows lie in
-        // one block (B is a multiple of 16), so every branch below is uniform across the warp.
-        const unsigned partial = __ballot_sync(0xffffffffu, blk < blocks_per_tile && !whole);
-        if (partial) {
-          const int first = (__ffs(partial) - 1) * B;  // rows before the first such block are all copied
-          for (int r0 = first; r0 < kTile; r0 += 4) {
-            const int b = r0 / B;
-            const int e = __shfl_sync(0xffffffffu, entry, b);
-            if (!((partial >> b) & 1)) continue;
-            const int r = r0 + (lane >> 3), chunk = lane & 7;
-            const int pos = t * kTile + r;
-            uint8_t* dst = st + swz128(r, chunk);
-            if (pos < L && e >= 0 && e < p.num_blocks)
-              cp_async16(dst, cache + (((size_t)e * p.num_kv_heads + hkv) * B + (pos % B)) * kD + half * 64 +
-                                  chunk * 8);
-            else
-              *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        const int entry = entry_next;
+        entry_next = fetch(t + 1);
+        uint64_t* bar = is_v ? &bar_v[tg & 1] : &bar_k[tg & 1];
+        uint8_t* st = ring + (tg & 1) * 2 * kHalf + half * kHalf;
+        const bool in_pool = entry >= 0 && entry < p.num_blocks;
+        if (!is_v && half == 0 && entry != kPastEnd && !in_pool) report_error(p.err_flag, PA_DEVERR_BLOCK_ID);
+        // V: only blocks entirely inside the sequence go by tensor-map copy
+        const bool whole = in_pool && (!is_v || (t * blocks_per_tile + blk + 1) * B <= it.L);
+        if (blk < blocks_per_tile) {
+          if (whole) {
+            mbar_arrive_expect_tx(bar, (uint32_t)B * 128);
+            tma_load_2d(st + blk * B * 128, tmap, half * 64, (entry * p.num_kv_heads + it.hkv) * B, bar);
+          } else {
+            mbar_arrive(bar);
           }
-          cp_async_wait_all();
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor-core reads
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar);
+        if (is_v) {
+          // this half of the blocks not copied above: rows inside the sequence of an in-pool block by
+          // cp.async, the rest zeros.  Four rows of eight 16-byte chunks per step; the four rows lie in
+          // one block (B is a multiple of 16), so every branch below is uniform across the warp.
+          const unsigned partial = __ballot_sync(0xffffffffu, blk < blocks_per_tile && !whole);
+          if (partial) {
+            const int first = (__ffs(partial) - 1) * B;  // rows before the first such block are all copied
+            for (int r0 = first; r0 < kTile; r0 += 4) {
+              const int b = r0 / B;
+              const int e = __shfl_sync(0xffffffffu, entry, b);
+              if (!((partial >> b) & 1)) continue;
+              const int r = r0 + (lane >> 3), chunk = lane & 7;
+              const int pos = t * kTile + r;
+              uint8_t* dst = st + swz128(r, chunk);
+              if (pos < it.L && e >= 0 && e < p.num_blocks)
+                cp_async16(dst, cache + (((size_t)e * p.num_kv_heads + it.hkv) * B + (pos % B)) * kD + half * 64 +
+                                    chunk * 8);
+              else
+                *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+            }
+            cp_async_wait_all();
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor-core reads
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar);
+        }
+        ++n_issued;
       }
-      ++n_issued;
     }
   } else if (warp == kSWarp) {
     // =================================================================== S = Q K^T issuer
     if (lane == 0) {
       const uint32_t id_s = idesc<T>(0);
-      bool ok = wait_bar(bar_q, 0, abort_flag);
-      for (int t = 0; ok && t < key_tiles; ++t) {
-        // buffer t % 2 held P of tile t - 2 (its P V must have finished; the barrier's next phase,
-        // tile t, needs this S, so the wait is exact) and K stage t % 2 must hold key tile t
-        if (t >= 2) ok = wait_bar_spin(&bar_o[t & 1], ((t - 2) >> 1) & 1, abort_flag);
-        ok = ok && wait_bar_spin(&bar_k[t & 1], (t >> 1) & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t kb = smem_u32(smem + kKOff + (t & 1) * 2 * kHalf);
+      bool ok = true;
+      int tg = 0, item_no = 0;
+      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+        PfItem it;
+        if (!pf_item(p, idx, it, false)) continue;
+        // Q of this item in tensor memory (the barrier's next phase, the item after, is written only
+        // after this item's S MMAs have finished, so the wait is exact)
+        ok = wait_bar_spin(bar_q, item_no & 1, abort_flag);
+        for (int t = 0; ok && t < it.key_tiles; ++t, ++tg) {
+          // buffer tg % 2 held P of tile tg - 2 (its P V must have finished; the barrier's next phase,
+          // tile tg, needs this S, so the wait is exact) and K stage tg % 2 must hold key tile tg
+          if (tg >= 2) ok = wait_bar_spin(&bar_o[tg & 1], ((tg - 2) >> 1) & 1, abort_flag);
+          ok = ok && wait_bar_spin(&bar_k[tg & 1], (tg >> 1) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t kb = smem_u32(smem + kKOff + (tg & 1) * 2 * kHalf);
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ts(tmem + (t & 1) * 128, tmem + kQCol + kk * 8,
-                 sw128_desc(kb + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
-        mma_commit(&bar_s[t & 1]);
-        ++n_s;
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_ts(tmem + (tg & 1) * 128, tmem + kQCol + kk * 8,
+                   sw128_desc(kb + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
+          mma_commit(&bar_s[tg & 1]);
+          ++n_s;
+        }
+        ++item_no;
       }
     }
     __syncwarp();
@@ -488,27 +528,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t id_o = idesc<T>(1);
       bool ok = true;
-      for (int kt = 0; ok && kt < key_tiles; ++kt) {
-        const int buf = kt & 1;
-        // once every softmax warp has written P of tile kt and V of tile kt is in place
-        ok = wait_bar_spin(&bar_p[buf], (kt >> 1) & 1, abort_flag) && wait_bar_spin(&bar_v[buf], (kt >> 1) & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t vb = smem_u32(smem + kVOff + buf * 2 * kHalf);
-        // keys 16kk .. 16kk + 15 of the tile: P hi (lo) in columns 8kk (64 + 8kk) of the buffer
+      int tg = 0, item_no = 0;
+      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+        PfItem it;
+        if (!pf_item(p, idx, it, false)) continue;
+        // the first P V overwrites O: the previous item's epilogue must have read it (the barrier's
+        // next phase is this item's epilogue, which needs these MMAs, so the wait is exact)
+        if (item_no > 0) ok = wait_bar_spin(bar_ofree, (item_no - 1) & 1, abort_flag);
+        for (int kt = 0; ok && kt < it.key_tiles; ++kt, ++tg) {
+          const int buf = tg & 1;
+          // once every softmax warp has written P of tile tg and V of tile tg is in place
+          ok = wait_bar_spin(&bar_p[buf], (tg >> 1) & 1, abort_flag) &&
+               wait_bar_spin(&bar_v[buf], (tg >> 1) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t vb = smem_u32(smem + kVOff + buf * 2 * kHalf);
+          // keys 16kk .. 16kk + 15 of the tile: P hi (lo) in columns 8kk (64 + 8kk) of the buffer
 #pragma unroll
-        for (int part = 0; part < (split_p<T>() ? 2 : 1); ++part) {
+          for (int part = 0; part < (split_p<T>() ? 2 : 1); ++part) {
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tmem + kOCol, tmem + buf * 128 + part * 64 + kk * 8, sw128_desc(vb + kk * 2048, kHalf, 1024), id_o,
-                   kt > 0 || part > 0 || kk > 0);
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_ts(tmem + kOCol, tmem + buf * 128 + part * 64 + kk * 8, sw128_desc(vb + kk * 2048, kHalf, 1024),
+                     id_o, kt > 0 || part > 0 || kk > 0);
+          }
+          mma_commit(&bar_o[buf]);
+          ++n_o;
         }
-        mma_commit(&bar_o[buf]);
-        ++n_o;
+        // the item's last P V has finished: O is complete (the stage barrier's previous phase finished
+        // before the S that fed this P; its next phase needs a P V not yet issued, so the wait is exact)
+        if (ok) ok = wait_bar_spin(&bar_o[(tg - 1) & 1], ((tg - 1) >> 1) & 1, abort_flag);
+        if (ok) mbar_arrive(bar_done);
+        ++item_no;
       }
-      // the last P V on each stage barrier (earlier ones finished before the S that fed the later P)
-      for (int t = max(0, n_o - 2); ok && t < n_o; ++t) ok = wait_bar(&bar_o[t & 1], (t >> 1) & 1, abort_flag);
-      if (ok && n_o == key_tiles) mbar_arrive(bar_done);
     }
     __syncwarp();
   } else {
@@ -519,14 +570,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q4 = warp & 3, hh = warp >> 2, c4 = lane & 3;
     const uint32_t half_base = (uint32_t)(q4 * 32 + hh * 16) << 16;  // first lane of this warp's rows
     const int r0 = q4 * 32 + hh * 16 + (lane >> 2), r1 = r0 + 8;
-    if (hh == 0) {
-      // Q row -> tensor memory columns kQCol.. (two elements per column, lower index in the low half)
+    const float sl2 = p.scale_log2;
+    // Q rows of an item -> tensor memory columns kQCol.. (two elements per column, lower index in the
+    // low half); warps 0..3, one row per thread
+    auto write_q = [&](const PfItem& it) {
       const int row = q4 * 32 + lane;
       const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
       uint32_t qw[64];
-      if (row < rows) {
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
-                                                          ((size_t)(q0 + tile0 + row) * p.num_q_heads + h) * kD);
+      if (row < it.rows) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            static_cast<const T*>(p.q) + ((size_t)(it.q0 + it.tile0 + row) * p.num_q_heads + it.h) * kD);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const uint4 u = __ldg(src + i);
@@ -542,129 +595,155 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_q);
-    }
-    const float sl2 = p.scale_log2;
-    const int lim0 = min(pos0 + r0, L - 1), lim1 = min(pos0 + r1, L - 1);  // last key position each row sees
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // reference maxima (log2 units), partial sums
+    };
+    // the first item with queries at or after index idx (n_items when none); every item of this CTA
+    // passes through here exactly once, so thread 0 reports inconsistent chunks here
+    auto next_item = [&](int idx, PfItem& it) {
+      for (; idx < n_items; idx += gridDim.x)
+        if (pf_item(p, idx, it, threadIdx.x == 0)) return idx;
+      return n_items;
+    };
     bool ok = true;
-    // Every softmax warp runs all key_tiles iterations: after a failure the waits return at once (the
-    // abort flag is set) and the arithmetic is just discarded.
-    for (int kt = 0; kt < key_tiles; ++kt) {
-      const int buf = kt & 1;
-      ok = __all_sync(0xffffffffu, wait_bar_spin(&bar_s[buf], (kt >> 1) & 1, abort_flag)) && ok;
-      tc_fence_after();
-      const uint32_t s_addr = tmem + half_base + buf * 128;
-      float v[64];
-      tmem_ld16x256_x8(s_addr, v);
-      tmem_ld16x256_x8(s_addr + 64, v + 32);
-      tmem_wait_ld<64>(v);
-      const int key0 = kt * kTile + 2 * c4;      // key of this thread's pair 0
-      const int e0 = lim0 - key0, e1 = lim1 - key0;  // pair j's keys 8j, 8j + 1 are visible up to e
-      const bool unmasked = __all_sync(0xffffffffu, min(lim0, lim1) >= kt * kTile + kTile - 1);
-      // ---- the rows' tile maxima, and the reference maxima they imply
-      float a0 = -INFINITY, b0 = -INFINITY, a1 = -INFINITY, b1 = -INFINITY;  // two chains per row
-      if (unmasked) {
-#pragma unroll
-        for (int j = 0; j < 16; j += 2) {
-          a0 = max3(a0, v[4 * j], v[4 * j + 1]);
-          a1 = max3(a1, v[4 * j + 2], v[4 * j + 3]);
-          b0 = max3(b0, v[4 * j + 4], v[4 * j + 5]);
-          b1 = max3(b1, v[4 * j + 6], v[4 * j + 7]);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          a0 = max3(a0, 8 * j <= e0 ? v[4 * j] : -INFINITY, 8 * j + 1 <= e0 ? v[4 * j + 1] : -INFINITY);
-          a1 = max3(a1, 8 * j <= e1 ? v[4 * j + 2] : -INFINITY, 8 * j + 1 <= e1 ? v[4 * j + 3] : -INFINITY);
-        }
-      }
-      a0 = fmaxf(a0, b0);
-      a1 = fmaxf(a1, b1);
-      a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, 1));
-      a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
-      a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, 2));
-      a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 2));
-      const float mx0 = a0 * sl2, mx1 = a1 * sl2;  // scale > 0
-      const bool upd0 = mx0 > m0 + kRescaleThreshold, upd1 = mx1 > m1 + kRescaleThreshold;
-      const float al0 = upd0 ? fast_exp2(m0 - mx0) : 1.f, al1 = upd1 ? fast_exp2(m1 - mx1) : 1.f;
-      if (__any_sync(0xffffffffu, upd0 || upd1) && kt > 0 && ok) {
-        // O of these rows is rescaled between P V of tile kt - 1 and that of tile kt.  The barrier of
-        // its V stage finished tile kt - 3 before S(kt - 1) was issued and its next phase (tile kt + 1)
-        // needs this warp's P, so the parity wait below is exact.
-        ok = warp_wait(&bar_o[(kt - 1) & 1], ((kt - 1) >> 1) & 1);
+    int tg = 0, item_no = 0;
+    PfItem it;
+    int idx = next_item(blockIdx.x, it);
+    if (hh == 0 && idx < n_items) write_q(it);
+    // Every softmax warp walks every item and tile: after a failure the waits return at once (the
+    // abort flag is set) and the arithmetic is just discarded, so all of them pass the same named
+    // barriers.
+    while (idx < n_items) {
+      const int lim0 = min(it.pos0 + r0, it.L - 1), lim1 = min(it.pos0 + r1, it.L - 1);  // last key each row sees
+      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // reference maxima (log2 units), partial sums
+      for (int kt = 0; kt < it.key_tiles; ++kt, ++tg) {
+        const int buf = tg & 1;
+        ok = __all_sync(0xffffffffu, wait_bar_spin(&bar_s[buf], (tg >> 1) & 1, abort_flag)) && ok;
         tc_fence_after();
+        const uint32_t s_addr = tmem + half_base + buf * 128;
+        float v[64];
+        tmem_ld16x256_x8(s_addr, v);
+        tmem_ld16x256_x8(s_addr + 64, v + 32);
+        tmem_wait_ld<64>(v);
+        const int key0 = kt * kTile + 2 * c4;          // key of this thread's pair 0
+        const int e0 = lim0 - key0, e1 = lim1 - key0;  // pair j's keys 8j, 8j + 1 are visible up to e
+        const bool unmasked = __all_sync(0xffffffffu, min(lim0, lim1) >= kt * kTile + kTile - 1);
+        // ---- the rows' tile maxima, and the reference maxima they imply
+        float a0 = -INFINITY, b0 = -INFINITY, a1 = -INFINITY, b1 = -INFINITY;  // two chains per row
+        if (unmasked) {
+#pragma unroll
+          for (int j = 0; j < 16; j += 2) {
+            a0 = max3(a0, v[4 * j], v[4 * j + 1]);
+            a1 = max3(a1, v[4 * j + 2], v[4 * j + 3]);
+            b0 = max3(b0, v[4 * j + 4], v[4 * j + 5]);
+            b1 = max3(b1, v[4 * j + 6], v[4 * j + 7]);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            a0 = max3(a0, 8 * j <= e0 ? v[4 * j] : -INFINITY, 8 * j + 1 <= e0 ? v[4 * j + 1] : -INFINITY);
+            a1 = max3(a1, 8 * j <= e1 ? v[4 * j + 2] : -INFINITY, 8 * j + 1 <= e1 ? v[4 * j + 3] : -INFINITY);
+          }
+        }
+        a0 = fmaxf(a0, b0);
+        a1 = fmaxf(a1, b1);
+        a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, 1));
+        a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
+        a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, 2));
+        a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 2));
+        const float mx0 = a0 * sl2, mx1 = a1 * sl2;  // scale > 0
+        const bool upd0 = mx0 > m0 + kRescaleThreshold, upd1 = mx1 > m1 + kRescaleThreshold;
+        const float al0 = upd0 ? fast_exp2(m0 - mx0) : 1.f, al1 = upd1 ? fast_exp2(m1 - mx1) : 1.f;
+        if (__any_sync(0xffffffffu, upd0 || upd1) && kt > 0 && ok) {
+          // O of these rows is rescaled between P V of tile tg - 1 and that of tile tg.  The barrier
+          // of its V stage finished tile tg - 3 before S(tg - 1) was issued and its next phase (tile
+          // tg + 1) needs this warp's P, so the parity wait below is exact.
+          ok = warp_wait(&bar_o[(tg - 1) & 1], ((tg - 1) >> 1) & 1);
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {
+            float o[32];
+            tmem_ld16x256_x8(tmem + half_base + kOCol + 64 * c, o);
+            tmem_wait_ld<32>(o);
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              o[i] *= al0, o[i + 1] *= al0;
+              o[i + 2] *= al1, o[i + 3] *= al1;
+            }
+            tmem_st16x256_x8(tmem + half_base + kOCol + 64 * c, reinterpret_cast<const uint32_t*>(o));
+          }
+          tmem_wait_st();
+        }
+        if (upd0) m0 = mx0;
+        if (upd1) m1 = mx1;
+        // ---- P into the buffer, 8 pairs (32 columns of packed words) at a time: hi words in columns
+        //      0..63, lo words in 64..127
+        l0 *= al0;
+        l1 *= al1;
+#pragma unroll
+        for (int j0 = 0; j0 < 16; j0 += 8) {
+          uint32_t hi[16], lo[16];
+          if (unmasked)
+            make_p<T, false>(v, j0, sl2, m0, m1, e0, e1, hi, lo, l0, l1);
+          else
+            make_p<T, true>(v, j0, sl2, m0, m1, e0, e1, hi, lo, l0, l1);
+          tmem_st16x128_x8(s_addr + 4 * j0, hi);
+          if constexpr (split_p<T>()) tmem_st16x128_x8(s_addr + 64 + 4 * j0, lo);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_p[buf]);
+      }
+      // ---- the next item's Q: its S MMAs may run while this item's epilogue does (this item's S
+      //      MMAs, the only readers of Q, have all finished: the last bar_s wait above covered them)
+      PfItem nx;
+      const int idx_next = next_item(idx + gridDim.x, nx);
+      if (hh == 0 && idx_next < n_items) write_q(nx);
+      // ---- row sums over each row's four threads, then to shared memory for the epilogue's layout
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+      float* xs = xsum + (item_no & 1) * kTile;  // two buffers: item + 2 writes after item + 1's barrier
+      if (c4 == 0) {
+        xs[r0] = l0;
+        xs[r1] = l1;
+      }
+      // ---- epilogue: out = O / l, this warp's 64 columns of its quarter's 32 rows
+      const int g = hh;
+      const int row = q4 * 32 + lane;  // query row = tensor-memory lane (32x32b shape)
+      const uint32_t o_addr = tmem + ((uint32_t)(q4 * 32) << 16) + kOCol + 64 * g;
+      if (ok) ok = warp_wait(bar_done, item_no & 1);
+      asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxWarps * 32) : "memory");
+      if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
+        tc_fence_after();
+        const float den = xs[row];
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        T* out = reinterpret_cast<T*>(p.out) + ((size_t)(it.q0 + it.tile0 + row) * p.num_q_heads + it.h) * kD + 64 * g;
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
           float o[32];
-          tmem_ld16x256_x8(tmem + half_base + kOCol + 64 * c, o);
+          tmem_ld32(o_addr + 32 * c, o);
           tmem_wait_ld<32>(o);
+          if (row < it.rows) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            o[i] *= al0, o[i + 1] *= al0;
-            o[i + 2] *= al1, o[i + 3] *= al1;
+            for (int i = 0; i < 32; i += 8) {
+              uint4 val;
+              val.x = Mma<T>::pack(o[i] * inv, o[i + 1] * inv);
+              val.y = Mma<T>::pack(o[i + 2] * inv, o[i + 3] * inv);
+              val.z = Mma<T>::pack(o[i + 4] * inv, o[i + 5] * inv);
+              val.w = Mma<T>::pack(o[i + 6] * inv, o[i + 7] * inv);
+              *reinterpret_cast<uint4*>(out + 32 * c + i) = val;
+            }
           }
-          tmem_st16x256_x8(tmem + half_base + kOCol + 64 * c, reinterpret_cast<const uint32_t*>(o));
         }
-        tmem_wait_st();
       }
-      if (upd0) m0 = mx0;
-      if (upd1) m1 = mx1;
-      // ---- P into the buffer, 8 pairs (32 columns of packed words) at a time: hi words in columns
-      //      0..63, lo words in 64..127
-      l0 *= al0;
-      l1 *= al1;
-#pragma unroll
-      for (int j0 = 0; j0 < 16; j0 += 8) {
-        uint32_t hi[16], lo[16];
-        if (unmasked)
-          make_p<T, false>(v, j0, sl2, m0, m1, e0, e1, hi, lo, l0, l1);
-        else
-          make_p<T, true>(v, j0, sl2, m0, m1, e0, e1, hi, lo, l0, l1);
-        tmem_st16x128_x8(s_addr + 4 * j0, hi);
-        if constexpr (split_p<T>()) tmem_st16x128_x8(s_addr + 64 + 4 * j0, lo);
-      }
-      tmem_wait_st();
+      // O may take the next item's first P V
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_p[buf]);
-    }
-    // ---- row sums over each row's four threads, then to shared memory for the epilogue's layout
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    if (c4 == 0) {
-      xsum[r0] = l0;
-      xsum[r1] = l1;
-    }
-    const int g = hh;                                // epilogue: columns 64g .. 64g + 63 of O
-    const int row = q4 * 32 + lane;                  // query row = tensor-memory lane (32x32b shape)
-    const uint32_t o_addr = tmem + ((uint32_t)(q4 * 32) << 16) + kOCol + 64 * g;
-    // ---- epilogue: out = O / l, this warp's 64 columns of its quarter's 32 rows
-    if (ok) ok = warp_wait(bar_done, 0);
-    asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxWarps * 32) : "memory");
-    if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
-      tc_fence_after();
-      const float den = xsum[row];
-      const float inv = den > 0.f ? 1.f / den : 0.f;
-      T* out = reinterpret_cast<T*>(p.out) + ((size_t)(q0 + tile0 + row) * p.num_q_heads + h) * kD + 64 * g;
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        float o[32];
-        tmem_ld32(o_addr + 32 * c, o);
-        tmem_wait_ld<32>(o);
-        if (row < rows) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 val;
-            val.x = Mma<T>::pack(o[i] * inv, o[i + 1] * inv);
-            val.y = Mma<T>::pack(o[i + 2] * inv, o[i + 3] * inv);
-            val.z = Mma<T>::pack(o[i + 4] * inv, o[i + 5] * inv);
-            val.w = Mma<T>::pack(o[i + 6] * inv, o[i + 7] * inv);
-            *reinterpret_cast<uint4*>(out + 32 * c + i) = val;
-          }
-        }
-      }
+      if (lane == 0) mbar_arrive(bar_ofree);
+      ++item_no;
+      idx = idx_next;
+      it = nx;
     }
   }
   tc_fence_before();
@@ -687,21 +766,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512u) : "memory");
 }
 
+// one CTA per SM (the kernel holds all of tensor memory and most of shared memory), at most one per item
 cudaError_t launch_prefill_tc(int dtype, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                               cudaStream_t stream) {
-  const long long grid = (long long)p.num_seqs * p.num_q_heads * p.q_tiles;
-  if (grid == 0) return cudaSuccess;
+  const long long items = (long long)p.num_seqs * p.num_q_heads * p.q_tiles;
+  if (items == 0) return cudaSuccess;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)(items < sms ? items : sms);
   if (dtype == PA_F16) {
-    cudaError_t e =
-        cudaFuncSetAttribute(prefill_tc_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(prefill_tc_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<__half><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(tk, tv, p);
+    prefill_tc_kernel<__half><<<grid, kThreads, kSmemBytes, stream>>>(tk, tv, p);
   } else if (dtype == PA_BF16) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<__nv_bfloat16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(prefill_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<__nv_bfloat16><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(tk, tv, p);
+    prefill_tc_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, stream>>>(tk, tv, p);
   } else {
     return cudaErrorInvalidValue;
   }
