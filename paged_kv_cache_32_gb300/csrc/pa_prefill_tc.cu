@@ -69,8 +69,9 @@ constexpr int kD = 128;               // head size of this kernel
 constexpr int kHalf = kTile * 128;    // one 128-row x 128-byte swizzled region (16 KB)
 constexpr int kKOff = 0;              // K stages: 2 x 2 regions (dims 0-63, 64-127)
 constexpr int kVOff = 4 * kHalf;      // V stages: 2 x 2 regions
-constexpr int kBarOff = 8 * kHalf;    // barriers, flags, the row-max and row-sum exchange
-constexpr int kSmemBytes = kBarOff + 128 + 2 * 2 * kTile * 4 + 2 * kTile * 4 + 1024;
+constexpr int kQOff = 8 * kHalf;      // the next item's Q tile: 2 regions (dims 0-63, 64-127)
+constexpr int kBarOff = 10 * kHalf;   // barriers, flags, the published work items
+constexpr int kSmemBytes = kBarOff + 256 + 1024;
 constexpr uint32_t kOCol = 256;       // tensor-memory column of O
 constexpr uint32_t kQCol = 384;       // tensor-memory column of Q
 constexpr int kSoftmaxWarps = 8;
@@ -166,18 +167,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
-// 32 consecutive columns of this warp's 32 lanes; completes with tmem_wait_ld()
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
-  uint32_t* r = reinterpret_cast<uint32_t*>(v);
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // wait for outstanding tensor-memory loads, then tie each loaded register to the wait so that
@@ -366,7 +355,7 @@ __device__ __forceinline__ bool pf_item(const PrefillParams& p, int idx, PfItem&
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                      const PrefillParams p) {
+                      const __grid_constant__ CUtensorMap tmap_q, const PrefillParams p) {
   const int n_items = p.num_seqs * p.num_q_heads * p.q_tiles;
   const int B = p.block_size;
   const int blocks_per_tile = kTile / B;
@@ -382,9 +371,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_o = bar_q + 9;      // [2] O += P V of the tile in V stage b done (one phase per tile held)
   uint64_t* bar_done = bar_q + 11;  // every P V of the item done (one phase per item)
   uint64_t* bar_ofree = bar_q + 12; // the item's epilogue has read O (one phase per item)
+  uint64_t* bar_qs = bar_q + 13;    // an item published (and its Q tile in shared memory; one phase per item)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 112);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 120);
-  float* xsum = reinterpret_cast<float*>(smem + kBarOff + 128);  // [2 items][128] row sums for the epilogue
+  PfItem* items = reinterpret_cast<PfItem*>(smem + kBarOff + 128);  // [2] published items (s < 0: none left)
+  uint8_t* qbuf = smem + kQOff;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int n_s = 0, n_o = 0;  // S / P V commits (control thread)
   int n_issued = 0;      // tiles whose copies this producer warp has issued
@@ -400,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar_done, 1);
     mbar_init(bar_ofree, kSoftmaxWarps);
+    mbar_init(bar_qs, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -496,14 +488,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     // =================================================================== S = Q K^T issuer
     if (lane == 0) {
       const uint32_t id_s = idesc<T>(0);
+      tma_prefetch_descriptor(&tmap_q);
+      // This thread also schedules: it publishes item k (the first one with queries at or after index
+      // idx) in items[k % 2] and starts the copy of its Q tile into shared memory, both completing
+      // phase k of bar_qs; the softmax warps move the tile into tensor memory.  It reports
+      // inconsistent chunks: every item of this CTA passes through here once.
+      auto publish = [&](int idx, int k, PfItem& it) {
+        for (; idx < n_items; idx += gridDim.x)
+          if (pf_item(p, idx, it, true)) break;
+        if (idx >= n_items) it.s = -1;
+        items[k & 1] = it;
+        if (idx < n_items) {
+          mbar_arrive_expect_tx(bar_qs, 2 * kHalf);
+          tma_load_3d(qbuf, &tmap_q, 0, it.h, it.q0 + it.tile0, bar_qs);
+          tma_load_3d(qbuf + kHalf, &tmap_q, 64, it.h, it.q0 + it.tile0, bar_qs);
+        } else {
+          mbar_arrive(bar_qs);
+        }
+        return idx;
+      };
       bool ok = true;
       int tg = 0, item_no = 0;
-      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
-        PfItem it;
-        if (!pf_item(p, idx, it, false)) continue;
-        // Q of this item in tensor memory (the barrier's next phase, the item after, is written only
-        // after this item's S MMAs have finished, so the wait is exact)
+      PfItem it;
+      int idx = publish(blockIdx.x, 0, it);
+      while (ok && idx < n_items) {
+        // Q of this item in tensor memory, so the Q buffer may take the next one (the barrier's next
+        // phase, the item after, is written only after this item's S MMAs have finished: exact)
         ok = wait_bar_spin(bar_q, item_no & 1, abort_flag);
+        if (!ok) break;
+        PfItem nx;
+        const int idx_next = publish(idx + gridDim.x, item_no + 1, nx);
         for (int t = 0; ok && t < it.key_tiles; ++t, ++tg) {
           // buffer tg % 2 held P of tile tg - 2 (its P V must have finished; the barrier's next phase,
           // tile tg, needs this S, so the wait is exact) and K stage tg % 2 must hold key tile tg
@@ -520,6 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++n_s;
         }
         ++item_no;
+        idx = idx_next;
+        it = nx;
       }
     }
     __syncwarp();
@@ -571,23 +587,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t half_base = (uint32_t)(q4 * 32 + hh * 16) << 16;  // first lane of this warp's rows
     const int r0 = q4 * 32 + hh * 16 + (lane >> 2), r1 = r0 + 8;
     const float sl2 = p.scale_log2;
-    // Q rows of an item -> tensor memory columns kQCol.. (two elements per column, lower index in the
-    // low half); warps 0..3, one row per thread
-    auto write_q = [&](const PfItem& it) {
+    // the Q tile in shared memory (two 128-byte-swizzled halves) -> tensor memory columns kQCol.. (two
+    // elements per column, lower index in the low half); warps 0..3, one row per thread
+    auto copy_q = [&]() {
       const int row = q4 * 32 + lane;
       const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
       uint32_t qw[64];
-      if (row < it.rows) {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            static_cast<const T*>(p.q) + ((size_t)(it.q0 + it.tile0 + row) * p.num_q_heads + it.h) * kD);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint4 u = __ldg(src + i);
-          qw[4 * i] = u.x, qw[4 * i + 1] = u.y, qw[4 * i + 2] = u.z, qw[4 * i + 3] = u.w;
+      for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 u = *reinterpret_cast<const uint4*>(qbuf + hf * kHalf + swz128(row, c));
+          qw[32 * hf + 4 * c] = u.x, qw[32 * hf + 4 * c + 1] = u.y, qw[32 * hf + 4 * c + 2] = u.z,
+                         qw[32 * hf + 4 * c + 3] = u.w;
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) qw[i] = 0;
       }
       tmem_st32(tmem + lane_base + kQCol, qw);
       tmem_st32(tmem + lane_base + kQCol + 32, qw + 32);
@@ -596,22 +609,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_q);
     };
-    // the first item with queries at or after index idx (n_items when none); every item of this CTA
-    // passes through here exactly once, so thread 0 reports inconsistent chunks here
-    auto next_item = [&](int idx, PfItem& it) {
-      for (; idx < n_items; idx += gridDim.x)
-        if (pf_item(p, idx, it, threadIdx.x == 0)) return idx;
-      return n_items;
-    };
     bool ok = true;
     int tg = 0, item_no = 0;
-    PfItem it;
-    int idx = next_item(blockIdx.x, it);
-    if (hh == 0 && idx < n_items) write_q(it);
-    // Every softmax warp walks every item and tile: after a failure the waits return at once (the
-    // abort flag is set) and the arithmetic is just discarded, so all of them pass the same named
-    // barriers.
-    while (idx < n_items) {
+    // the first item and its Q
+    ok = warp_wait(bar_qs, 0);
+    PfItem it = items[0];
+    if (ok && it.s >= 0 && hh == 0) copy_q();
+    // After a failure (a wait gave up) every warp leaves at the next wait: no warp waits for another
+    // softmax warp, and the other roles stop at their next wait too.
+    while (ok && it.s >= 0) {
       const int lim0 = min(it.pos0 + r0, it.L - 1), lim1 = min(it.pos0 + r1, it.L - 1);  // last key each row sees
       float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // reference maxima (log2 units), partial sums
       for (int kt = 0; kt < it.key_tiles; ++kt, ++tg) {
@@ -693,56 +699,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_p[buf]);
       }
-      // ---- the next item's Q: its S MMAs may run while this item's epilogue does (this item's S
-      //      MMAs, the only readers of Q, have all finished: the last bar_s wait above covered them)
-      PfItem nx;
-      const int idx_next = next_item(idx + gridDim.x, nx);
-      if (hh == 0 && idx_next < n_items) write_q(nx);
-      // ---- row sums over each row's four threads, then to shared memory for the epilogue's layout
+      if (!ok) break;
+      // ---- the next item and its Q: its S MMAs may run while this item's epilogue does (this item's
+      //      S MMAs, the only readers of Q in tensor memory, have all finished: the last bar_s wait
+      //      above covered them)
+      ok = warp_wait(bar_qs, (item_no + 1) & 1);
+      const PfItem nx = items[(item_no + 1) & 1];
+      if (ok && nx.s >= 0 && hh == 0) copy_q();
+      // ---- row sums over each row's four threads
       l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
       l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
       l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
       l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-      float* xs = xsum + (item_no & 1) * kTile;  // two buffers: item + 2 writes after item + 1's barrier
-      if (c4 == 0) {
-        xs[r0] = l0;
-        xs[r1] = l1;
-      }
-      // ---- epilogue: out = O / l, this warp's 64 columns of its quarter's 32 rows
-      const int g = hh;
-      const int row = q4 * 32 + lane;  // query row = tensor-memory lane (32x32b shape)
-      const uint32_t o_addr = tmem + ((uint32_t)(q4 * 32) << 16) + kOCol + 64 * g;
+      // ---- epilogue: out = O / l for this warp's 16 rows, from the 16x256b layout (thread: rows r0, r1,
+      //      columns 8j + 2 (t % 4) and + 1)
       if (ok) ok = warp_wait(bar_done, item_no & 1);
-      asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxWarps * 32) : "memory");
-      if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
-        tc_fence_after();
-        const float den = xs[row];
-        const float inv = den > 0.f ? 1.f / den : 0.f;
-        T* out = reinterpret_cast<T*>(p.out) + ((size_t)(it.q0 + it.tile0 + row) * p.num_q_heads + it.h) * kD + 64 * g;
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          float o[32];
-          tmem_ld32(o_addr + 32 * c, o);
-          tmem_wait_ld<32>(o);
-          if (row < it.rows) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              uint4 val;
-              val.x = Mma<T>::pack(o[i] * inv, o[i + 1] * inv);
-              val.y = Mma<T>::pack(o[i + 2] * inv, o[i + 3] * inv);
-              val.z = Mma<T>::pack(o[i + 4] * inv, o[i + 5] * inv);
-              val.w = Mma<T>::pack(o[i + 6] * inv, o[i + 7] * inv);
-              *reinterpret_cast<uint4*>(out + 32 * c + i) = val;
-            }
-          }
-        }
-      }
+      if (!ok) break;
+      tc_fence_after();
+      float o[64];
+      tmem_ld16x256_x8(tmem + half_base + kOCol, o);
+      tmem_ld16x256_x8(tmem + half_base + kOCol + 64, o + 32);
+      tmem_wait_ld<64>(o);
       // O may take the next item's first P V
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ofree);
+      const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+      T* out0 = reinterpret_cast<T*>(p.out) + ((size_t)(it.q0 + it.tile0 + r0) * p.num_q_heads + it.h) * kD + 2 * c4;
+      T* out1 = out0 + (size_t)8 * p.num_q_heads * kD;  // row r1 = r0 + 8
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (r0 < it.rows)
+          *reinterpret_cast<uint32_t*>(out0 + 8 * j) = Mma<T>::pack(o[4 * j] * inv0, o[4 * j + 1] * inv0);
+        if (r1 < it.rows)
+          *reinterpret_cast<uint32_t*>(out1 + 8 * j) = Mma<T>::pack(o[4 * j + 2] * inv1, o[4 * j + 3] * inv1);
+      }
       ++item_no;
-      idx = idx_next;
       it = nx;
     }
   }
@@ -767,8 +759,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // one CTA per SM (the kernel holds all of tensor memory and most of shared memory), at most one per item
-cudaError_t launch_prefill_tc(int dtype, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
-                              cudaStream_t stream) {
+cudaError_t launch_prefill_tc(int dtype, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                              const PrefillParams& p, cudaStream_t stream) {
   const long long items = (long long)p.num_seqs * p.num_q_heads * p.q_tiles;
   if (items == 0) return cudaSuccess;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -780,12 +772,12 @@ cudaError_t launch_prefill_tc(int dtype, const CUtensorMap& tk, const CUtensorMa
   if (dtype == PA_F16) {
     e = cudaFuncSetAttribute(prefill_tc_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<__half><<<grid, kThreads, kSmemBytes, stream>>>(tk, tv, p);
+    prefill_tc_kernel<__half><<<grid, kThreads, kSmemBytes, stream>>>(tk, tv, tq, p);
   } else if (dtype == PA_BF16) {
     e = cudaFuncSetAttribute(prefill_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes);
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, stream>>>(tk, tv, p);
+    prefill_tc_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, stream>>>(tk, tv, tq, p);
   } else {
     return cudaErrorInvalidValue;
   }
