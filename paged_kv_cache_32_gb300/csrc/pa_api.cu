@@ -88,16 +88,16 @@ bool encode_cache_map(CUtensorMap* map, const void* base, const pa_cache_desc* c
   return r == CUDA_SUCCESS;
 }
 
-// FP8 keys as rows of D bytes (box 16 rows x 128 bytes, 128-byte swizzle); FP8 values need no map
+// FP8 keys as rows of D bytes (box `rows` rows x 128 bytes, 128-byte swizzle); FP8 values need no map
 // (every 16 tokens of one head are one contiguous run, read by 1-D bulk copies)
-bool encode_fp8_key_map(CUtensorMap* tk, const void* k_cache, const pa_cache_desc* c) {
+bool encode_fp8_key_map(CUtensorMap* tk, const void* k_cache, const pa_cache_desc* c, int rows) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   cuuint32_t estr[2] = {1, 1};
   const cuuint64_t heads = (cuuint64_t)c->num_blocks * c->num_kv_heads;
   cuuint64_t kdims[2] = {(cuuint64_t)c->head_size, heads * c->block_size};
   cuuint64_t kstrides[1] = {(cuuint64_t)c->head_size};
-  cuuint32_t kbox[2] = {(cuuint32_t)c->head_size, (cuuint32_t)pa::kTcSlabTokens};
+  cuuint32_t kbox[2] = {(cuuint32_t)c->head_size, (cuuint32_t)rows};
   CUresult r = enc(tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(k_cache), kdims, kstrides, kbox, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -218,9 +218,11 @@ int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_ca
     e = pa::launch_decode_f32(cache->head_size, static_cast<const float*>(k_cache),
                               static_cast<const float*>(v_cache), p, st);
   } else if (cache->dtype == PA_FP8_E4M3) {
-    CUtensorMap tk;
-    if (!encode_fp8_key_map(&tk, k_cache, cache)) return PA_ERR_CUDA;
-    e = pa::launch_decode_fp8(cache->head_size, tk, v_cache, p, k_scale, v_scale, st);
+    CUtensorMap tk, tk32;
+    if (!encode_fp8_key_map(&tk, k_cache, cache, pa::kTcSlabTokens) ||
+        !encode_fp8_key_map(&tk32, k_cache, cache, 2 * pa::kTcSlabTokens))
+      return PA_ERR_CUDA;
+    e = pa::launch_decode_fp8(cache->head_size, tk, tk32, v_cache, p, k_scale, v_scale, st);
   } else {
     CUtensorMap tk, tv;
     if (!encode_cache_map(&tk, k_cache, cache, pa::kTcSlabTokens) ||

@@ -22,7 +22,9 @@
 // sub-slabs, each inside one block, each one 2 KB tensor-map box of keys (16
 // rows x 128 bytes, 128-byte swizzle) and one 2 KB 1-D bulk copy of values
 // (D rows of 16 bytes; a tensor-map box of 128 rows x 16 bytes moves the same
-// bytes measurably slower);
+// bytes measurably slower).  When B is a multiple of 32 both sub-slabs lie in
+// one block, and a slab is one 32-row key box and one 4 KB run of values: two
+// copies instead of four, the same shared-memory image;
 // 32 tokens per slab halve the fixed per-slab work (barrier wait, block-table
 // shuffle, row-max shuffles) per byte against 16.  The output rescale is
 // skipped when no running max of the warp moved.  E4M3 values convert exactly to fp16 (cvt e4m3x2 -> f16x2), so
@@ -257,8 +259,9 @@ __device__ __forceinline__ void fp8_slab(const uint8_t* kst, const uint8_t* vst,
 
 template <int D, int NW, int NS>
 __global__ void __launch_bounds__(Fp8Shape<D, NW, NS>::THREADS)
-    decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k, const uint8_t* __restrict__ v_cache,
-                      const DecodeParams p, const float k_scale, const float v_scale) {
+    decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_k32,
+                      const uint8_t* __restrict__ v_cache, const DecodeParams p, const float k_scale,
+                      const float v_scale) {
   using S = Fp8Shape<D, NW, NS>;
   Fp8Item it;
   if (!fp8_item(p, blockIdx.x, it)) return;
@@ -284,6 +287,9 @@ __global__ void __launch_bounds__(Fp8Shape<D, NW, NS>::THREADS)
 
   const int n_my = it.nslabs > warp ? (it.nslabs - warp + NW - 1) / NW : 0;
   const int B = p.block_size;
+  // B a multiple of 32: a slab (32 tokens from a multiple of 32; partitions start on block boundaries)
+  // lies in one block, so one 32-row key box and one 4 KB value run fetch it
+  const bool whole_slabs = B % S::SB == 0;
   const int32_t* table = p.block_tables + (size_t)it.s * p.max_blocks;
   // first token of sub-slab u of this warp's k-th slab
   auto sub_tok = [&](int k, int u) { return it.j0 + (warp + k * NW) * S::SB + u * S::SUB; };
@@ -331,7 +337,15 @@ __global__ void __launch_bounds__(Fp8Shape<D, NW, NS>::THREADS)
     valid_mask = valid ? (valid_mask | (1u << stage)) : (valid_mask & ~(1u << stage));
     if (lane == 0) {
       uint64_t* bar = &bars[stage];
-      if (valid) {
+      if (valid && whole_slabs) {
+        // both sub-slabs in block pb0 (rows past the item inside that block are masked, or zeroed for values)
+        uint8_t* dst = ring + stage * S::SLAB_BYTES;
+        const int slot0 = sub_tok(k, 0) % B;
+        const int head_row = pb0 * p.num_kv_heads + it.hkv;
+        mbar_arrive_expect_tx(bar, S::NSUB * (S::KBOX + S::VBOX));
+        tma_load_2d(dst, &tmap_k32, 0, head_row * B + slot0, bar);
+        bulk_load_1d(dst + S::NSUB * S::KBOX, v_cache + (size_t)(head_row * B + slot0) * D, S::NSUB * S::VBOX, bar);
+      } else if (valid) {
         uint8_t* dst = ring + stage * S::SLAB_BYTES;
         mbar_arrive_expect_tx(bar, (has1 ? 2 : 1) * (S::KBOX + S::VBOX));
 #pragma unroll
@@ -470,8 +484,8 @@ __global__ void __launch_bounds__(128)
 
 }  // namespace
 
-cudaError_t launch_decode_fp8(int head_size, const CUtensorMap& tk, const void* v_cache, const DecodeParams& p,
-                              float k_scale, float v_scale, cudaStream_t stream) {
+cudaError_t launch_decode_fp8(int head_size, const CUtensorMap& tk, const CUtensorMap& tk32, const void* v_cache,
+                              const DecodeParams& p, float k_scale, float v_scale, cudaStream_t stream) {
   if (head_size != 128) return cudaErrorInvalidValue;
   using S = Fp8Shape<128, 4, 2>;
   auto kernel = decode_fp8_kernel<128, 4, 2>;
@@ -479,8 +493,8 @@ cudaError_t launch_decode_fp8(int head_size, const CUtensorMap& tk, const void* 
   if (e != cudaSuccess) return e;
   const long long items = (long long)p.num_seqs * p.num_kv_heads * p.head_groups * p.pmax;
   if (items == 0) return cudaSuccess;
-  kernel<<<(unsigned)items, S::THREADS, S::SMEM_BYTES, stream>>>(tk, static_cast<const uint8_t*>(v_cache), p,
-                                                                  k_scale, v_scale);
+  kernel<<<(unsigned)items, S::THREADS, S::SMEM_BYTES, stream>>>(tk, tk32, static_cast<const uint8_t*>(v_cache),
+                                                                  p, k_scale, v_scale);
   return cudaGetLastError();
 }
 

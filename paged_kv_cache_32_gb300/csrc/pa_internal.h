@@ -36,8 +36,9 @@ cudaError_t launch_decode_tc(int dtype, int head_size, int block_size, const CUt
                              const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_f32(int head_size, const float* k_cache, const float* v_cache, const DecodeParams& p,
                               cudaStream_t stream);
-cudaError_t launch_decode_fp8(int head_size, const CUtensorMap& tk, const void* v_cache, const DecodeParams& p,
-                              float k_scale, float v_scale, cudaStream_t stream);
+// tk: FP8 keys in 16-row boxes; tk32: the same in 32-row boxes (used when the block size is a multiple of 32)
+cudaError_t launch_decode_fp8(int head_size, const CUtensorMap& tk, const CUtensorMap& tk32, const void* v_cache,
+                              const DecodeParams& p, float k_scale, float v_scale, cudaStream_t stream);
 cudaError_t launch_merge(int dtype, int head_size, const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_reshape_and_cache_fp8(void* k_cache, void* v_cache, const void* key, const void* value,
                                          const int64_t* slot_mapping, int32_t num_tokens, int32_t num_blocks,
@@ -59,8 +60,8 @@ int check_cache(const pa_cache_desc* c);  // shape checks common to every call
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 // 2-D tensor map over a cache pool viewed as rows of head_size elements, box of `slab` rows x 64 columns
 bool encode_cache_map(CUtensorMap* map, const void* base, const pa_cache_desc* c, int slab);
-// FP8 keys: rows of D bytes (16-row boxes, 128-byte swizzle)
-bool encode_fp8_key_map(CUtensorMap* tk, const void* k_cache, const pa_cache_desc* c);
+// FP8 keys: rows of D bytes (boxes of `rows` rows, 128-byte swizzle)
+bool encode_fp8_key_map(CUtensorMap* tk, const void* k_cache, const pa_cache_desc* c, int rows);
 }  // namespace host
 
 // Slab (TMA box height in tokens) of the tensor-core decode: 16 tokens of one
