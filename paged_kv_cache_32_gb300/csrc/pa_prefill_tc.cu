@@ -363,7 +363,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bar_q = reinterpret_cast<uint64_t*>(smem + kBarOff);  // Q of the next item written into tensor memory
+  // Q of the item written into tensor memory, and every softmax warp past the item's publication (one phase
+  // per item: the next item is published only after this phase, so no softmax warp can find bar_qs two phases on)
+  uint64_t* bar_q = reinterpret_cast<uint64_t*>(smem + kBarOff);
   uint64_t* bar_k = bar_q + 1;      // [2] K stage filled
   uint64_t* bar_v = bar_q + 3;      // [2] V stage filled
   uint64_t* bar_s = bar_q + 5;      // [2] S buffer computed
@@ -381,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int n_issued = 0;      // tiles whose copies this producer warp has issued
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_q, 4);  // the four warps that write Q
+    mbar_init(bar_q, kSoftmaxWarps);  // warps 0..3 after writing Q, warps 4..7 after reading the item
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bar_k[b], slots);      // each copy slot arrives once per tile (with its bytes, or none)
       mbar_init(&bar_v[b], slots + 2);  // + each V producer's partial-block / zero-fill arrival
@@ -606,6 +608,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32(tmem + lane_base + kQCol + 32, qw + 32);
       tmem_wait_st();
       tc_fence_before();
+    };
+    // warps 0..3 move the published item's Q into tensor memory; every warp then arrives on bar_q
+    auto take_item = [&]() {
+      if (hh == 0) copy_q();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_q);
     };
@@ -614,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the first item and its Q
     ok = warp_wait(bar_qs, 0);
     PfItem it = items[0];
-    if (ok && it.s >= 0 && hh == 0) copy_q();
+    if (ok && it.s >= 0) take_item();
     // After a failure (a wait gave up) every warp leaves at the next wait: no warp waits for another
     // softmax warp, and the other roles stop at their next wait too.
     while (ok && it.s >= 0) {
@@ -705,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       //      above covered them)
       ok = warp_wait(bar_qs, (item_no + 1) & 1);
       const PfItem nx = items[(item_no + 1) & 1];
-      if (ok && nx.s >= 0 && hh == 0) copy_q();
+      if (ok && nx.s >= 0) take_item();
       // ---- row sums over each row's four threads
       l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
       l1 += __shfl_xor_sync(0xffffffffu, l1, 1);

@@ -139,16 +139,18 @@ def test_fp8_append_bad_slot_reported():
 
 
 # ---------------------------------------------------------------- decode, small cases
-@pytest.mark.parametrize("block_size", [16, 32, 64])
+@pytest.mark.parametrize("block_size", [16, 32, 48, 64, 128])
 @pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 2), (16, 2), (32, 2)])
 def test_fp8_decode_small(block_size, hq, hkv):
-    """Ragged lengths (1, 15, 16, 17, 100, 300, 777) across several slabs and partitions."""
+    """Ragged lengths (1, 15, 16, 17, 100, 300, 777) across several slabs and partitions.  B = 48
+    puts the two 16-token halves of some slabs in different blocks (two copies each); multiples
+    of 32 fetch a slab as one key box and one value run."""
     w = W.build_decode(f"fp8_b{block_size}_{hq}x{hkv}", seed=311 + block_size + hq, dtype="f16",
                        seq_lens=[1, 15, 16, 17, 100, 300, 777], num_q_heads=hq, num_kv_heads=hkv, head_size=128,
                        block_size=block_size, pool_factor=1.3)
     g = Fp8Step(w, 0.0123, 0.0117)
     k, v = g.host_after_append()
-    for part in (0, 64, 256):
+    for part in (0, 2 * block_size, 4 * block_size, 16 * block_size):  # explicit sizes are whole blocks
         got = g.decode(partition_size=part)
         assert int(g.err.item()) == 0
         err = assert_close(got, g.oracle(k, v), f"{w.name} partition {part}")

@@ -123,6 +123,26 @@ def test_prefill_small_mha():
     assert_close(got, oracle_prefill(w, k, v), "bf16", w.name)
 
 
+@pytest.mark.parametrize("dtype,block_size,hq,hkv", [("bf16", 16, 32, 8), ("f16", 64, 16, 4)])
+def test_prefill_many_items_per_cta(dtype, block_size, hq, hkv):
+    """More work items (sequence, head, query tile) than SMs, so each persistent CTA walks
+    several items and its K/V rings, S buffers, barrier phases and Q buffer run on across
+    item boundaries (items of 1 to 3 query tiles and 1 to 11 key tiles); every output and
+    both pools compared."""
+    w = W.build_prefill(f"prefill_multi_{dtype}", seed=41, dtype=dtype,
+                        prefix_lens=[0, 300, 17, 129, 500, 64, 0, 200, 31, 1000, 256, 90],
+                        chunk_lens=[300, 129, 256, 1, 77, 200, 130, 45, 260, 150, 128, 300], num_q_heads=hq,
+                        num_kv_heads=hkv, head_size=128, block_size=block_size)
+    g = PrefillStep(w)
+    got = g.run()
+    assert int(g.err.item()) == 0
+    k, v = host_pools(w)
+    assert np.array_equal(to_numpy_storage(g.k, dtype).view(np.uint8), k.view(np.uint8))
+    assert np.array_equal(to_numpy_storage(g.v, dtype).view(np.uint8), v.view(np.uint8))
+    err = assert_close(got, oracle_prefill(w, k, v), dtype, w.name)
+    print(w.name, "max abs err", err)
+
+
 def test_prefill_long_context_many_key_tiles():
     """One 200-token chunk after a 3000-token cached prefix: 25 key tiles, the
     online-softmax rescale of O in tensor memory runs many times."""
