@@ -10,14 +10,17 @@
 // 0..p: out = softmax_i(scale * q . k_i) v_i.  Keys and values of token i come
 // from offset i % B of block block_tables[s][i / B] (section "软件地址翻译").
 //
-// How (one CTA per sequence, query head and tile of 128 queries; 14 warps):
+// How (persistent: one CTA of 14 warps per SM walks work items = (sequence,
+// query head, tile of 128 queries); see pf_item for the order):
 //  * Tensor memory (512 columns): two S buffers (0..127, 128..255), the
 //    output accumulator O (256..383) and the query tile Q (384..447, two
-//    16-bit elements per column).  Q is written there once by the first four
-//    warps straight from global memory, so both MMAs take their A operand
-//    from tensor memory; only K and V stream through shared memory (an
-//    MMA with both operands in shared memory runs at about half rate at this
-//    shape, limited by the shared-memory read bandwidth).
+//    16-bit elements per column).  The next item's Q tile is copied into
+//    shared memory by a tensor-map copy while the current item runs; the
+//    first four warps move it into tensor memory once the current item's S
+//    MMAs have finished.  Both MMAs take their A operand from tensor memory
+//    and only K and V stream through shared memory (an MMA with both operands
+//    in shared memory runs at about half rate at this shape, limited by the
+//    shared-memory read bandwidth).
 //  * Data: key and value tiles of 128 tokens are gathered block by block
 //    through the block table by four producer warps (K and V, one warp per
 //    64-column half: a single thread issues a copy in about 200 cycles and
@@ -317,16 +320,17 @@ struct PfItem {
   int s, h, hkv, q0, n, L, tile0, rows, pos0, key_tiles, nblocks_seq;
 };
 
-// The idx-th work item in schedule order: the last query tile of every (sequence, head) first (it
-// sees the most keys), then the next-to-last ones, and so on, so that a CTA taking every
-// gridDim.x-th item gets a mix of long and short ones.  False when the item has no queries, or when
-// its sequence's chunk is inconsistent (reported once per sequence, by the item of its first tile
-// and head, when `report`).
+// The idx-th work item in schedule order: sequence by sequence; within a sequence its last query
+// tile (the one that sees the most keys) first, then the next-to-last, each over all query heads
+// (heads sharing a kv head side by side).  The CTAs at work at any time then share one sequence's
+// K/V, which stays in L2, and the schedule ends on short items.  False when the item has no queries,
+// or when its sequence's chunk is inconsistent (reported once per sequence, by the item of its first
+// tile and head, when `report`).
 __device__ __forceinline__ bool pf_item(const PrefillParams& p, int idx, PfItem& it, bool report) {
-  const int per_level = p.num_seqs * p.num_q_heads;
-  const int qt = p.q_tiles - 1 - idx / per_level;
-  const int rem = idx % per_level;
-  it.s = rem / p.num_q_heads;
+  const int per_seq = p.q_tiles * p.num_q_heads;
+  it.s = idx / per_seq;
+  const int rem = idx % per_seq;
+  const int qt = p.q_tiles - 1 - rem / p.num_q_heads;
   it.h = rem % p.num_q_heads;
   it.q0 = __ldg(p.query_start + it.s);
   it.n = __ldg(p.query_start + it.s + 1) - it.q0;
