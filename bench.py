@@ -51,6 +51,8 @@ WORKLOAD_DESC = {
                "lognormal(ln 1200, 0.6) lens in [64, 4096], pool 1.2x needed",
     "prefill_bf16": "chunked prefill bf16: 16 seqs, cached prefix U[0,2048] + chunk U[256,2048] tokens, 32 q / 8 kv "
                     "heads, D 128, B 16, pool 1.2x needed, shuffled; chunk K/V appended, then causal attention",
+    "prefill_f16": "chunked prefill fp16, the prefill_bf16 shapes: P enters the value MMA as one fp16 term "
+                   "(two bf16 terms for bf16)",
 }
 TORCH_DT = {"f32": "float32", "f16": "float16", "bf16": "bfloat16"}
 
@@ -519,6 +521,10 @@ def run_ours(args, world, rank, local):
     if not args.no_extra and world == 1 and args.prefill:
         line["prefill"] = bench_prefill(args.prefill, device, max(5, min(args.steps, 20)), args.warmup, peaks)
         torch.cuda.empty_cache()
+        for name in args.prefill_extra:
+            line.setdefault("prefill_other", {})[name] = bench_prefill(name, device, max(5, min(args.steps, 20)),
+                                                                        args.warmup, peaks)
+            torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
@@ -542,7 +548,7 @@ def bench_prefill(name: str, device, steps: int, warmup: int, peaks):
     att = statistics.mean(att_ms)
     flops = w.prefill_flops()
     tflops = flops / (att * 1e-3) / 1e12
-    peak = (peaks or {}).get("bf16_tflops")
+    peak = (peaks or {}).get("bf16_tflops")  # fp16 and bf16 share the dense tensor rate
     peak_src = "measured (burst)" if peak else "fallback"
     peak = peak or 1900.0
     T = w.num_query_tokens
@@ -609,6 +615,8 @@ def main():
                                                    "long_bf16_b64", "shared_prefix_f16", "mha_fp8", "gqa_fp8"])
     ap.add_argument("--no-extra", action="store_true", help="time only the headline workload")
     ap.add_argument("--prefill", default="prefill_bf16", help="chunked-prefill workload timed beside decode ('' = none)")
+    ap.add_argument("--prefill-extra", nargs="*", default=["prefill_f16"],
+                    help="further chunked-prefill workloads, reported under prefill_other")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--partition", type=int, default=None,
                     help="tokens per split-KV partition (multiple of the block size; 0 = library default)")

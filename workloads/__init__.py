@@ -475,6 +475,16 @@ def prefill_bf16(num_seqs: int = 16, materialize: bool = True, max_prefix: int =
                          num_kv_heads=8, head_size=128, block_size=16, materialize=materialize)
 
 
+def prefill_f16(num_seqs: int = 16, materialize: bool = True) -> Workload:
+    """The prefill_bf16 shapes (same prefix and chunk lengths) in fp16, where P enters the value
+    MMA as one fp16 term instead of two bf16 terms."""
+    rng = np.random.default_rng(1005)
+    prefix = rng.integers(0, 2048, size=num_seqs, endpoint=True)
+    chunk = rng.integers(256, 2048, size=num_seqs, endpoint=True)
+    return build_prefill("prefill_f16", seed=1008, dtype="f16", prefix_lens=prefix, chunk_lens=chunk, num_q_heads=32,
+                         num_kv_heads=8, head_size=128, block_size=16, materialize=materialize)
+
+
 WORKLOADS = {
     "tiny_f32": lambda materialize=True: tiny_f32(),
     "mha_f16": mha_f16,
@@ -484,6 +494,7 @@ WORKLOADS = {
     "long_bf16_b32": lambda materialize=True: long_bf16(32, materialize=materialize),
     "long_bf16_b64": lambda materialize=True: long_bf16(64, materialize=materialize),
     "prefill_bf16": prefill_bf16,
+    "prefill_f16": prefill_f16,
     "mha_fp8": mha_fp8,
     "gqa_fp8": gqa_fp8,
 }
