@@ -343,6 +343,90 @@ def time_device(ds, steps: int, warmup: int, world: int):
     return total_ms / steps, decode_ms, write_ms, (t0, t1)
 
 
+def time_calls(fn, steps: int, warmup: int) -> float:
+    """Mean device time in ms of fn(stream) over `steps` back-to-back calls, CUDA events on the
+    launching stream, after `warmup` untimed calls."""
+    import torch
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn(stream)
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn(stream)
+        e1.record(stream)
+        stream.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def bench_secondary(device, steps: int, warmup: int, peak: float):
+    """The secondary measurements: the cost of the block-table indirection (the MHA fp16 decode
+    with each sequence's blocks contiguous and in order, i.e. identity tables, against the
+    shuffled pool), a block-size sweep on the same sequences, and the two write calls at sizes
+    where bandwidth means something, plus their decode-step sizes.  Byte counts are algorithmic
+    (reads + writes for the writes, like the copy peak)."""
+    import torch
+    import paged_kv_cache_32_gb300 as pa
+    lens = np.random.default_rng(1001).integers(128, 2048, size=64, endpoint=True)  # the mha_f16 lengths
+    res = {}
+
+    def decode(name, block_size, shuffle, num_blocks=None):
+        w = W.build_decode(name, seed=1001, dtype="f16", seq_lens=lens, num_q_heads=32, num_kv_heads=32,
+                           head_size=128, block_size=block_size, num_blocks=num_blocks, shuffle=shuffle,
+                           materialize=False)
+        ds = DeviceStep(w, device)
+        ms = time_calls(ds.decode, steps, warmup)
+        err = int(ds.err.item())
+        gbs = ds.decode_bytes() / (ms * 1e-3) / 1e9
+        del ds
+        torch.cuda.empty_cache()
+        if err:
+            raise RuntimeError(f"device error flag {err} in {name}")
+        return {"decode_ms": round(ms, 5), "decode_gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+
+    shuffled = decode("tables_shuffled", 16, True, 8192)
+    identity = decode("tables_identity", 16, False, 8192)
+    res["block_tables"] = {"workload": "mha_f16 sequences, B 16, pool 8192", "shuffled": shuffled,
+                           "identity": identity,
+                           "shuffled_over_identity_time": round(shuffled["decode_ms"] / identity["decode_ms"], 4)}
+    res["block_size_sweep"] = {"workload": "mha_f16 sequences, shuffled pool 1.2x needed",
+                               **{f"B{b}": decode(f"sweep_b{b}", b, True) for b in (16, 32, 64, 128, 256)}}
+
+    # the write calls on an MHA fp16 pool (8192 blocks of 16 slots, 32 heads, D 128)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(1001)
+    nb, hkv, B, D = 8192, 32, 16, 128
+    k = torch.randn((nb, hkv, B, D), generator=gen, device=device, dtype=torch.float32).to(torch.float16)
+    v = torch.randn((nb, hkv, B, D), generator=gen, device=device, dtype=torch.float32).to(torch.float16)
+    desc = pa.cache_desc(k)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    perm = torch.randperm(nb * B, generator=gen, device=device)
+    writes = {}
+    for T in (64, 16384):  # a decode step's appends; a prefill chunk's worth
+        key = torch.randn((T, hkv, D), generator=gen, device=device, dtype=torch.float32).to(torch.float16)
+        val = torch.randn((T, hkv, D), generator=gen, device=device, dtype=torch.float32).to(torch.float16)
+        slots = perm[:T].contiguous()
+        ms = time_calls(lambda st: pa.pa_reshape_and_cache(k, v, key, val, slots, err_flag=err, stream=st, desc=desc),
+                        steps, warmup)
+        nbytes = T * 2 * hkv * D * 2 * 2 + T * 8  # K and V rows read and written, slots read
+        writes[f"reshape_and_cache_{T}_tokens"] = {"us": round(ms * 1e3, 2), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+    bperm = torch.randperm(nb, generator=gen, device=device).to(torch.int32)
+    for n in (128, 2048):  # the shared-prefix step's copies; a large copy-on-write burst
+        pairs = torch.stack([bperm[:n], bperm[n:2 * n]], dim=1).contiguous()
+        ms = time_calls(lambda st: pa.pa_copy_blocks(k, v, pairs, err_flag=err, stream=st, desc=desc), steps, warmup)
+        nbytes = n * 2 * hkv * B * D * 2 * 2 + n * 8  # both caches' blocks read and written, pairs read
+        writes[f"copy_blocks_{n}_pairs"] = {"us": round(ms * 1e3, 2), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+    torch.cuda.synchronize()
+    if int(err.item()):
+        raise RuntimeError(f"device error flag {int(err.item())} in the write calls")
+    res["writes"] = {"pool": "MHA fp16, 8192 blocks x 32 heads x 16 x 128", **writes}
+    del k, v
+    torch.cuda.empty_cache()
+    return res
+
+
 def time_e2e(ds: DeviceStep, steps: int, warmup: int, world: int):
     """Same step through the public API with the step's inputs copied from pinned
     host memory and the output copied back, inside the timed region."""
@@ -525,6 +609,8 @@ def run_ours(args, world, rank, local):
             line.setdefault("prefill_other", {})[name] = bench_prefill(name, device, max(5, min(args.steps, 20)),
                                                                         args.warmup, peaks)
             torch.cuda.empty_cache()
+    if not args.no_extra and world == 1 and not args.no_secondary:
+        line["secondary"] = bench_secondary(device, max(5, min(args.steps, 50)), args.warmup, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
@@ -618,6 +704,8 @@ def main():
     ap.add_argument("--prefill-extra", nargs="*", default=["prefill_f16"],
                     help="further chunked-prefill workloads, reported under prefill_other")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the block-table, block-size and write-call measurements")
     ap.add_argument("--partition", type=int, default=None,
                     help="tokens per split-KV partition (multiple of the block size; 0 = library default)")
     args = ap.parse_args()
