@@ -12,15 +12,14 @@
 //
 // How (persistent: one CTA of 14 warps per SM walks work items = (sequence,
 // query head, tile of 128 queries); see pf_item for the order):
-//  * Tensor memory (512 columns): two S buffers (0..127, 128..255), the
-//    output accumulator O (256..383) and the query tile Q (384..447, two
-//    16-bit elements per column).  The next item's Q tile is copied into
-//    shared memory by a tensor-map copy while the current item runs; the
-//    first four warps move it into tensor memory once the current item's S
-//    MMAs have finished.  Both MMAs take their A operand from tensor memory
-//    and only K and V stream through shared memory (an MMA with both operands
-//    in shared memory runs at about half rate at this shape, limited by the
-//    shared-memory read bandwidth).
+//  * Tensor memory (512 columns): three S buffers (0..127, 128..255,
+//    256..383) and the output accumulator O (384..511).  Q stays in shared
+//    memory: each item's Q tile is copied there by a tensor-map copy (two
+//    buffers, so the next item's copy overlaps the current item), and the S
+//    MMA reads both operands from shared memory (measured about as fast as
+//    with A in tensor memory, alongside the P V MMAs, the copies and the
+//    softmax's tensor-memory traffic).  Three S buffers let S of tile kt + 3
+//    wait for P V of tile kt instead of S of tile kt + 2.
 //  * Data: key and value tiles of 128 tokens are gathered block by block
 //    through the block table by four producer warps (K and V, one warp per
 //    64-column half: a single thread issues a copy in about 200 cycles and
@@ -35,9 +34,9 @@
 //  * Two threads in different warps issue the MMAs (kind::f16, fp32
 //    accumulation): warp 9 S = Q K^T (M = 128 queries, N = 128 keys, K = D),
 //    warp 8 O += P V (M = 128, N = D, K = 128 keys; P from tensor memory).
-//    S of tile kt + 2 goes into the buffer of tile kt once P V of tile kt has
+//    S of tile kt + 3 goes into the buffer of tile kt once P V of tile kt has
 //    finished; with separate issuers that wait never delays the next P V, and
-//    the softmax of tile kt + 1 overlaps P V of tile kt and S of tile kt + 2.
+//    the softmax of tile kt + 1 overlaps P V of tile kt and S of tile kt + 3.
 //  * Warps 0..7 run the softmax.  Each owns 16 query rows (tensor-memory
 //    lanes) and all 128 keys of a tile, read with the 16-lane 16x256b shape:
 //    a thread holds two rows, 32 keys of each, so a row's maximum and sum
@@ -49,8 +48,8 @@
 //  * Rescaling: a row's reference max moves only when the tile max exceeds it
 //    by more than 8 (log2 units), so P <= 2^8 and O is rescaled in place
 //    (tcgen05.ld / st of the warp's 16 rows) on few tiles.
-//  * Epilogue: the row sums go through shared memory once; out = O / l, two
-//    warps per lane quarter each writing 64 columns of its 32 rows.
+//  * Epilogue: each warp normalises its 16 rows (out = O / l) straight from
+//    the 16x256b layout, after releasing O to the next item's first P V.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -72,11 +71,11 @@ constexpr int kD = 128;               // head size of this kernel
 constexpr int kHalf = kTile * 128;    // one 128-row x 128-byte swizzled region (16 KB)
 constexpr int kKOff = 0;              // K stages: 2 x 2 regions (dims 0-63, 64-127)
 constexpr int kVOff = 4 * kHalf;      // V stages: 2 x 2 regions
-constexpr int kQOff = 8 * kHalf;      // the next item's Q tile: 2 regions (dims 0-63, 64-127)
-constexpr int kBarOff = 10 * kHalf;   // barriers, flags, the published work items
-constexpr int kSmemBytes = kBarOff + 256 + 1024;
-constexpr uint32_t kOCol = 256;       // tensor-memory column of O
-constexpr uint32_t kQCol = 384;       // tensor-memory column of Q
+constexpr int kQOff = 8 * kHalf;      // Q tiles of two items (item k in buffer k % 2): 2 x 2 regions
+constexpr int kBarOff = 12 * kHalf;   // barriers, flags, the published work items
+constexpr int kSmemBytes = kBarOff + 512 + 1024;
+constexpr int kSBufs = 3;             // S buffers in tensor memory (columns 128 b .. 128 b + 127)
+constexpr uint32_t kOCol = 384;       // tensor-memory column of O
 constexpr int kSoftmaxWarps = 8;
 constexpr int kPVWarp = kSoftmaxWarps;         // issues O += P V
 constexpr int kSWarp = kSoftmaxWarps + 1;      // issues S = Q K^T
@@ -165,6 +164,28 @@ __device__ __forceinline__ void mma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_
       : "memory");
 }
 
+// D (tensor memory) (+)= A (shared memory) x B (shared memory)
+__device__ __forceinline__ void mma_ss(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t id, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(id), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+// non-blocking: has the phase of the given parity completed?
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
@@ -181,16 +202,6 @@ __device__ __forceinline__ void tmem_wait_ld(float* v) {
   for (int i = 0; i < N; ++i) asm volatile("" : "+f"(v[i]));
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
-      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
-      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // The 16-lane shapes: a warp addresses one half (16 lanes) of its lane quarter.  Thread t holds
@@ -367,30 +378,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // Q of the item written into tensor memory, and every softmax warp past the item's publication (one phase
-  // per item: the next item is published only after this phase, so no softmax warp can find bar_qs two phases on)
+  // every softmax warp has read item k's publication (phase k; item k + 1 is published only after it, so
+  // no softmax warp can find bar_qs two phases on)
   uint64_t* bar_q = reinterpret_cast<uint64_t*>(smem + kBarOff);
   uint64_t* bar_k = bar_q + 1;      // [2] K stage filled
   uint64_t* bar_v = bar_q + 3;      // [2] V stage filled
-  uint64_t* bar_s = bar_q + 5;      // [2] S buffer computed
-  uint64_t* bar_p = bar_q + 7;      // [2] P of the buffer written by all softmax warps
-  uint64_t* bar_o = bar_q + 9;      // [2] O += P V of the tile in V stage b done (one phase per tile held)
-  uint64_t* bar_done = bar_q + 11;  // every P V of the item done (one phase per item)
-  uint64_t* bar_ofree = bar_q + 12; // the item's epilogue has read O (one phase per item)
-  uint64_t* bar_qs = bar_q + 13;    // an item published (and its Q tile in shared memory; one phase per item)
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 112);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 120);
-  PfItem* items = reinterpret_cast<PfItem*>(smem + kBarOff + 128);  // [2] published items (s < 0: none left)
+  uint64_t* bar_s = bar_q + 5;      // [3] S buffer computed (one phase per tile held)
+  uint64_t* bar_p = bar_q + 8;      // [3] P in the S buffer written by all softmax warps
+  uint64_t* bar_o = bar_q + 11;     // [3] O += P V of the tile in S buffer b done (one phase per tile held)
+  uint64_t* bar_done = bar_q + 14;  // every P V of the item done (one phase per item)
+  uint64_t* bar_ofree = bar_q + 15; // the item's epilogue has read O (one phase per item)
+  uint64_t* bar_qs = bar_q + 16;    // item k published and its Q tile in shared memory (phase k)
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 192);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 200);
+  PfItem* items = reinterpret_cast<PfItem*>(smem + kBarOff + 256);  // [2] published items (s < 0: none left)
   uint8_t* qbuf = smem + kQOff;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int n_s = 0, n_o = 0;  // S / P V commits (control thread)
   int n_issued = 0;      // tiles whose copies this producer warp has issued
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_q, kSoftmaxWarps);  // warps 0..3 after writing Q, warps 4..7 after reading the item
+    mbar_init(bar_q, kSoftmaxWarps);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bar_k[b], slots);      // each copy slot arrives once per tile (with its bytes, or none)
       mbar_init(&bar_v[b], slots + 2);  // + each V producer's partial-block / zero-fill arrival
+    }
+    for (int b = 0; b < kSBufs; ++b) {
       mbar_init(&bar_s[b], 1);
       mbar_init(&bar_p[b], kSoftmaxWarps);
       mbar_init(&bar_o[b], 1);
@@ -439,9 +452,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       int entry_next = fetch(0);
       for (int t = 0; t < it.key_tiles; ++t, ++tg) {
-        // the stage of tile tg held tile tg - 2: wait until the MMA that read it has finished (the
-        // stage's barrier has one phase per tile held; its next phase needs this tile, so the wait is exact)
-        if (tg >= 2 && !warp_wait(is_v ? &bar_o[tg & 1] : &bar_s[tg & 1], ((tg - 2) >> 1) & 1)) {
+        // the stage of tile tg held tile tg - 2: wait until the MMA that read it has finished.  The
+        // barrier of its S buffer has one phase per tile held; this producer waits them in order and
+        // their next phase (tile tg + 1) needs this producer's copies, so the wait is exact.
+        if (tg >= 2 && !warp_wait(is_v ? &bar_o[(tg - 2) % kSBufs] : &bar_s[(tg - 2) % kSBufs],
+                                  ((tg - 2) / kSBufs) & 1)) {
           ok = false;
           break;
         }
@@ -496,18 +511,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_s = idesc<T>(0);
       tma_prefetch_descriptor(&tmap_q);
       // This thread also schedules: it publishes item k (the first one with queries at or after index
-      // idx) in items[k % 2] and starts the copy of its Q tile into shared memory, both completing
-      // phase k of bar_qs; the softmax warps move the tile into tensor memory.  It reports
-      // inconsistent chunks: every item of this CTA passes through here once.
+      // idx) in items[k % 2] and starts the copy of its Q tile into Q buffer k % 2, both completing
+      // phase k of bar_qs.  Item k + 1 is published once every softmax warp has read item k (bar_q
+      // phase k), which also means the S MMAs of item k - 1, the last readers of that Q buffer, have
+      // finished.  It reports inconsistent chunks: every item of this CTA passes through here once.
       auto publish = [&](int idx, int k, PfItem& it) {
         for (; idx < n_items; idx += gridDim.x)
           if (pf_item(p, idx, it, true)) break;
         if (idx >= n_items) it.s = -1;
         items[k & 1] = it;
         if (idx < n_items) {
+          uint8_t* qb = qbuf + (k & 1) * 2 * kHalf;
           mbar_arrive_expect_tx(bar_qs, 2 * kHalf);
-          tma_load_3d(qbuf, &tmap_q, 0, it.h, it.q0 + it.tile0, bar_qs);
-          tma_load_3d(qbuf + kHalf, &tmap_q, 64, it.h, it.q0 + it.tile0, bar_qs);
+          tma_load_3d(qb, &tmap_q, 0, it.h, it.q0 + it.tile0, bar_qs);
+          tma_load_3d(qb + kHalf, &tmap_q, 64, it.h, it.q0 + it.tile0, bar_qs);
         } else {
           mbar_arrive(bar_qs);
         }
@@ -518,27 +535,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       PfItem it;
       int idx = publish(blockIdx.x, 0, it);
       while (ok && idx < n_items) {
-        // Q of this item in tensor memory, so the Q buffer may take the next one (the barrier's next
-        // phase, the item after, is written only after this item's S MMAs have finished: exact)
-        ok = wait_bar_spin(bar_q, item_no & 1, abort_flag);
+        // Q of this item in its buffer (this thread publishes the barrier's next phase: exact)
+        ok = wait_bar_spin(bar_qs, item_no & 1, abort_flag);
         if (!ok) break;
         PfItem nx;
-        const int idx_next = publish(idx + gridDim.x, item_no + 1, nx);
+        int idx_next = n_items;
+        bool published = false;
+        // publish the next item once every softmax warp has read this one (checked between tiles, and
+        // waited for at the end of the item; the barrier's next phase needs that publication: exact)
+        auto try_publish = [&](bool block) {
+          if (published) return;
+          if (block ? wait_bar_spin(bar_q, item_no & 1, abort_flag) : mbar_test_wait(bar_q, item_no & 1)) {
+            idx_next = publish(idx + gridDim.x, item_no + 1, nx);
+            published = true;
+          } else if (block) {
+            ok = false;
+          }
+        };
+        const uint32_t qa = smem_u32(qbuf + (item_no & 1) * 2 * kHalf);
         for (int t = 0; ok && t < it.key_tiles; ++t, ++tg) {
-          // buffer tg % 2 held P of tile tg - 2 (its P V must have finished; the barrier's next phase,
+          try_publish(false);
+          const int buf = tg % kSBufs;
+          // buffer tg % 3 held P of tile tg - 3 (its P V must have finished; the barrier's next phase,
           // tile tg, needs this S, so the wait is exact) and K stage tg % 2 must hold key tile tg
-          if (tg >= 2) ok = wait_bar_spin(&bar_o[tg & 1], ((tg - 2) >> 1) & 1, abort_flag);
+          if (tg >= kSBufs) ok = wait_bar_spin(&bar_o[buf], ((tg - kSBufs) / kSBufs) & 1, abort_flag);
           ok = ok && wait_bar_spin(&bar_k[tg & 1], (tg >> 1) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
           const uint32_t kb = smem_u32(smem + kKOff + (tg & 1) * 2 * kHalf);
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk)
-            mma_ts(tmem + (tg & 1) * 128, tmem + kQCol + kk * 8,
+            mma_ss(tmem + buf * 128, sw128_desc(qa + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
                    sw128_desc(kb + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
-          mma_commit(&bar_s[tg & 1]);
+          mma_commit(&bar_s[buf]);
           ++n_s;
         }
+        if (ok) try_publish(true);
         ++item_no;
         idx = idx_next;
         it = nx;
@@ -558,13 +590,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // next phase is this item's epilogue, which needs these MMAs, so the wait is exact)
         if (item_no > 0) ok = wait_bar_spin(bar_ofree, (item_no - 1) & 1, abort_flag);
         for (int kt = 0; ok && kt < it.key_tiles; ++kt, ++tg) {
-          const int buf = tg & 1;
+          const int buf = tg % kSBufs;
           // once every softmax warp has written P of tile tg and V of tile tg is in place
-          ok = wait_bar_spin(&bar_p[buf], (tg >> 1) & 1, abort_flag) &&
-               wait_bar_spin(&bar_v[buf], (tg >> 1) & 1, abort_flag);
+          ok = wait_bar_spin(&bar_p[buf], (tg / kSBufs) & 1, abort_flag) &&
+               wait_bar_spin(&bar_v[tg & 1], (tg >> 1) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t vb = smem_u32(smem + kVOff + buf * 2 * kHalf);
+          const uint32_t vb = smem_u32(smem + kVOff + (tg & 1) * 2 * kHalf);
           // keys 16kk .. 16kk + 15 of the tile: P hi (lo) in columns 8kk (64 + 8kk) of the buffer
 #pragma unroll
           for (int part = 0; part < (split_p<T>() ? 2 : 1); ++part) {
@@ -576,9 +608,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(&bar_o[buf]);
           ++n_o;
         }
-        // the item's last P V has finished: O is complete (the stage barrier's previous phase finished
+        // the item's last P V has finished: O is complete (the buffer barrier's previous phase finished
         // before the S that fed this P; its next phase needs a P V not yet issued, so the wait is exact)
-        if (ok) ok = wait_bar_spin(&bar_o[(tg - 1) & 1], ((tg - 1) >> 1) & 1, abort_flag);
+        if (ok) ok = wait_bar_spin(&bar_o[(tg - 1) % kSBufs], ((tg - 1) / kSBufs) & 1, abort_flag);
         if (ok) mbar_arrive(bar_done);
         ++item_no;
       }
@@ -593,35 +625,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t half_base = (uint32_t)(q4 * 32 + hh * 16) << 16;  // first lane of this warp's rows
     const int r0 = q4 * 32 + hh * 16 + (lane >> 2), r1 = r0 + 8;
     const float sl2 = p.scale_log2;
-    // the Q tile in shared memory (two 128-byte-swizzled halves) -> tensor memory columns kQCol.. (two
-    // elements per column, lower index in the low half); warps 0..3, one row per thread
-    auto copy_q = [&]() {
-      const int row = q4 * 32 + lane;
-      const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-      uint32_t qw[64];
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 u = *reinterpret_cast<const uint4*>(qbuf + hf * kHalf + swz128(row, c));
-          qw[32 * hf + 4 * c] = u.x, qw[32 * hf + 4 * c + 1] = u.y, qw[32 * hf + 4 * c + 2] = u.z,
-                         qw[32 * hf + 4 * c + 3] = u.w;
-        }
-      }
-      tmem_st32(tmem + lane_base + kQCol, qw);
-      tmem_st32(tmem + lane_base + kQCol + 32, qw + 32);
-      tmem_wait_st();
-      tc_fence_before();
-    };
-    // warps 0..3 move the published item's Q into tensor memory; every warp then arrives on bar_q
+    // every warp arrives on bar_q once it has read the published item
     auto take_item = [&]() {
-      if (hh == 0) copy_q();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_q);
     };
     bool ok = true;
     int tg = 0, item_no = 0;
-    // the first item and its Q
+    // the first item
     ok = warp_wait(bar_qs, 0);
     PfItem it = items[0];
     if (ok && it.s >= 0) take_item();
@@ -631,8 +642,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int lim0 = min(it.pos0 + r0, it.L - 1), lim1 = min(it.pos0 + r1, it.L - 1);  // last key each row sees
       float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // reference maxima (log2 units), partial sums
       for (int kt = 0; kt < it.key_tiles; ++kt, ++tg) {
-        const int buf = tg & 1;
-        ok = __all_sync(0xffffffffu, wait_bar_spin(&bar_s[buf], (tg >> 1) & 1, abort_flag)) && ok;
+        const int buf = tg % kSBufs;
+        ok = __all_sync(0xffffffffu, wait_bar_spin(&bar_s[buf], (tg / kSBufs) & 1, abort_flag)) && ok;
         tc_fence_after();
         const uint32_t s_addr = tmem + half_base + buf * 128;
         float v[64];
@@ -670,9 +681,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float al0 = upd0 ? fast_exp2(m0 - mx0) : 1.f, al1 = upd1 ? fast_exp2(m1 - mx1) : 1.f;
         if (__any_sync(0xffffffffu, upd0 || upd1) && kt > 0 && ok) {
           // O of these rows is rescaled between P V of tile tg - 1 and that of tile tg.  The barrier
-          // of its V stage finished tile tg - 3 before S(tg - 1) was issued and its next phase (tile
-          // tg + 1) needs this warp's P, so the parity wait below is exact.
-          ok = warp_wait(&bar_o[(tg - 1) & 1], ((tg - 1) >> 1) & 1);
+          // of its S buffer finished tile tg - 4 before S(tg - 1) was issued and its next phase (tile
+          // tg + 2) needs this warp's P, so the parity wait below is exact.
+          ok = warp_wait(&bar_o[(tg - 1) % kSBufs], ((tg - 1) / kSBufs) & 1);
           tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < 2; ++c) {
@@ -710,9 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bar_p[buf]);
       }
       if (!ok) break;
-      // ---- the next item and its Q: its S MMAs may run while this item's epilogue does (this item's
-      //      S MMAs, the only readers of Q in tensor memory, have all finished: the last bar_s wait
-      //      above covered them)
+      // ---- the next item (its S MMAs may run while this item's epilogue does)
       ok = warp_wait(bar_qs, (item_no + 1) & 1);
       const PfItem nx = items[(item_no + 1) & 1];
       if (ok && nx.s >= 0) take_item();
@@ -759,9 +768,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = max(0, n_issued - 2); t < n_issued; ++t) drain_wait(&ring_bar[t & 1], (t >> 1) & 1);
     }
     if (warp == kSWarp && lane == 0)
-      for (int t = max(0, n_s - 2); t < n_s; ++t) drain_wait(&bar_s[t & 1], (t >> 1) & 1);
+      for (int t = max(0, n_s - kSBufs); t < n_s; ++t) drain_wait(&bar_s[t % kSBufs], (t / kSBufs) & 1);
     if (warp == kPVWarp && lane == 0)
-      for (int t = max(0, n_o - 2); t < n_o; ++t) drain_wait(&bar_o[t & 1], (t >> 1) & 1);
+      for (int t = max(0, n_o - kSBufs); t < n_o; ++t) drain_wait(&bar_o[t % kSBufs], (t / kSBufs) & 1);
     __syncthreads();
   }
   if (warp == 0)
