@@ -744,14 +744,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ofree);
       const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-      T* out0 = reinterpret_cast<T*>(p.out) + ((size_t)(it.q0 + it.tile0 + r0) * p.num_q_heads + it.h) * kD + 2 * c4;
+      // Thread c of a quad holds packed word j of a row for columns 8j + 2c, 8j + 2c + 1.  A 4 x 4 word
+      // transpose within the quad (two xor-shuffle steps per group of 4 j) gives thread c the 16 bytes
+      // of columns 8j .. 8j + 7 for j = 4g + c, so a store writes 16 bytes per thread and 64
+      // contiguous bytes per row and quad.
+      T* out0 = reinterpret_cast<T*>(p.out) + ((size_t)(it.q0 + it.tile0 + r0) * p.num_q_heads + it.h) * kD;
       T* out1 = out0 + (size_t)8 * p.num_q_heads * kD;  // row r1 = r0 + 8
+      const bool hi2 = (c4 >> 1) != 0, odd = (c4 & 1) != 0;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        if (r0 < it.rows)
-          *reinterpret_cast<uint32_t*>(out0 + 8 * j) = Mma<T>::pack(o[4 * j] * inv0, o[4 * j + 1] * inv0);
-        if (r1 < it.rows)
-          *reinterpret_cast<uint32_t*>(out1 + 8 * j) = Mma<T>::pack(o[4 * j + 2] * inv1, o[4 * j + 3] * inv1);
+      for (int rr = 0; rr < 2; ++rr) {
+        const float inv = rr ? inv1 : inv0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            w[i] = Mma<T>::pack(o[4 * (4 * g + i) + 2 * rr] * inv, o[4 * (4 * g + i) + 2 * rr + 1] * inv);
+          // step 1 (lanes c, c ^ 2): the upper pair of words of threads 0, 1 swaps with the lower pair of 2, 3
+          const uint32_t x0 = __shfl_xor_sync(0xffffffffu, hi2 ? w[0] : w[2], 2);
+          const uint32_t x1 = __shfl_xor_sync(0xffffffffu, hi2 ? w[1] : w[3], 2);
+          if (hi2) w[0] = x0, w[1] = x1;
+          else w[2] = x0, w[3] = x1;
+          // step 2 (lanes c, c ^ 1): within each pair of words, an odd word of an even thread swaps with an
+          // even word of an odd thread
+          const uint32_t y0 = __shfl_xor_sync(0xffffffffu, odd ? w[0] : w[1], 1);
+          const uint32_t y1 = __shfl_xor_sync(0xffffffffu, odd ? w[2] : w[3], 1);
+          if (odd) w[0] = y0, w[2] = y1;
+          else w[1] = y0, w[3] = y1;
+          if ((rr ? r1 : r0) < it.rows)
+            *reinterpret_cast<uint4*>((rr ? out1 : out0) + 8 * (4 * g + c4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
       }
       ++item_no;
       it = nx;
