@@ -632,104 +632,118 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     bool ok = true;
     int tg = 0, item_no = 0;
-    // the first item
+    int lim0 = 0, lim1 = 0;                                    // last key position each row sees
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // reference maxima (log2 units), partial sums
+    // key tile kt of the current item (this CTA's tile tg)
+    auto tile = [&](int kt) {
+      const int buf = tg % kSBufs;
+      ok = __all_sync(0xffffffffu, wait_bar_spin(&bar_s[buf], (tg / kSBufs) & 1, abort_flag)) && ok;
+      tc_fence_after();
+      const uint32_t s_addr = tmem + half_base + buf * 128;
+      float v[64];
+      tmem_ld16x256_x8(s_addr, v);
+      tmem_ld16x256_x8(s_addr + 64, v + 32);
+      tmem_wait_ld<64>(v);
+      const int key0 = kt * kTile + 2 * c4;          // key of this thread's pair 0
+      const int e0 = lim0 - key0, e1 = lim1 - key0;  // pair j's keys 8j, 8j + 1 are visible up to e
+      const bool unmasked = __all_sync(0xffffffffu, min(lim0, lim1) >= kt * kTile + kTile - 1);
+      // ---- the rows' tile maxima, and the reference maxima they imply
+      float a0 = -INFINITY, b0 = -INFINITY, a1 = -INFINITY, b1 = -INFINITY;  // two chains per row
+      if (unmasked) {
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+          a0 = max3(a0, v[4 * j], v[4 * j + 1]);
+          a1 = max3(a1, v[4 * j + 2], v[4 * j + 3]);
+          b0 = max3(b0, v[4 * j + 4], v[4 * j + 5]);
+          b1 = max3(b1, v[4 * j + 6], v[4 * j + 7]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          a0 = max3(a0, 8 * j <= e0 ? v[4 * j] : -INFINITY, 8 * j + 1 <= e0 ? v[4 * j + 1] : -INFINITY);
+          a1 = max3(a1, 8 * j <= e1 ? v[4 * j + 2] : -INFINITY, 8 * j + 1 <= e1 ? v[4 * j + 3] : -INFINITY);
+        }
+      }
+      a0 = fmaxf(a0, b0);
+      a1 = fmaxf(a1, b1);
+      a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, 1));
+      a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
+      a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, 2));
+      a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 2));
+      const float mx0 = a0 * sl2, mx1 = a1 * sl2;  // scale > 0
+      const bool upd0 = mx0 > m0 + kRescaleThreshold, upd1 = mx1 > m1 + kRescaleThreshold;
+      const float al0 = upd0 ? fast_exp2(m0 - mx0) : 1.f, al1 = upd1 ? fast_exp2(m1 - mx1) : 1.f;
+      if (__any_sync(0xffffffffu, upd0 || upd1) && kt > 0 && ok) {
+        // O of these rows is rescaled between P V of tile tg - 1 and that of tile tg.  The barrier
+        // of its S buffer finished tile tg - 4 before S(tg - 1) was issued and its next phase (tile
+        // tg + 2) needs this warp's P, so the parity wait below is exact.
+        ok = warp_wait(&bar_o[(tg - 1) % kSBufs], ((tg - 1) / kSBufs) & 1);
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          float o[32];
+          tmem_ld16x256_x8(tmem + half_base + kOCol + 64 * c, o);
+          tmem_wait_ld<32>(o);
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            o[i] *= al0, o[i + 1] *= al0;
+            o[i + 2] *= al1, o[i + 3] *= al1;
+          }
+          tmem_st16x256_x8(tmem + half_base + kOCol + 64 * c, reinterpret_cast<const uint32_t*>(o));
+        }
+        tmem_wait_st();
+      }
+      if (upd0) m0 = mx0;
+      if (upd1) m1 = mx1;
+      // ---- P into the buffer, 8 pairs (32 columns of packed words) at a time: hi words in columns
+      //      0..63, lo words in 64..127
+      l0 *= al0;
+      l1 *= al1;
+#pragma unroll
+      for (int j0 = 0; j0 < 16; j0 += 8) {
+        uint32_t hi[16], lo[16];
+        if (unmasked)
+          make_p<T, false>(v, j0, sl2, m0, m1, e0, e1, hi, lo, l0, l1);
+        else
+          make_p<T, true>(v, j0, sl2, m0, m1, e0, e1, hi, lo, l0, l1);
+        tmem_st16x128_x8(s_addr + 4 * j0, hi);
+        if constexpr (split_p<T>()) tmem_st16x128_x8(s_addr + 64 + 4 * j0, lo);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_p[buf]);
+      ++tg;
+    };
+    auto start_item = [&](const PfItem& x) {
+      take_item();
+      lim0 = min(x.pos0 + r0, x.L - 1);
+      lim1 = min(x.pos0 + r1, x.L - 1);
+      m0 = m1 = -INFINITY;
+      l0 = l1 = 0.f;
+      tile(0);
+    };
+    // the first item and its first tile
     ok = warp_wait(bar_qs, 0);
     PfItem it = items[0];
-    if (ok && it.s >= 0) take_item();
+    if (ok && it.s >= 0) start_item(it);
     // After a failure (a wait gave up) every warp leaves at the next wait: no warp waits for another
     // softmax warp, and the other roles stop at their next wait too.
     while (ok && it.s >= 0) {
-      const int lim0 = min(it.pos0 + r0, it.L - 1), lim1 = min(it.pos0 + r1, it.L - 1);  // last key each row sees
-      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // reference maxima (log2 units), partial sums
-      for (int kt = 0; kt < it.key_tiles; ++kt, ++tg) {
-        const int buf = tg % kSBufs;
-        ok = __all_sync(0xffffffffu, wait_bar_spin(&bar_s[buf], (tg / kSBufs) & 1, abort_flag)) && ok;
-        tc_fence_after();
-        const uint32_t s_addr = tmem + half_base + buf * 128;
-        float v[64];
-        tmem_ld16x256_x8(s_addr, v);
-        tmem_ld16x256_x8(s_addr + 64, v + 32);
-        tmem_wait_ld<64>(v);
-        const int key0 = kt * kTile + 2 * c4;          // key of this thread's pair 0
-        const int e0 = lim0 - key0, e1 = lim1 - key0;  // pair j's keys 8j, 8j + 1 are visible up to e
-        const bool unmasked = __all_sync(0xffffffffu, min(lim0, lim1) >= kt * kTile + kTile - 1);
-        // ---- the rows' tile maxima, and the reference maxima they imply
-        float a0 = -INFINITY, b0 = -INFINITY, a1 = -INFINITY, b1 = -INFINITY;  // two chains per row
-        if (unmasked) {
-#pragma unroll
-          for (int j = 0; j < 16; j += 2) {
-            a0 = max3(a0, v[4 * j], v[4 * j + 1]);
-            a1 = max3(a1, v[4 * j + 2], v[4 * j + 3]);
-            b0 = max3(b0, v[4 * j + 4], v[4 * j + 5]);
-            b1 = max3(b1, v[4 * j + 6], v[4 * j + 7]);
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            a0 = max3(a0, 8 * j <= e0 ? v[4 * j] : -INFINITY, 8 * j + 1 <= e0 ? v[4 * j + 1] : -INFINITY);
-            a1 = max3(a1, 8 * j <= e1 ? v[4 * j + 2] : -INFINITY, 8 * j + 1 <= e1 ? v[4 * j + 3] : -INFINITY);
-          }
-        }
-        a0 = fmaxf(a0, b0);
-        a1 = fmaxf(a1, b1);
-        a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, 1));
-        a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
-        a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, 2));
-        a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 2));
-        const float mx0 = a0 * sl2, mx1 = a1 * sl2;  // scale > 0
-        const bool upd0 = mx0 > m0 + kRescaleThreshold, upd1 = mx1 > m1 + kRescaleThreshold;
-        const float al0 = upd0 ? fast_exp2(m0 - mx0) : 1.f, al1 = upd1 ? fast_exp2(m1 - mx1) : 1.f;
-        if (__any_sync(0xffffffffu, upd0 || upd1) && kt > 0 && ok) {
-          // O of these rows is rescaled between P V of tile tg - 1 and that of tile tg.  The barrier
-          // of its S buffer finished tile tg - 4 before S(tg - 1) was issued and its next phase (tile
-          // tg + 2) needs this warp's P, so the parity wait below is exact.
-          ok = warp_wait(&bar_o[(tg - 1) % kSBufs], ((tg - 1) / kSBufs) & 1);
-          tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
-            float o[32];
-            tmem_ld16x256_x8(tmem + half_base + kOCol + 64 * c, o);
-            tmem_wait_ld<32>(o);
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              o[i] *= al0, o[i + 1] *= al0;
-              o[i + 2] *= al1, o[i + 3] *= al1;
-            }
-            tmem_st16x256_x8(tmem + half_base + kOCol + 64 * c, reinterpret_cast<const uint32_t*>(o));
-          }
-          tmem_wait_st();
-        }
-        if (upd0) m0 = mx0;
-        if (upd1) m1 = mx1;
-        // ---- P into the buffer, 8 pairs (32 columns of packed words) at a time: hi words in columns
-        //      0..63, lo words in 64..127
-        l0 *= al0;
-        l1 *= al1;
-#pragma unroll
-        for (int j0 = 0; j0 < 16; j0 += 8) {
-          uint32_t hi[16], lo[16];
-          if (unmasked)
-            make_p<T, false>(v, j0, sl2, m0, m1, e0, e1, hi, lo, l0, l1);
-          else
-            make_p<T, true>(v, j0, sl2, m0, m1, e0, e1, hi, lo, l0, l1);
-          tmem_st16x128_x8(s_addr + 4 * j0, hi);
-          if constexpr (split_p<T>()) tmem_st16x128_x8(s_addr + 64 + 4 * j0, lo);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_p[buf]);
-      }
+      for (int kt = 1; kt < it.key_tiles; ++kt) tile(kt);
       if (!ok) break;
-      // ---- the next item (its S MMAs may run while this item's epilogue does)
+      // ---- row sums of this item over each row's four threads
+      float s0 = l0, s1 = l1;
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+      // ---- the next item and its first tile.  That tile writes no O (no rescale on a first tile) and its
+      //      P V waits for this item's epilogue to have read O, so it runs before the epilogue, beside
+      //      this item's last P V.
       ok = warp_wait(bar_qs, (item_no + 1) & 1);
       const PfItem nx = items[(item_no + 1) & 1];
-      if (ok && nx.s >= 0) take_item();
-      // ---- row sums over each row's four threads
-      l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-      l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+      if (ok && nx.s >= 0) start_item(nx);
       // ---- epilogue: out = O / l for this warp's 16 rows, from the 16x256b layout (thread: rows r0, r1,
       //      columns 8j + 2 (t % 4) and + 1)
       if (ok) ok = warp_wait(bar_done, item_no & 1);
@@ -743,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ofree);
-      const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+      const float inv0 = s0 > 0.f ? 1.f / s0 : 0.f, inv1 = s1 > 0.f ? 1.f / s1 : 0.f;
       // Thread c of a quad holds packed word j of a row for columns 8j + 2c, 8j + 2c + 1.  A 4 x 4 word
       // transpose within the quad (two xor-shuffle steps per group of 4 j) gives thread c the 16 bytes
       // of columns 8j .. 8j + 7 for j = 4g + c, so a store writes 16 bytes per thread and 64
