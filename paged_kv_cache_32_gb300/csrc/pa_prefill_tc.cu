@@ -741,9 +741,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- the next item and its first tile.  That tile writes no O (no rescale on a first tile) and its
       //      P V waits for this item's epilogue to have read O, so it runs before the epilogue, beside
       //      this item's last P V.
+      // (what the epilogue needs of this item is kept apart, and the next item becomes the current one)
+      T* out0 = reinterpret_cast<T*>(p.out) + ((size_t)(it.q0 + it.tile0 + r0) * p.num_q_heads + it.h) * kD;
+      const int rows = it.rows;
       ok = warp_wait(bar_qs, (item_no + 1) & 1);
-      const PfItem nx = items[(item_no + 1) & 1];
-      if (ok && nx.s >= 0) start_item(nx);
+      it = items[(item_no + 1) & 1];
+      if (ok && it.s >= 0) start_item(it);
       // ---- epilogue: out = O / l for this warp's 16 rows, from the 16x256b layout (thread: rows r0, r1,
       //      columns 8j + 2 (t % 4) and + 1)
       if (ok) ok = warp_wait(bar_done, item_no & 1);
@@ -762,7 +765,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // transpose within the quad (two xor-shuffle steps per group of 4 j) gives thread c the 16 bytes
       // of columns 8j .. 8j + 7 for j = 4g + c, so a store writes 16 bytes per thread and 64
       // contiguous bytes per row and quad.
-      T* out0 = reinterpret_cast<T*>(p.out) + ((size_t)(it.q0 + it.tile0 + r0) * p.num_q_heads + it.h) * kD;
       T* out1 = out0 + (size_t)8 * p.num_q_heads * kD;  // row r1 = r0 + 8
       const bool hi2 = (c4 >> 1) != 0, odd = (c4 & 1) != 0;
 #pragma unroll
@@ -785,12 +787,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t y1 = __shfl_xor_sync(0xffffffffu, odd ? w[2] : w[3], 1);
           if (odd) w[0] = y0, w[2] = y1;
           else w[1] = y0, w[3] = y1;
-          if ((rr ? r1 : r0) < it.rows)
+          if ((rr ? r1 : r0) < rows)
             *reinterpret_cast<uint4*>((rr ? out1 : out0) + 8 * (4 * g + c4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
       ++item_no;
-      it = nx;
     }
   }
   tc_fence_before();
