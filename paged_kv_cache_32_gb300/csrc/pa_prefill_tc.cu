@@ -37,6 +37,11 @@
 //    S of tile kt + 3 goes into the buffer of tile kt once P V of tile kt has
 //    finished; with separate issuers that wait never delays the next P V, and
 //    the softmax of tile kt + 1 overlaps P V of tile kt and S of tile kt + 3.
+//  * Items: the S-issuing thread also publishes each item in shared memory
+//    and starts its Q copy; item k + 1 is published once every softmax warp
+//    has read item k.  The softmax warps process the next item's first tile
+//    right after the current item's last one (it writes no O), then run the
+//    current item's epilogue while its last P V finishes.
 //  * Warps 0..7 run the softmax.  Each owns 16 query rows (tensor-memory
 //    lanes) and all 128 keys of a tile, read with the 16-lane 16x256b shape:
 //    a thread holds two rows, 32 keys of each, so a row's maximum and sum
