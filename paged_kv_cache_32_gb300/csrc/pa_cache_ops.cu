@@ -1,5 +1,5 @@
-// pa_merge_and_cache.cu - the partition merge of long-context decode, the
-// slot-mapping append and the copy-on-write block copy.
+// pa_cache_ops.cu - the cache writes: the slot-mapping append and the
+// copy-on-write block copy.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -10,76 +10,6 @@
 #include "pa_internal.h"
 
 namespace pa {
-
-// ---------------------------------------------------------------------------
-// Partition merge ("PagedAttention是什麼？", section "PagedAttention Kernel在做
-// 什麼？": long contexts use a partition reduction).  Partition p of a
-// sequence left m_p (max score, log2 units), l_p = sum 2^(s_i - m_p) and the
-// unnormalised o_p = sum 2^(s_i - m_p) v_i.  With m* = max_p m_p and
-// w_p = 2^(m_p - m*):  out = sum_p w_p o_p / sum_p w_p l_p.
-// One CTA of D threads per (sequence, query head); thread d owns output dim d.
-// ---------------------------------------------------------------------------
-template <typename T, int D>
-__global__ void __launch_bounds__(D) merge_kernel(const DecodeParams p) {
-  constexpr int CHUNK = 256;
-  __shared__ float s_w[CHUNK];
-  __shared__ float s_lw[CHUNK];
-  __shared__ float s_red[D / 32];
-
-  const int sh = blockIdx.x;
-  const int s = sh / p.num_q_heads;
-  int L = p.seq_lens[s];
-  L = max(0, min(L, p.max_blocks * p.block_size));
-  const int nparts = (L + p.partition_size - 1) / p.partition_size;
-  if (nparts <= 1) return;  // written directly by the decode kernel
-  const float* ml = p.ws_ml + (size_t)sh * p.pmax * 2;
-  const float* os = p.ws_o + (size_t)sh * p.pmax * D;
-  const int tid = threadIdx.x;
-
-  float mx = -INFINITY;
-  for (int i = tid; i < nparts; i += D) mx = fmaxf(mx, ml[2 * i]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  if ((tid & 31) == 0) s_red[tid >> 5] = mx;
-  __syncthreads();
-  float mstar = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < D / 32; ++w) mstar = fmaxf(mstar, s_red[w]);
-
-  float acc = 0.f, lsum = 0.f;
-  for (int base = 0; base < nparts; base += CHUNK) {
-    const int n = min(CHUNK, nparts - base);
-    __syncthreads();
-    for (int i = tid; i < n; i += D) {
-      const float mi = ml[2 * (base + i)];
-      const float w = (mi == -INFINITY || mstar == -INFINITY) ? 0.f : fast_exp2(mi - mstar);
-      s_w[i] = w;
-      s_lw[i] = w * ml[2 * (base + i) + 1];
-    }
-    __syncthreads();
-    for (int i = 0; i < n; ++i) {
-      acc = fmaf(s_w[i], os[(size_t)(base + i) * D + tid], acc);
-      lsum += s_lw[i];
-    }
-  }
-  T* out = reinterpret_cast<T*>(p.out);
-  out[(size_t)sh * D + tid] = from_float<T>(lsum > 0.f ? acc / lsum : 0.f);
-}
-
-cudaError_t launch_merge(int dtype, int head_size, const DecodeParams& p, cudaStream_t stream) {
-  const long long grid = (long long)p.num_seqs * p.num_q_heads;
-  if (grid == 0) return cudaSuccess;
-#define PA_MERGE(T, DD) merge_kernel<T, DD><<<(unsigned)grid, DD, 0, stream>>>(p)
-  if (dtype == PA_F32 && head_size == 64) PA_MERGE(float, 64);
-  else if (dtype == PA_F32 && head_size == 128) PA_MERGE(float, 128);
-  else if (dtype == PA_F16 && head_size == 64) PA_MERGE(__half, 64);
-  else if (dtype == PA_F16 && head_size == 128) PA_MERGE(__half, 128);
-  else if (dtype == PA_BF16 && head_size == 64) PA_MERGE(__nv_bfloat16, 64);
-  else if (dtype == PA_BF16 && head_size == 128) PA_MERGE(__nv_bfloat16, 128);
-  else return cudaErrorInvalidValue;
-#undef PA_MERGE
-  return cudaGetLastError();
-}
 
 // ---------------------------------------------------------------------------
 // Slot-mapping append ("PagedAttention 详解：缓存的存储结构", section "写入新

@@ -3,8 +3,8 @@
 // Same definition as the fp16/bf16 kernel ("vLLM 核心工程深度剖析", section
 // "3.1 Kernel 签名与分块策略"; address translation per "PagedAttention 详解：
 // 缓存的存储结构", section "软件地址翻译"), same grid of (sequence, kv head,
-// head group, partition) CTAs and same partial-result format, so the merge
-// kernel serves both.  fp32 needs exact fp32 products, so no tensor-core path:
+// head group, partition) CTAs and same partial-result format, so one merge
+// kernel serves all decode kernels.  fp32 needs exact fp32 products, so no tensor-core path:
 // each warp walks a strided subset of the partition's tokens, every lane holds
 // D/32 consecutive elements of each row (coalesced 256/512-byte row loads),
 // dot products are reduced with warp shuffles, and the softmax is online.
@@ -24,6 +24,7 @@ __global__ void __launch_bounds__(NW * 32)
   __shared__ float s_o[NW][8][D];
   __shared__ float s_ml[NW][8][2];
 
+  griddep_launch_dependents();  // the partition merge may be scheduled behind this grid's last CTAs
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int per_seq = p.num_kv_heads * p.head_groups;

@@ -263,6 +263,7 @@ __global__ void __launch_bounds__(Fp8Shape<D, NW, NS>::THREADS)
                       const uint8_t* __restrict__ v_cache, const DecodeParams p, const float k_scale,
                       const float v_scale) {
   using S = Fp8Shape<D, NW, NS>;
+  griddep_launch_dependents();  // the partition merge may be scheduled behind this grid's last CTAs
   Fp8Item it;
   if (!fp8_item(p, blockIdx.x, it)) return;
 

@@ -228,6 +228,7 @@ __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                      const DecodeParams p) {
   using S = Shape<D, NW, NS>;
+  griddep_launch_dependents();  // the partition merge may be scheduled behind this grid's last CTAs
   Item it;
   if (!decode_item(p, blockIdx.x, it)) return;  // partition past the end of its sequence
 

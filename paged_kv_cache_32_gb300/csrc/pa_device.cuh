@@ -165,6 +165,16 @@ __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t chunk) {
   return row * 128u + (((chunk ^ (row & 7u)) & 7u) << 4);
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// launch_dependents: the next kernel on the stream, if launched with programmatic
+// stream serialization, may start once every CTA of this grid has executed this
+// (or exited).  wait: block until the grid this one depends on has completed and
+// its memory operations are visible.  Both are no-ops without such a launch.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- errors
 __device__ __forceinline__ void report_error(int32_t* flag, int32_t code) {
   if (flag != nullptr) atomicCAS(flag, 0, code);

@@ -157,6 +157,17 @@ def test_fp8_decode_small(block_size, hq, hkv):
     print(w.name, "max abs err", err)
 
 
+def test_fp8_merge_many_partitions():
+    """One 16-token block per partition: 157, 69, 2 and 65 partitions in one launch."""
+    w = W.build_decode("fp8_many_parts", seed=371, dtype="f16", seq_lens=[2500, 1100, 17, 0, 1040], num_q_heads=16,
+                       num_kv_heads=2, head_size=128, block_size=16, pool_factor=1.2)
+    g = Fp8Step(w, 0.0123, 0.0117)
+    k, v = g.host_after_append()
+    got = g.decode(partition_size=16)
+    assert int(g.err.item()) == 0
+    assert_close(got, g.oracle(k, v), "fp8, one block per partition")
+
+
 def test_fp8_decode_alibi():
     w = W.build_decode("fp8_alibi", seed=331, dtype="f16", seq_lens=[5, 33, 500], num_q_heads=16, num_kv_heads=2,
                        head_size=128, block_size=16, pool_factor=1.3)

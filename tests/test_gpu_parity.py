@@ -96,6 +96,42 @@ def test_small_cases(case, partition):
     check_step(w, partition_size=part)
 
 
+# ---------------------------------------------------------------- the partition merge
+MANY = [  # dtype, Hq, Hkv, B, lens; one block per partition: up to 157 partitions in a sequence
+    ("f16", 8, 1, 16, [2500, 1100, 17, 0, 1040]),    # G = 8: one group of eight query heads
+    ("bf16", 16, 1, 16, [2500, 1100, 17, 0, 1040]),  # G = 16: two head groups per kv head
+    ("f16", 4, 4, 32, [4100, 33, 2080]),             # G = 1
+    ("f32", 6, 2, 16, [1300, 20]),                   # G = 3, the CUDA-core kernel
+]
+
+
+@pytest.mark.parametrize("case", MANY, ids=lambda c: f"{c[0]}-Hq{c[1]}-Hkv{c[2]}-B{c[3]}")
+def test_merge_many_partitions_garbage_workspace(case):
+    """Up to 157 partitions in a sequence (the merge splits a row's partitions over eight
+    warps), ragged counts per sequence (157, 69, 2, none, 65) and a workspace full of garbage
+    (every partial is written before it is read).  A second call on the same workspace gives
+    the bit-identical output."""
+    import torch
+    dtype, Hq, Hkv, B, lens = case
+    w = W.build_decode("many_parts", seed=zlib.crc32(repr(case).encode()) % 10000, dtype=dtype, seq_lens=lens,
+                       num_q_heads=Hq, num_kv_heads=Hkv, head_size=128, block_size=B, pool_factor=1.2)
+    g = GpuStep(w)
+    need = g.pa.pa_decode_workspace_size(w.num_seqs, Hq, w.max_blocks_per_seq, g.desc, B)
+    ws = torch.full((need,), 0x7F, dtype=torch.uint8, device="cuda")
+    g.pa.pa_decode(g.out, g.q, g.k, g.v, g.tables, g.lens, w.scale, partition_size=B, workspace=ws,
+                   err_flag=g.err, desc=g.desc)
+    first = g.out.clone()
+    g.pa.pa_decode(g.out, g.q, g.k, g.v, g.tables, g.lens, w.scale, partition_size=B, workspace=ws,
+                   err_flag=g.err, desc=g.desc)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    assert torch.equal(first, g.out)
+    _, _, ref = oracle_step(w)
+    got = out_f64(g.out)
+    ok, err, ratio = within_bound(got, ref, w.dtype)
+    assert ok, f"{case}: max abs err {err}, worst err/bound {ratio}"
+
+
 def test_permuted_block_ids_bit_identical():
     """Relabelling physical blocks leaves the GPU output bit-identical."""
     import torch
