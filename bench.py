@@ -67,13 +67,15 @@ def measured_peaks():
 
 
 # sources that define the decode call's kernels and launch configuration
-KERNEL_SOURCES = ("pa_api.cu", "pa_decode_tc.cu", "pa_device.cuh", "pa_internal.h", "pa_merge.cu")
+KERNEL_SOURCES = ("pa_api.cu", "pa_decode_tc.cu", "pa_decode_epilogue.cuh", "pa_device.cuh", "pa_internal.h",
+                  "pa_merge.cu")
 
 
 # sources that define the prefill call's kernel
 PREFILL_SOURCES = ("pa_prefill_api.cu", "pa_prefill_tc.cu", "pa_prefill.h", "pa_device.cuh", "pa_internal.h")
 # sources that define the decode call on an FP8 cache
-FP8_SOURCES = ("pa_api.cu", "pa_decode_fp8.cu", "pa_device.cuh", "pa_internal.h", "pa_merge.cu")
+FP8_SOURCES = ("pa_api.cu", "pa_decode_fp8.cu", "pa_decode_epilogue.cuh", "pa_device.cuh", "pa_internal.h",
+               "pa_merge.cu")
 
 
 def kernel_source_hash(sources=KERNEL_SOURCES) -> str:

@@ -36,6 +36,7 @@
 #include <math.h>
 
 #include "pa.h"
+#include "pa_decode_epilogue.cuh"
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -361,35 +362,8 @@ __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
   }
   __syncthreads();
 
-  const size_t row0 = (size_t)it.s * p.num_q_heads + it.hq0;
-  for (int idx = threadIdx.x; idx < it.gcount * D; idx += NW * 32) {
-    const int gh = idx / D, d = idx % D;
-    float mstar = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NW; ++w)
-      mstar = fmaxf(mstar, reinterpret_cast<const float*>(smem + w * S::RING_BYTES)[8 * S::OROW + gh * 2]);
-    float lsum = 0.f, acc = 0.f;
-    if (mstar != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float* wb = reinterpret_cast<const float*>(smem + w * S::RING_BYTES);
-        const float wt = fast_exp2(wb[8 * S::OROW + gh * 2] - mstar);
-        lsum += wt * wb[8 * S::OROW + gh * 2 + 1];
-        acc += wt * wb[gh * S::OROW + d];
-      }
-    }
-    if (it.final_out) {
-      T* out = reinterpret_cast<T*>(p.out);
-      out[(row0 + gh) * D + d] = from_float<T>(lsum > 0.f ? acc / lsum : 0.f);
-    } else {
-      const size_t slot = (row0 + gh) * p.pmax + it.part;
-      p.ws_o[slot * D + d] = acc;
-      if (d == 0) {
-        p.ws_ml[slot * 2] = mstar;
-        p.ws_ml[slot * 2 + 1] = lsum;
-      }
-    }
-  }
+  finish_item<T, D, NW, S::OROW, S::RING_BYTES>(smem, p, (size_t)it.s * p.num_q_heads + it.hq0, it.gcount,
+                                                it.final_out, it.part);
 }
 
 // ------------------------------------------------------------------ launch

@@ -32,9 +32,32 @@
 namespace pa {
 
 constexpr int kMergeThreads = 256;
+constexpr int KPRE = 4;  // partitions per warp whose outputs are loaded before the weights are known
+
+template <int V>
+__device__ __forceinline__ void load_vec(const float* src, float (&v)[V]) {
+  if constexpr (V == 4) {
+    const float4 x = *reinterpret_cast<const float4*>(src);
+    v[0] = x.x, v[1] = x.y, v[2] = x.z, v[3] = x.w;
+  } else if constexpr (V == 2) {
+    const float2 x = *reinterpret_cast<const float2*>(src);
+    v[0] = x.x, v[1] = x.y;
+  } else {
+#pragma unroll
+    for (int e = 0; e < V; ++e) v[e] = src[e];
+  }
+}
+
+// w_i = 2^(m_i - m*) of partition i (the same i in every lane of the warp): lane i
+// holds it for the first 32 partitions, later ones are read again.
+__device__ __forceinline__ float partition_weight(int i, float w_own, const float2* ml, float mx) {
+  if (i < 32) return __shfl_sync(0xffffffffu, w_own, i);
+  const float m = ml[i].x;
+  return (m == -INFINITY || mx == -INFINITY) ? 0.f : fast_exp2(m - mx);
+}
 
 template <typename T, int D, int WPR>
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kMergeThreads, 5) merge_kernel(const DecodeParams p) {
   constexpr int NWARP = kMergeThreads / 32;
   constexpr int ROWS = NWARP / WPR;  // rows per CTA
   constexpr int V = D / 32;          // output elements per lane
@@ -56,34 +79,41 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
   for (int e = 0; e < V; ++e) acc[e] = 0.f;
   float lsum = 0.f;
   if (nparts > 1) {  // a single partition was written out by the decode kernel
-    const float* ml = p.ws_ml + (size_t)row * p.pmax * 2;
+    const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + (size_t)row * p.pmax;  // (m_p, l_p)
     const float* os = p.ws_o + (size_t)row * p.pmax * D + lane * V;
-    float mx = -INFINITY;
-    for (int i = lane; i < nparts; i += 32) mx = fmaxf(mx, ml[2 * i]);
+    // One round trip: this warp's first KPRE partial outputs and lane i's pair (m_i, l_i).
+    float pre[KPRE][V];
+#pragma unroll
+    for (int k = 0; k < KPRE; ++k)
+      if (sub + k * WPR < nparts) load_vec<V>(os + (size_t)(sub + k * WPR) * D, pre[k]);
+    const float2 own = lane < nparts ? ml[lane] : make_float2(-INFINITY, 0.f);
+    float mx = own.x;
+    for (int i = lane + 32; i < nparts; i += 32) mx = fmaxf(mx, ml[i].x);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (sub == 0 && mx != -INFINITY) {
-      for (int i = lane; i < nparts; i += 32) {
-        const float2 v = *reinterpret_cast<const float2*>(ml + 2 * i);
-        if (v.x != -INFINITY) lsum += fast_exp2(v.x - mx) * v.y;
+    const float w_own = (own.x == -INFINITY || mx == -INFINITY) ? 0.f : fast_exp2(own.x - mx);  // w_lane
+    if (sub == 0) {
+      lsum = w_own * own.y;
+      for (int i = lane + 32; i < nparts; i += 32) {
+        const float2 v = ml[i];
+        if (v.x != -INFINITY && mx != -INFINITY) lsum += fast_exp2(v.x - mx) * v.y;
       }
     }
-    if (mx != -INFINITY) {
-#pragma unroll 4
-      for (int i = sub; i < nparts; i += WPR) {
-        const float m = ml[2 * i];  // the same word for every lane: one broadcast load
-        const float w = m == -INFINITY ? 0.f : fast_exp2(m - mx);
-        if constexpr (V == 4) {
-          const float4 o = *reinterpret_cast<const float4*>(os + (size_t)i * D);
-          acc[0] = fmaf(w, o.x, acc[0]);
-          acc[1] = fmaf(w, o.y, acc[1]);
-          acc[2] = fmaf(w, o.z, acc[2]);
-          acc[3] = fmaf(w, o.w, acc[3]);
-        } else {
 #pragma unroll
-          for (int e = 0; e < V; ++e) acc[e] = fmaf(w, os[(size_t)i * D + e], acc[e]);
-        }
+    for (int k = 0; k < KPRE; ++k) {
+      if (sub + k * WPR < nparts) {
+        const float w = partition_weight(sub + k * WPR, w_own, ml, mx);
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] = fmaf(w, pre[k][e], acc[e]);
       }
+    }
+#pragma unroll 4
+    for (int i = sub + KPRE * WPR; i < nparts; i += WPR) {
+      const float w = partition_weight(i, w_own, ml, mx);
+      float o[V];
+      load_vec<V>(os + (size_t)i * D, o);
+#pragma unroll
+      for (int e = 0; e < V; ++e) acc[e] = fmaf(w, o[e], acc[e]);
     }
   }
   if constexpr (WPR > 1) {  // the row's warps add their partition subsets
