@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(kAppendThreads)
                              const uint8_t* __restrict__ key, const uint8_t* __restrict__ value,
                              const int64_t* __restrict__ slot_mapping, int32_t num_blocks, int32_t block_size,
                              int32_t num_kv_heads, int32_t row_bytes, int32_t* err_flag) {
+  griddep_launch_dependents();  // a decode launched as a dependent may be scheduled behind this grid
   const int t = blockIdx.x;
   const int64_t slot = slot_mapping[t];
   if (slot < 0) return;
@@ -75,6 +76,7 @@ __global__ void __launch_bounds__(kCopyThreads)
     copy_blocks_kernel(uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
                        const int32_t* __restrict__ pairs, int32_t num_blocks, int64_t block_bytes,
                        int32_t pieces, int32_t* err_flag) {
+  griddep_launch_dependents();  // a decode launched as a dependent may be scheduled behind this grid
   const int pair = blockIdx.x / pieces;
   const int piece = blockIdx.x % pieces;
   const int32_t src = pairs[2 * pair];

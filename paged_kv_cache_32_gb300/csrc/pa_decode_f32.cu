@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(NW * 32)
   __shared__ float s_ml[NW][8][2];
 
   griddep_launch_dependents();  // the partition merge may be scheduled behind this grid's last CTAs
+  griddep_wait();               // launched as a dependent: the previous kernel's writes are visible from here
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int per_seq = p.num_kv_heads * p.head_groups;
@@ -151,14 +152,11 @@ cudaError_t launch_decode_f32(int head_size, const float* k_cache, const float* 
                               cudaStream_t stream) {
   const long long grid = (long long)p.num_seqs * p.num_kv_heads * p.head_groups * p.pmax;
   if (grid == 0) return cudaSuccess;
-  if (head_size == 64) {
-    decode_f32_kernel<64, 4><<<(unsigned)grid, 128, 0, stream>>>(k_cache, v_cache, p);
-  } else if (head_size == 128) {
-    decode_f32_kernel<128, 4><<<(unsigned)grid, 128, 0, stream>>>(k_cache, v_cache, p);
-  } else {
-    return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
+  if (head_size == 64) return launch_dependent(decode_f32_kernel<64, 4>, dim3((unsigned)grid), dim3(128), 0, stream,
+                                               k_cache, v_cache, p);
+  if (head_size == 128)
+    return launch_dependent(decode_f32_kernel<128, 4>, dim3((unsigned)grid), dim3(128), 0, stream, k_cache, v_cache, p);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pa

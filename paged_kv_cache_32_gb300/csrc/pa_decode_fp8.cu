@@ -265,6 +265,7 @@ __global__ void __launch_bounds__(Fp8Shape<D, NW, NS>::THREADS)
                       const float v_scale) {
   using S = Fp8Shape<D, NW, NS>;
   griddep_launch_dependents();  // the partition merge may be scheduled behind this grid's last CTAs
+  griddep_wait();               // launched as a dependent: the previous kernel's writes are visible from here
   Fp8Item it;
   if (!fp8_item(p, blockIdx.x, it)) return;
 
@@ -434,6 +435,7 @@ __global__ void __launch_bounds__(128)
                                  const int64_t* __restrict__ slot_mapping, int32_t num_blocks, int32_t block_size,
                                  int32_t num_kv_heads, int32_t head_size, float k_scale, float v_scale,
                                  int32_t* err_flag) {
+  griddep_launch_dependents();  // a decode launched as a dependent may be scheduled behind this grid
   const int t = blockIdx.x, h = blockIdx.y;
   const int64_t slot = __ldg(slot_mapping + t);
   if (slot < 0) return;  // padding token
@@ -469,9 +471,8 @@ cudaError_t launch_decode_fp8(int head_size, const CUtensorMap& tk, const CUtens
   if (e != cudaSuccess) return e;
   const long long items = (long long)p.num_seqs * p.num_kv_heads * p.head_groups * p.pmax;
   if (items == 0) return cudaSuccess;
-  kernel<<<(unsigned)items, S::THREADS, S::SMEM_BYTES, stream>>>(tk, tk32, static_cast<const uint8_t*>(v_cache),
-                                                                  p, k_scale, v_scale);
-  return cudaGetLastError();
+  return launch_dependent(kernel, dim3((unsigned)items), dim3(S::THREADS), S::SMEM_BYTES, stream, tk, tk32,
+                          static_cast<const uint8_t*>(v_cache), p, k_scale, v_scale);
 }
 
 cudaError_t launch_reshape_and_cache_fp8(void* k_cache, void* v_cache, const void* key, const void* value,

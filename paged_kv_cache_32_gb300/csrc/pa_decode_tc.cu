@@ -230,6 +230,7 @@ __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
                      const DecodeParams p) {
   using S = Shape<D, NW, NS>;
   griddep_launch_dependents();  // the partition merge may be scheduled behind this grid's last CTAs
+  griddep_wait();               // launched as a dependent: the previous kernel's writes are visible from here
   Item it;
   if (!decode_item(p, blockIdx.x, it)) return;  // partition past the end of its sequence
 
@@ -376,8 +377,7 @@ static cudaError_t launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const
   if (e != cudaSuccess) return e;
   const long long items = (long long)p.num_seqs * p.num_kv_heads * p.head_groups * p.pmax;
   if (items == 0) return cudaSuccess;
-  kernel<<<(unsigned)items, S::THREADS, S::SMEM_BYTES, stream>>>(tk, tv, p);
-  return cudaGetLastError();
+  return launch_dependent(kernel, dim3((unsigned)items), dim3(S::THREADS), S::SMEM_BYTES, stream, tk, tv, p);
 }
 
 // Four warps per CTA, two slab buffers per warp (64 KB per CTA at D = 128):

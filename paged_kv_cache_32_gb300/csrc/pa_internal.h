@@ -51,6 +51,28 @@ cudaError_t launch_reshape_and_cache(void* k_cache, void* v_cache, const void* k
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int32_t num_pairs,
                                int32_t num_blocks, int64_t block_bytes, int32_t* err_flag, cudaStream_t stream);
 
+// Launch `kernel` as a programmatic dependent of the kernel before it on `stream`:
+// its CTAs may be scheduled once every CTA of that kernel has executed
+// griddepcontrol.launch_dependents (or exited), so the launch and CTA start-up
+// overlap that kernel's end.  The kernel must execute griddepcontrol.wait before
+// it reads anything the previous kernel writes or writes anything it reads.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                    Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // Host-side helpers of the C ABI (pa_api.cu), shared by the entry points in other files.
 namespace host {
 constexpr int64_t kInt32Max = 2147483647;

@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(kMergeThreads, 5) merge_kernel(const DecodePar
   constexpr int V = D / 32;          // output elements per lane
   __shared__ float s_acc[WPR > 1 ? NWARP : 1][WPR > 1 ? D : 1];
 
+  griddep_launch_dependents();  // the next decode, launched as a dependent, may be scheduled behind this grid
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = warp % WPR;
   const long long row = (long long)blockIdx.x * ROWS + warp / WPR;
@@ -140,35 +141,24 @@ static cudaError_t launch_merge_t(const DecodeParams& p, cudaStream_t stream) {
   const long long rows = (long long)p.num_seqs * p.num_q_heads;
   const int wpr = p.pmax <= 4 ? 1 : p.pmax <= 8 ? 2 : p.pmax <= 16 ? 4 : 8;
   const long long per_cta = (kMergeThreads / 32) / wpr;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((rows + per_cta - 1) / per_cta));
-  cfg.blockDim = dim3(kMergeThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  const dim3 grid((unsigned)((rows + per_cta - 1) / per_cta)), block(kMergeThreads);
   switch (wpr) {
-    case 1: return cudaLaunchKernelEx(&cfg, merge_kernel<T, D, 1>, p);
-    case 2: return cudaLaunchKernelEx(&cfg, merge_kernel<T, D, 2>, p);
-    case 4: return cudaLaunchKernelEx(&cfg, merge_kernel<T, D, 4>, p);
-    default: return cudaLaunchKernelEx(&cfg, merge_kernel<T, D, 8>, p);
+    case 1: return launch_dependent(merge_kernel<T, D, 1>, grid, block, 0, stream, p);
+    case 2: return launch_dependent(merge_kernel<T, D, 2>, grid, block, 0, stream, p);
+    case 4: return launch_dependent(merge_kernel<T, D, 4>, grid, block, 0, stream, p);
+    default: return launch_dependent(merge_kernel<T, D, 8>, grid, block, 0, stream, p);
   }
 }
 
 cudaError_t launch_merge(int dtype, int head_size, const DecodeParams& p, cudaStream_t stream) {
   if ((long long)p.num_seqs * p.num_q_heads == 0) return cudaSuccess;
-  cudaError_t e;
-  if (dtype == PA_F32 && head_size == 64) e = launch_merge_t<float, 64>(p, stream);
-  else if (dtype == PA_F32 && head_size == 128) e = launch_merge_t<float, 128>(p, stream);
-  else if (dtype == PA_F16 && head_size == 64) e = launch_merge_t<__half, 64>(p, stream);
-  else if (dtype == PA_F16 && head_size == 128) e = launch_merge_t<__half, 128>(p, stream);
-  else if (dtype == PA_BF16 && head_size == 64) e = launch_merge_t<__nv_bfloat16, 64>(p, stream);
-  else if (dtype == PA_BF16 && head_size == 128) e = launch_merge_t<__nv_bfloat16, 128>(p, stream);
-  else return cudaErrorInvalidValue;
-  return e != cudaSuccess ? e : cudaGetLastError();
+  if (dtype == PA_F32 && head_size == 64) return launch_merge_t<float, 64>(p, stream);
+  if (dtype == PA_F32 && head_size == 128) return launch_merge_t<float, 128>(p, stream);
+  if (dtype == PA_F16 && head_size == 64) return launch_merge_t<__half, 64>(p, stream);
+  if (dtype == PA_F16 && head_size == 128) return launch_merge_t<__half, 128>(p, stream);
+  if (dtype == PA_BF16 && head_size == 64) return launch_merge_t<__nv_bfloat16, 64>(p, stream);
+  if (dtype == PA_BF16 && head_size == 128) return launch_merge_t<__nv_bfloat16, 128>(p, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pa
