@@ -122,6 +122,12 @@ enum {
  *   workspace    device scratch of at least pa_decode_workspace_size(...) bytes,
  *                256-byte aligned; may be NULL when that size is 0.
  *   err_flag     nullable device int32 (see above).
+ *   Launches: the decode kernel, then (when a sequence spans two partitions) the
+ *   merge kernel, both with programmatic stream serialization.  Their CTAs may be
+ *   scheduled while the kernel before them on `stream` finishes, but each executes
+ *   griddepcontrol.wait before it reads or writes any memory, so stream order holds
+ *   as for a plain launch; stream capture records the dependencies as programmatic
+ *   edges.
  */
 int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
               const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,

@@ -32,7 +32,7 @@
 namespace pa {
 
 constexpr int kMergeThreads = 256;
-constexpr int KPRE = 4;  // partitions per warp whose outputs are loaded before the weights are known
+constexpr int kMergePreload = 4;  // partitions per warp whose outputs are loaded before the weights are known
 
 template <int V>
 __device__ __forceinline__ void load_vec(const float* src, float (&v)[V]) {
@@ -82,10 +82,10 @@ __global__ void __launch_bounds__(kMergeThreads, 5) merge_kernel(const DecodePar
   if (nparts > 1) {  // a single partition was written out by the decode kernel
     const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + (size_t)row * p.pmax;  // (m_p, l_p)
     const float* os = p.ws_o + (size_t)row * p.pmax * D + lane * V;
-    // One round trip: this warp's first KPRE partial outputs and lane i's pair (m_i, l_i).
-    float pre[KPRE][V];
+    // One round trip: this warp's first kMergePreload partial outputs and lane i's pair (m_i, l_i).
+    float pre[kMergePreload][V];
 #pragma unroll
-    for (int k = 0; k < KPRE; ++k)
+    for (int k = 0; k < kMergePreload; ++k)
       if (sub + k * WPR < nparts) load_vec<V>(os + (size_t)(sub + k * WPR) * D, pre[k]);
     const float2 own = lane < nparts ? ml[lane] : make_float2(-INFINITY, 0.f);
     float mx = own.x;
@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(kMergeThreads, 5) merge_kernel(const DecodePar
       }
     }
 #pragma unroll
-    for (int k = 0; k < KPRE; ++k) {
+    for (int k = 0; k < kMergePreload; ++k) {
       if (sub + k * WPR < nparts) {
         const float w = partition_weight(sub + k * WPR, w_own, ml, mx);
 #pragma unroll
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kMergeThreads, 5) merge_kernel(const DecodePar
       }
     }
 #pragma unroll 4
-    for (int i = sub + KPRE * WPR; i < nparts; i += WPR) {
+    for (int i = sub + kMergePreload * WPR; i < nparts; i += WPR) {
       const float w = partition_weight(i, w_own, ml, mx);
       float o[V];
       load_vec<V>(os + (size_t)i * D, o);
