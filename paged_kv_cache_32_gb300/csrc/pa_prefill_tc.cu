@@ -654,19 +654,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool unmasked = __all_sync(0xffffffffu, min(lim0, lim1) >= kt * kTile + kTile - 1);
       // ---- the rows' tile maxima, and the reference maxima they imply
       float a0 = -INFINITY, b0 = -INFINITY, a1 = -INFINITY, b1 = -INFINITY;  // two chains per row
-      if (unmasked) {
 #pragma unroll
-        for (int j = 0; j < 16; j += 2) {
-          a0 = max3(a0, v[4 * j], v[4 * j + 1]);
-          a1 = max3(a1, v[4 * j + 2], v[4 * j + 3]);
-          b0 = max3(b0, v[4 * j + 4], v[4 * j + 5]);
-          b1 = max3(b1, v[4 * j + 6], v[4 * j + 7]);
-        }
-      } else {
+      for (int j = 0; j < 16; j += 2) {
+        a0 = max3(a0, v[4 * j], v[4 * j + 1]);
+        a1 = max3(a1, v[4 * j + 2], v[4 * j + 3]);
+        b0 = max3(b0, v[4 * j + 4], v[4 * j + 5]);
+        b1 = max3(b1, v[4 * j + 6], v[4 * j + 7]);
+      }
+      if (!unmasked) {
+        // The maxima over all 128 keys bound the visible keys' maxima from above.  A bound that moves
+        // no row's reference max decides as the visible maxima would, so those are taken only when
+        // the bound would move one (rare after an item's first tiles).
+        float u0 = fmaxf(a0, b0), u1 = fmaxf(a1, b1);
+        u0 = fmaxf(u0, __shfl_xor_sync(0xffffffffu, u0, 1));
+        u1 = fmaxf(u1, __shfl_xor_sync(0xffffffffu, u1, 1));
+        u0 = fmaxf(u0, __shfl_xor_sync(0xffffffffu, u0, 2));
+        u1 = fmaxf(u1, __shfl_xor_sync(0xffffffffu, u1, 2));
+        if (__any_sync(0xffffffffu, u0 * sl2 > m0 + kRescaleThreshold || u1 * sl2 > m1 + kRescaleThreshold)) {
+          a0 = b0 = a1 = b1 = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          a0 = max3(a0, 8 * j <= e0 ? v[4 * j] : -INFINITY, 8 * j + 1 <= e0 ? v[4 * j + 1] : -INFINITY);
-          a1 = max3(a1, 8 * j <= e1 ? v[4 * j + 2] : -INFINITY, 8 * j + 1 <= e1 ? v[4 * j + 3] : -INFINITY);
+          for (int j = 0; j < 16; j += 2) {
+            a0 = max3(a0, 8 * j <= e0 ? v[4 * j] : -INFINITY, 8 * j + 1 <= e0 ? v[4 * j + 1] : -INFINITY);
+            a1 = max3(a1, 8 * j <= e1 ? v[4 * j + 2] : -INFINITY, 8 * j + 1 <= e1 ? v[4 * j + 3] : -INFINITY);
+            b0 = max3(b0, 8 * j + 8 <= e0 ? v[4 * j + 4] : -INFINITY, 8 * j + 9 <= e0 ? v[4 * j + 5] : -INFINITY);
+            b1 = max3(b1, 8 * j + 8 <= e1 ? v[4 * j + 6] : -INFINITY, 8 * j + 9 <= e1 ? v[4 * j + 7] : -INFINITY);
+          }
         }
       }
       a0 = fmaxf(a0, b0);
