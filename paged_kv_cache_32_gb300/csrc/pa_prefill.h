@@ -24,8 +24,8 @@ struct PrefillParams {
 };
 
 // tk, tv: the caches as rows of D elements (box 64 columns x block_size rows, 128-byte swizzle);
-// tq: q as [tokens][heads][D] (box 64 columns x 1 head x 128 tokens, 128-byte swizzle)
+// tq: q as [tokens][heads][D] (box 64 columns x 1 head x 128 tokens, 128-byte swizzle); to: out, the same
 cudaError_t launch_prefill_tc(int dtype, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
-                              const PrefillParams& p, cudaStream_t stream);
+                              const CUtensorMap& to, const PrefillParams& p, cudaStream_t stream);
 
 }  // namespace pa

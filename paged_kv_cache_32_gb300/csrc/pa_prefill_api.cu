@@ -40,12 +40,12 @@ int pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cach
 
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return PA_ERR_CUDA;
-  CUtensorMap tk, tv, tq;
+  CUtensorMap tk, tv, tq, to;
   if (!encode_cache_map(&tk, k_cache, cache, cache->block_size) ||
       !encode_cache_map(&tv, v_cache, cache, cache->block_size))
     return PA_ERR_CUDA;
   {
-    // q [tokens][heads][D]: a 128-token tile of one head is one box of 64 columns x 1 x 128 per half
+    // q and out [tokens][heads][D]: a 128-token tile of one head is one box of 64 columns x 1 x 128 per half
     cuuint64_t dims[3] = {(cuuint64_t)cache->head_size, (cuuint64_t)num_q_heads, (cuuint64_t)num_query_tokens};
     cuuint64_t strides[2] = {(cuuint64_t)cache->head_size * 2, (cuuint64_t)num_q_heads * cache->head_size * 2};
     cuuint32_t box[3] = {64, 1, 128};
@@ -54,7 +54,9 @@ int pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cach
         cache->dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     if (enc(&tq, dt, 3, const_cast<void*>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        enc(&to, dt, 3, out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return PA_ERR_CUDA;
   }
   pa::PrefillParams p;
@@ -75,7 +77,7 @@ int pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cach
   p.q_tiles = (int32_t)q_tiles;
   p.num_query_tokens = num_query_tokens;
   p.scale_log2 = scale * 1.4426950408889634f;
-  cudaError_t e = pa::launch_prefill_tc(cache->dtype, tk, tv, tq, p, static_cast<cudaStream_t>(stream));
+  cudaError_t e = pa::launch_prefill_tc(cache->dtype, tk, tv, tq, to, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

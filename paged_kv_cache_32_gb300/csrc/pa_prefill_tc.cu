@@ -53,8 +53,13 @@
 //  * Rescaling: a row's reference max moves only when the tile max exceeds it
 //    by more than 8 (log2 units), so P <= 2^8 and O is rescaled in place
 //    (tcgen05.ld / st of the warp's 16 rows) on few tiles.
-//  * Epilogue: each warp normalises its 16 rows (out = O / l) straight from
-//    the 16x256b layout, after releasing O to the next item's first P V.
+//  * Epilogue: each warp reads its 16 rows of O (16x256b layout), releases O
+//    to the next item's first P V and normalises them (out = O / l).  bf16
+//    stores them from registers.  fp16, whose softmax warps set the pace,
+//    writes them into a 32 KB shared-memory stage in the output tensor map's
+//    swizzled layout; the P V issuer then stores a full tile with two
+//    tensor-map stores, and a ragged tile (rows past the chunk belong to
+//    another sequence) is copied out row by row by its warps.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -77,7 +82,8 @@ constexpr int kHalf = kTile * 128;    // one 128-row x 128-byte swizzled region 
 constexpr int kKOff = 0;              // K stages: 2 x 2 regions (dims 0-63, 64-127)
 constexpr int kVOff = 4 * kHalf;      // V stages: 2 x 2 regions
 constexpr int kQOff = 8 * kHalf;      // Q tiles of two items (item k in buffer k % 2): 2 x 2 regions
-constexpr int kBarOff = 12 * kHalf;   // barriers, flags, the published work items
+constexpr int kOutOff = 12 * kHalf;   // one item's output tile, staged for a tensor-map store: 2 regions
+constexpr int kBarOff = 14 * kHalf;   // barriers, flags, the published work items
 constexpr int kSmemBytes = kBarOff + 512 + 1024;
 constexpr int kSBufs = 3;             // S buffers in tensor memory (columns 128 b .. 128 b + 127)
 constexpr uint32_t kOCol = 384;       // tensor-memory column of O
@@ -95,6 +101,13 @@ template <typename T>
 constexpr bool split_p() {
   return std::is_same<T, __nv_bfloat16>::value;
 }
+
+// Where the epilogue writes the output tile.  fp16 (softmax-bound): to a shared-memory stage that the P V
+// issuer sends out with two tensor-map stores, which takes the global stores off the softmax warps.  bf16
+// (tensor-bound): straight from registers; its copies keep the tensor-memory-access unit busy, and the
+// stores through it cost more than the softmax time they save (measured 3.9% slower).
+template <typename T>
+constexpr bool kStagedOut = !split_p<T>();
 
 // try_wait that lets the hardware park the thread (up to ~20 us) until the phase completes,
 // instead of spinning on the barrier and taking issue slots from the softmax warps
@@ -375,7 +388,8 @@ __device__ __forceinline__ bool pf_item(const PrefillParams& p, int idx, PfItem&
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                      const __grid_constant__ CUtensorMap tmap_q, const PrefillParams p) {
+                      const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_out,
+                      const PrefillParams p) {
   const int n_items = p.num_seqs * p.num_q_heads * p.q_tiles;
   const int B = p.block_size;
   const int blocks_per_tile = kTile / B;
@@ -394,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_done = bar_q + 14;  // every P V of the item done (one phase per item)
   uint64_t* bar_ofree = bar_q + 15; // the item's epilogue has read O (one phase per item)
   uint64_t* bar_qs = bar_q + 16;    // item k published and its Q tile in shared memory (phase k)
+  uint64_t* bar_staged = bar_q + 17; // the item's output tile written to the stage (or stored) (phase per item)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 192);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 200);
   PfItem* items = reinterpret_cast<PfItem*>(smem + kBarOff + 256);  // [2] published items (s < 0: none left)
@@ -416,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_done, 1);
     mbar_init(bar_ofree, kSoftmaxWarps);
     mbar_init(bar_qs, 1);
+    mbar_init(bar_staged, kSoftmaxWarps);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -588,6 +604,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_o = idesc<T>(1);
       bool ok = true;
       int tg = 0, item_no = 0;
+      int prev_row0 = 0, prev_h = 0;  // the previous item's output tile
+      bool prev_full = false;
+      // The previous item's output, once every softmax warp has staged (or, ragged, written) its rows:
+      // two tensor-map stores of a full tile (the barrier's next phase needs this item's bar_done, which
+      // this thread arrives on later, so the wait is exact).
+      auto store_prev = [&]() {
+        if constexpr (!kStagedOut<T>) return;
+        ok = wait_bar_spin(bar_staged, (item_no - 1) & 1, abort_flag);
+        if (ok && prev_full) {
+          tma_store_3d(&tmap_out, 0, prev_h, prev_row0, smem + kOutOff);
+          tma_store_3d(&tmap_out, 64, prev_h, prev_row0, smem + kOutOff + kHalf);
+          bulk_commit_group();
+        }
+      };
       for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
         PfItem it;
         if (!pf_item(p, idx, it, false)) continue;
@@ -612,13 +642,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(&bar_o[buf]);
           ++n_o;
+          // the previous item's store, a few tiles into this item: clear of the copies that start an item
+          if (kt == min(2, it.key_tiles - 1) && item_no > 0) store_prev();
         }
         // the item's last P V has finished: O is complete (the buffer barrier's previous phase finished
         // before the S that fed this P; its next phase needs a P V not yet issued, so the wait is exact)
         if (ok) ok = wait_bar_spin(&bar_o[(tg - 1) % kSBufs], ((tg - 1) / kSBufs) & 1, abort_flag);
+        // the stage may take this item's output once the previous item's store has read it
+        if constexpr (kStagedOut<T>) bulk_wait_group_read0();
         if (ok) mbar_arrive(bar_done);
+        prev_row0 = it.q0 + it.tile0;
+        prev_h = it.h;
+        prev_full = it.rows == kTile;
         ++item_no;
       }
+      if (ok && item_no > 0) store_prev();
+      if constexpr (kStagedOut<T>) bulk_wait_group0();  // the output is written before the CTA ends
     }
     __syncwarp();
   } else {
@@ -759,7 +798,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       //      P V waits for this item's epilogue to have read O, so it runs before the epilogue, beside
       //      this item's last P V.
       // (what the epilogue needs of this item is kept apart, and the next item becomes the current one)
-      T* out0 = reinterpret_cast<T*>(p.out) + ((size_t)(it.q0 + it.tile0 + r0) * p.num_q_heads + it.h) * kD;
+      const int orow0 = it.q0 + it.tile0, oh = it.h;  // the tile's first output row, and its head
+      T* out0 = reinterpret_cast<T*>(p.out) + ((size_t)(orow0 + r0) * p.num_q_heads + oh) * kD;  // row r0
       const int rows = it.rows;
       ok = warp_wait(bar_qs, (item_no + 1) & 1);
       it = items[(item_no + 1) & 1];
@@ -778,34 +818,70 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ofree);
       const float inv0 = s0 > 0.f ? 1.f / s0 : 0.f, inv1 = s1 > 0.f ? 1.f / s1 : 0.f;
-      // Thread c of a quad holds packed word j of a row for columns 8j + 2c, 8j + 2c + 1.  A 4 x 4 word
-      // transpose within the quad (two xor-shuffle steps per group of 4 j) gives thread c the 16 bytes
-      // of columns 8j .. 8j + 7 for j = 4g + c, so a store writes 16 bytes per thread and 64
-      // contiguous bytes per row and quad.
-      T* out1 = out0 + (size_t)8 * p.num_q_heads * kD;  // row r1 = r0 + 8
-      const bool hi2 = (c4 >> 1) != 0, odd = (c4 & 1) != 0;
+      if constexpr (kStagedOut<T>) {
+        // The tile goes to the stage, in the 128-byte-swizzled layout of the output's tensor map (row r's
+        // 16-byte chunk k of column half h at h * kHalf + swz128(r, k)).  Thread c of a quad writes bytes
+        // 4c .. 4c + 3 of each chunk, so the eight rows and four threads of a store fall in 32 banks.
+        uint8_t* stage = smem + kOutOff;
 #pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const float inv = rr ? inv1 : inv0;
+        for (int j = 0; j < 16; ++j) {
+          uint8_t* col = stage + (j >> 3) * kHalf + 4 * c4;
+          *reinterpret_cast<uint32_t*>(col + swz128(r0, j & 7)) =
+              Mma<T>::pack(o[4 * j] * inv0, o[4 * j + 1] * inv0);
+          *reinterpret_cast<uint32_t*>(col + swz128(r1, j & 7)) =
+              Mma<T>::pack(o[4 * j + 2] * inv1, o[4 * j + 3] * inv1);
+        }
+        if (rows == kTile) {
+          // a full tile: the P V issuer stores it once every softmax warp has written its rows
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> the tensor-map store
+        } else {
+          // a ragged tile (the last of a chunk): its rows past the chunk belong to another sequence, so this
+          // warp copies its own rows inside the chunk out, 16 lanes per 256-byte row
+          __syncwarp();
+          const int row_base = r0 - (lane >> 2);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint32_t w[4];
+          for (int i = 0; i < 8; ++i) {
+            const int rl = 2 * i + (lane >> 4), chunk = lane & 15;  // row row_base + rl, bytes 16 chunk ..
+            const int r = row_base + rl;
+            if (r < rows) {
+              const uint4 v = *reinterpret_cast<const uint4*>(stage + (chunk >> 3) * kHalf + swz128(r, chunk & 7));
+              T* dst = reinterpret_cast<T*>(p.out) + ((size_t)(orow0 + r) * p.num_q_heads + oh) * kD + 8 * chunk;
+              *reinterpret_cast<uint4*>(dst) = v;
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_staged);
+      } else {
+        // Thread c of a quad holds packed word j of a row for columns 8j + 2c, 8j + 2c + 1.  A 4 x 4 word
+        // transpose within the quad (two xor-shuffle steps per group of 4 j) gives thread c the 16 bytes
+        // of columns 8j .. 8j + 7 for j = 4g + c, so a store writes 16 bytes per thread and 64
+        // contiguous bytes per row and quad.
+        T* out1 = out0 + (size_t)8 * p.num_q_heads * kD;  // row r1 = r0 + 8
+        const bool hi2 = (c4 >> 1) != 0, odd = (c4 & 1) != 0;
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            w[i] = Mma<T>::pack(o[4 * (4 * g + i) + 2 * rr] * inv, o[4 * (4 * g + i) + 2 * rr + 1] * inv);
-          // step 1 (lanes c, c ^ 2): the upper pair of words of threads 0, 1 swaps with the lower pair of 2, 3
-          const uint32_t x0 = __shfl_xor_sync(0xffffffffu, hi2 ? w[0] : w[2], 2);
-          const uint32_t x1 = __shfl_xor_sync(0xffffffffu, hi2 ? w[1] : w[3], 2);
-          if (hi2) w[0] = x0, w[1] = x1;
-          else w[2] = x0, w[3] = x1;
-          // step 2 (lanes c, c ^ 1): within each pair of words, an odd word of an even thread swaps with an
-          // even word of an odd thread
-          const uint32_t y0 = __shfl_xor_sync(0xffffffffu, odd ? w[0] : w[1], 1);
-          const uint32_t y1 = __shfl_xor_sync(0xffffffffu, odd ? w[2] : w[3], 1);
-          if (odd) w[0] = y0, w[2] = y1;
-          else w[1] = y0, w[3] = y1;
-          if ((rr ? r1 : r0) < rows)
-            *reinterpret_cast<uint4*>((rr ? out1 : out0) + 8 * (4 * g + c4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int rr = 0; rr < 2; ++rr) {
+          const float inv = rr ? inv1 : inv0;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              w[i] = Mma<T>::pack(o[4 * (4 * g + i) + 2 * rr] * inv, o[4 * (4 * g + i) + 2 * rr + 1] * inv);
+            // step 1 (lanes c, c ^ 2): the upper pair of words of threads 0, 1 swaps with the lower pair of 2, 3
+            const uint32_t x0 = __shfl_xor_sync(0xffffffffu, hi2 ? w[0] : w[2], 2);
+            const uint32_t x1 = __shfl_xor_sync(0xffffffffu, hi2 ? w[1] : w[3], 2);
+            if (hi2) w[0] = x0, w[1] = x1;
+            else w[2] = x0, w[3] = x1;
+            // step 2 (lanes c, c ^ 1): within each pair of words, an odd word of an even thread swaps with an
+            // even word of an odd thread
+            const uint32_t y0 = __shfl_xor_sync(0xffffffffu, odd ? w[0] : w[1], 1);
+            const uint32_t y1 = __shfl_xor_sync(0xffffffffu, odd ? w[2] : w[3], 1);
+            if (odd) w[0] = y0, w[2] = y1;
+            else w[1] = y0, w[3] = y1;
+            if ((rr ? r1 : r0) < rows)
+              *reinterpret_cast<uint4*>((rr ? out1 : out0) + 8 * (4 * g + c4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
         }
       }
       ++item_no;
@@ -833,7 +909,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // one CTA per SM (the kernel holds all of tensor memory and most of shared memory), at most one per item
 cudaError_t launch_prefill_tc(int dtype, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
-                              const PrefillParams& p, cudaStream_t stream) {
+                              const CUtensorMap& to, const PrefillParams& p, cudaStream_t stream) {
   const long long items = (long long)p.num_seqs * p.num_q_heads * p.q_tiles;
   if (items == 0) return cudaSuccess;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -845,12 +921,12 @@ cudaError_t launch_prefill_tc(int dtype, const CUtensorMap& tk, const CUtensorMa
   if (dtype == PA_F16) {
     e = cudaFuncSetAttribute(prefill_tc_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<__half><<<grid, kThreads, kSmemBytes, stream>>>(tk, tv, tq, p);
+    prefill_tc_kernel<__half><<<grid, kThreads, kSmemBytes, stream>>>(tk, tv, tq, to, p);
   } else if (dtype == PA_BF16) {
     e = cudaFuncSetAttribute(prefill_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes);
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, stream>>>(tk, tv, tq, p);
+    prefill_tc_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, stream>>>(tk, tv, tq, to, p);
   } else {
     return cudaErrorInvalidValue;
   }

@@ -207,12 +207,15 @@ def test_prefill_empty_chunks_and_grid_slack():
     assert_close(got, oracle_prefill(w, k, v), "f16", w.name)
 
 
-def test_prefill_inconsistent_chunk_reported_and_skipped():
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_prefill_inconsistent_chunk_reported_and_skipped(dtype):
     """A chunk longer than its sequence (L < n) is reported as
     PA_DEVERR_QUERY; its rows keep their old contents and the other sequences
-    are still computed."""
+    are still computed.  The chunk before it ends in a ragged query tile, whose
+    rows past that chunk (the skipped chunk's) must not be written: fp16 writes
+    that tile through its shared-memory stage, bf16 from registers."""
     import torch
-    w = small("bf16", 16)
+    w = small(dtype, 16)
     g = PrefillStep(w)
     bad = 2
     lens = w.seq_lens.copy()
@@ -225,7 +228,7 @@ def test_prefill_inconsistent_chunk_reported_and_skipped():
     rows = np.arange(w.query_start[bad], w.query_start[bad + 1])
     assert np.all(got[rows] == SENTINEL)
     keep = np.setdiff1d(np.arange(len(got)), rows)
-    assert_close(got[keep], ref[keep], "bf16", "other sequences")
+    assert_close(got[keep], ref[keep], dtype, "other sequences")
 
 
 def test_prefill_bad_block_id_reported():
