@@ -152,6 +152,11 @@ def test_prefill_step_graph_replay_matches_eager(dtype):
     torch.cuda.synchronize()
     assert int(eager.err.item()) == 0
     assert eager.out.dtype == tdt
+    # the eager call against the oracle (the last chunk ends with a full tile at the end of out)
+    from test_gpu_prefill import host_pools, oracle_prefill
+    k, v = host_pools(w)
+    ok, err, ratio = within_bound(out_f64(eager.out), oracle_prefill(w, k, v), dtype)
+    assert ok, f"eager prefill: max abs err {err}, worst err/bound {ratio}"
 
     g = Step()
     side = torch.cuda.Stream()
