@@ -16,9 +16,10 @@
  *       sequence, head and partition; partition reduction for long contexts).
  *
  * Conventions shared by every call
- *  - All data pointers are DEVICE pointers owned by the caller.  The library
- *    allocates no memory and keeps no state between calls except a lazily
- *    resolved driver entry point and per-kernel launch attributes.
+ *  - All data pointers are DEVICE pointers owned by the caller.  No call
+ *    allocates memory.  Between calls the library keeps only a lazily resolved
+ *    driver entry point, per-kernel launch attributes and, for
+ *    pa_decode_noalloc alone, one fixed scratch array per device (see there).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Every call is asynchronous on that stream.
  *  - Cache layout (both K and V): [num_blocks][num_kv_heads][block_size][head_size],
@@ -27,10 +28,12 @@
  *  - Return value: PA_OK, or a PA_ERR_* code for an argument error detected on
  *    the host, in which case NOTHING is launched; PA_ERR_CUDA if a launch failed.
  *  - Data errors (a bad block ID or slot inside device arrays) are detected on
- *    the device.  The offending item is skipped (never read or written out of
- *    bounds); if `err_flag` is non-NULL the first error code (PA_DEVERR_*) is
- *    stored there with an atomic compare-and-swap from 0.  `err_flag` is a
- *    device int32 the caller zeroes.
+ *    the device, always: there is no switch that turns the checks off (each is
+ *    one integer compare per block or slot, next to a memory access).  The
+ *    offending item is skipped (never read or written out of bounds); if
+ *    `err_flag` is non-NULL the first error code (PA_DEVERR_*) is stored there
+ *    with an atomic compare-and-swap from 0.  `err_flag` is a device int32 the
+ *    caller zeroes.
  */
 #ifndef PA_H_
 #define PA_H_
@@ -143,11 +146,23 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
  *                 bias towards the query's own position: score_i of head h gains
  *                 alibi_slopes[h] * (i - (seq_lens[s] - 1)).
  *   k_scale, v_scale  the dequantisation scales of an FP8 cache (pa_decode uses 1).
+ *   test_flags    0 in normal use.  PA_DECODE_TEST_EXPIRE_FIRST_WAIT exists for
+ *                 tests of the kernels' hang protection (every wait on an
+ *                 asynchronous copy is bounded, and an expired wait ends the
+ *                 work item with PA_DEVERR_TIMEOUT once the copies already in
+ *                 flight have landed): the f16/bf16/fp8 kernels then never
+ *                 request the first slab of each warp's ring and bound the wait
+ *                 for it at 20000 cycles, so it expires.  The call reports
+ *                 PA_DEVERR_TIMEOUT in *err_flag and its output is undefined;
+ *                 later calls are unaffected.  Ignored for fp32 caches, which
+ *                 do not wait.
  */
+#define PA_DECODE_TEST_EXPIRE_FIRST_WAIT 1u
 typedef struct {
   const float* alibi_slopes;
   float k_scale; /* FP8 caches only (> 0); 0 means 1.  Ignored for other dtypes. */
   float v_scale; /* FP8 caches only (> 0); 0 means 1.  Ignored for other dtypes. */
+  uint32_t test_flags; /* 0, or PA_DECODE_TEST_EXPIRE_FIRST_WAIT (tests only) */
 } pa_decode_options;
 
 int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
@@ -191,8 +206,8 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t m
  *   reported; a bad block ID gives PA_DEVERR_BLOCK_ID and that sequence's
  *   output is undefined.
  *   Supported: dtype f16 / bf16, head_size 128, block_size 16, 32, 64 or 128.
- *   Runs on the tcgen05 tensor cores (one CTA per sequence, query head and tile
- *   of 128 queries).
+ *   Runs on the tcgen05 tensor cores: a persistent kernel, one CTA per SM,
+ *   whose CTAs walk the work items (sequence, query head, tile of 128 queries).
  */
 int pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
                const int32_t* seq_lens, const int32_t* query_start, int32_t num_seqs, int32_t num_query_tokens,
@@ -246,12 +261,21 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pairs, int
  *
  *   Same arguments and results as pa_decode, without workspace: the split-KV
  *   scratch is a library-owned device array of PA_NOALLOC_MAX_WORKSPACE_BYTES
- *   bytes, which every GPU that loads the library holds until the process
- *   exits.  Sizes whose pa_decode_workspace_size() exceeds that limit return
- *   PA_ERR_WORKSPACE and launch nothing.  The call allocates nothing.
- *   - The first call on a device looks up the array's device address (with that
- *     device current) and caches it; make that first call before any stream
- *     capture.  It returns PA_ERR_CUDA if the lookup fails.
+ *   bytes.  Sizes whose pa_decode_workspace_size() exceeds that limit return
+ *   PA_ERR_WORKSPACE and launch nothing.  The call itself allocates nothing.
+ *   - Which sizes fit: the workspace is num_seqs * num_q_heads * P_max *
+ *     (head_size + 2) * 4 bytes.  At the default 1024-token partition, 64
+ *     sequences x 32 heads of up to 2048 tokens need 2.1 MB and 128 x 32 heads
+ *     of up to 1280 tokens 4.3 MB; 8 sequences x 32 heads of 32768 tokens in
+ *     512-token partitions need 8.5 MB.  128 sequences x 64 query heads of up to
+ *     4096 tokens need 17.0 MB, over the limit: pass partition_size 2048
+ *     (8.5 MB) for them.  Sequences that fit one partition need none.
+ *   - The first call on a device, whatever its sizes, looks up the array's
+ *     device address with that device current and caches it.  Under CUDA's lazy
+ *     module loading (the default) that lookup is also when the array is
+ *     committed on the device, where it then stays until the process exits.
+ *     Make that first call before any stream capture and outside any
+ *     latency-critical loop.  It returns PA_ERR_CUDA if the lookup fails.
  *   - All calls share the one array and it keeps the previous call's contents;
  *     nothing in it needs clearing, but calls that overlap on the GPU (other
  *     streams, other host threads) race on it: order them on one stream.

@@ -27,8 +27,12 @@ EXPORTED = ("pa_decode", "pa_decode_ex", "pa_decode_partition_size", "pa_decode_
             "pa_reshape_and_cache_fp8")
 
 
+PA_DECODE_TEST_EXPIRE_FIRST_WAIT = 1
+
+
 class pa_decode_options(ctypes.Structure):
-    _fields_ = [("alibi_slopes", ctypes.c_void_p), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
+    _fields_ = [("alibi_slopes", ctypes.c_void_p), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
+                ("test_flags", ctypes.c_uint32)]
 
 
 class pa_cache_desc(ctypes.Structure):
@@ -157,7 +161,8 @@ def pa_decode_workspace_size(num_seqs: int, num_q_heads: int, max_blocks_per_seq
 
 def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale: float, partition_size: int = 0,
               workspace=None, err_flag=None, stream=None, desc: pa_cache_desc | None = None,
-              alibi_slopes=None, k_scale: float | None = None, v_scale: float | None = None) -> None:
+              alibi_slopes=None, k_scale: float | None = None, v_scale: float | None = None,
+              test_flags: int = 0) -> None:
     """out[s, h] = softmax(scale * q[s, h] K_s^T) V_s over seq_lens[s] paged tokens.
 
     out, q: [num_seqs, num_q_heads, head_size] (cache dtype); block_tables: int32
@@ -166,6 +171,7 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale: float, pa
     and one is needed, it is allocated with torch.  ``alibi_slopes``: optional
     float32 device tensor [num_q_heads] (calls pa_decode_ex).  ``k_scale`` /
     ``v_scale``: dequantisation scales of an FP8 cache (q and out are fp16 then).
+    ``test_flags``: 0, or PA_DECODE_TEST_EXPIRE_FIRST_WAIT in tests of the bounded waits.
     """
     desc = desc or cache_desc(k_cache)
     for t, n in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"),
@@ -181,11 +187,11 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale: float, pa
     args = (_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(seq_lens), num_seqs,
             num_q_heads, max_blocks, ctypes.byref(desc), float(scale), int(partition_size), _ptr(workspace), ws_bytes,
             _ptr(err_flag), _stream(stream))
-    if alibi_slopes is None and k_scale is None and v_scale is None:
+    if alibi_slopes is None and k_scale is None and v_scale is None and not test_flags:
         _check(lib().pa_decode(*args), "pa_decode")
     else:
         _dense(alibi_slopes, "alibi_slopes")
-        opts = pa_decode_options(_ptr(alibi_slopes), float(k_scale or 0.0), float(v_scale or 0.0))
+        opts = pa_decode_options(_ptr(alibi_slopes), float(k_scale or 0.0), float(v_scale or 0.0), int(test_flags))
         _check(lib().pa_decode_ex(*args, ctypes.byref(opts)), "pa_decode_ex")
 
 

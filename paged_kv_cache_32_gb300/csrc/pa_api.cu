@@ -111,7 +111,7 @@ using namespace pa::host;
 
 extern "C" {
 
-int pa_version(void) { return 100; }
+int pa_version(void) { return 10100; }
 
 const char* pa_status_string(int status) {
   switch (status) {
@@ -211,6 +211,8 @@ int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_ca
   p.pmax = pmax;
   p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
   p.alibi = alibi;
+  p.test_expire_first_wait =
+      (options != nullptr && (options->test_flags & PA_DECODE_TEST_EXPIRE_FIRST_WAIT) != 0u) ? 1 : 0;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;

@@ -52,6 +52,7 @@ namespace pa {
 namespace {
 
 constexpr long long kWaitCyclesFp8 = 500ll * 1000 * 1000;  // bound on one wait: ~0.25 s at 2 GHz
+constexpr long long kTestWaitCyclesFp8 = 20000;              // the test hook's bound on a ring's first wait
 
 template <int D, int NW, int NS>
 struct Fp8Shape {
@@ -118,13 +119,14 @@ __device__ __forceinline__ bool fp8_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-__device__ __forceinline__ bool fp8_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag) {
+__device__ __forceinline__ bool fp8_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag,
+                                         long long limit) {
   if (fp8_try_wait(bar, parity)) return true;
   const long long start = clock64();
   for (uint32_t i = 0;; ++i) {
     if (fp8_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if ((i & 15u) == 15u && clock64() - start > kWaitCyclesFp8) {
+    if ((i & 15u) == 15u && clock64() - start > limit) {
       *abort_flag = 1;
       return false;
     }
@@ -277,10 +279,8 @@ __global__ void __launch_bounds__(Fp8Shape<D, NW, NS>::THREADS)
   uint8_t* ring = smem + warp * S::RING_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF) + warp * NS;
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + S::FLAG_OFF);
-  volatile int32_t* never_flag = abort_flag + 1;
   if (threadIdx.x == 0) {
     abort_flag[0] = 0;
-    never_flag[0] = 0;
   }
   if (lane == 0) {
     for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
@@ -375,12 +375,16 @@ __global__ void __launch_bounds__(Fp8Shape<D, NW, NS>::THREADS)
   float m_a = -INFINITY, m_b = -INFINITY;
   float l_a = 0.f, l_b = 0.f;
 
+  // test hook (pa_decode_options.test_flags): slab 0 of each ring is never requested and the
+  // first wait has a short bound, so that wait expires and the abort path below runs
+  const int first_issued = p.test_expire_first_wait ? 1 : 0;
   const int prologue = n_my < NS ? n_my : NS;
-  for (int k = 0; k < prologue; ++k) issue(k);
+  for (int k = first_issued; k < prologue; ++k) issue(k);
   int k = 0;
   for (; k < n_my; ++k) {
     const int stage = k % NS;
-    if (!__all_sync(0xffffffffu, fp8_wait(&bars[stage], (k / NS) & 1, abort_flag))) break;
+    const long long limit = (k == 0 && p.test_expire_first_wait) ? kTestWaitCyclesFp8 : kWaitCyclesFp8;
+    if (!__all_sync(0xffffffffu, fp8_wait(&bars[stage], (k / NS) & 1, abort_flag, limit))) break;
     if ((valid_mask >> stage) & 1u) {
       const int tok0 = sub_tok(k, 0);
       const int nvalid = min(S::SB, it.t_end - tok0);
@@ -395,7 +399,7 @@ __global__ void __launch_bounds__(Fp8Shape<D, NW, NS>::THREADS)
     report_error(p.err_flag, PA_DEVERR_TIMEOUT);
     const int issued = n_my < k + NS ? n_my : k + NS;
     if (lane == 0)
-      for (int kk = k; kk < issued; ++kk) fp8_wait(&bars[kk % NS], (kk / NS) & 1, never_flag);
+      for (int kk = k > first_issued ? k : first_issued; kk < issued; ++kk) drain_phase(&bars[kk % NS], (kk / NS) & 1);
     __syncwarp();
   }
 

@@ -43,6 +43,7 @@
 namespace pa {
 
 constexpr long long kWaitCycles = 500ll * 1000 * 1000;  // bound on one wait: ~0.25 s at 2 GHz
+constexpr long long kTestWaitCycles = 20000;              // the test hook's bound on a ring's first wait
 
 // bf16 probabilities are split into a rounded part and its residual (see the value MMA)
 template <typename T>
@@ -61,7 +62,7 @@ struct Shape {
   static constexpr int OROW = D + 4;                       // merge row stride (floats): conflict-free stores
   static constexpr int WARP_MERGE = 8 * OROW + 16;         // per warp: O[8][OROW], (m, l)[8]
   static constexpr int BAR_OFF = NW * RING_BYTES;
-  static constexpr int FLAG_OFF = BAR_OFF + NW * NS * 8;   // abort flag, then a word that stays 0
+  static constexpr int FLAG_OFF = BAR_OFF + NW * NS * 8;   // the CTA's abort flag
   static constexpr int SMEM_BYTES = FLAG_OFF + 16 + 1024;  // + alignment slack
   static constexpr int THREADS = NW * 32;
   static_assert(D % 64 == 0, "head_size must be a multiple of 64");
@@ -109,14 +110,15 @@ __device__ __forceinline__ bool decode_item(const DecodeParams& p, int id, Item&
 }
 
 // Wait for a barrier phase; gives up (returning false) when the CTA's abort
-// flag is set or after kWaitCycles SM cycles, in which case it raises the flag.
-__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag) {
+// flag is set or after `limit` SM cycles, in which case it raises the flag.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag,
+                                           long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long start = clock64();
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if ((i & 15u) == 15u && clock64() - start > kWaitCycles) {
+    if ((i & 15u) == 15u && clock64() - start > limit) {
       *abort_flag = 1;
       return false;
     }
@@ -243,11 +245,7 @@ __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
   uint8_t* ring = smem + warp * S::RING_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF) + warp * NS;
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + S::FLAG_OFF);
-  volatile int32_t* never_flag = abort_flag + 1;  // stays 0: waits that must not be cut short
-  if (threadIdx.x == 0) {
-    abort_flag[0] = 0;
-    never_flag[0] = 0;
-  }
+  if (threadIdx.x == 0) abort_flag[0] = 0;
   if (lane == 0) {
     for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
     fence_barrier_init();
@@ -316,12 +314,16 @@ __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
   float m_a = -INFINITY, m_b = -INFINITY;  // running max (log2 units) of heads 2q4, 2q4+1
   float l_a = 0.f, l_b = 0.f;              // this lane's share of the running sums
 
+  // test hook (pa_decode_options.test_flags): slab 0 of each ring is never requested and the
+  // first wait has a short bound, so that wait expires and the abort path below runs
+  const int first_issued = p.test_expire_first_wait ? 1 : 0;
   const int prologue = n_my < NS ? n_my : NS;
-  for (int k = 0; k < prologue; ++k) issue(k);
+  for (int k = first_issued; k < prologue; ++k) issue(k);
   int k = 0;
   for (; k < n_my; ++k) {
     const int stage = k % NS;
-    if (!__all_sync(0xffffffffu, wait_phase(&bars[stage], (k / NS) & 1, abort_flag))) break;
+    const long long limit = (k == 0 && p.test_expire_first_wait) ? kTestWaitCycles : kWaitCycles;
+    if (!__all_sync(0xffffffffu, wait_phase(&bars[stage], (k / NS) & 1, abort_flag, limit))) break;
     if ((valid_mask >> stage) & 1u) {
       const int tok0 = (it.j0 + warp + k * NW) * S::SB;
       const int nvalid = min(S::SB, it.t_end - tok0);
@@ -336,7 +338,7 @@ __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
     report_error(p.err_flag, PA_DEVERR_TIMEOUT);
     const int issued = n_my < k + NS ? n_my : k + NS;
     if (lane == 0)
-      for (int kk = k; kk < issued; ++kk) wait_phase(&bars[kk % NS], (kk / NS) & 1, never_flag);
+      for (int kk = k > first_issued ? k : first_issued; kk < issued; ++kk) drain_phase(&bars[kk % NS], (kk / NS) & 1);
     __syncwarp();
   }
 

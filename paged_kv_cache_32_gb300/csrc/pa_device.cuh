@@ -45,6 +45,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Wait for a phase of a barrier that copies this thread started complete, when
+// the CTA is giving up after an expired wait: bounded (about 0.25 s at 2 GHz),
+// blind to any abort flag and writing none, so every copy lands before the
+// shared memory it targets is reused or released.
+__device__ __forceinline__ void drain_phase(uint64_t* bar, uint32_t parity) {
+  const long long start = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - start > 500ll * 1000 * 1000) return;
+}
+
 // ---------------------------------------------------------------- TMA
 // 1-D bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16),
 // completion counted on `bar` in bytes.

@@ -29,6 +29,7 @@ struct DecodeParams {
   int32_t pmax;               // partitions per sequence in the grid
   float scale_log2;           // scale * log2(e)
   const float* alibi;         // nullable [Hq]: score_i += slope_h * (i - (L - 1))
+  int32_t test_expire_first_wait;  // test hook: each ring's first slab is never requested (0 in normal use)
 };
 
 // Kernel launchers (return the cudaGetLastError of the launch).

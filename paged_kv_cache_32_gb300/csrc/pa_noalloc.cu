@@ -9,8 +9,10 @@
 // longer than a decode step).  Such a caller passes its inputs and output
 // buffers as usual and lets the library use the scratch array below.
 //
-// Cost: every GPU on which the library is loaded holds kScratchBytes of device
-// memory for the scratch array until the process exits.
+// Cost: every GPU on which this call has run once holds kScratchBytes of
+// device memory for the scratch array until the process exits.  With CUDA's
+// lazy module loading (the default) the array is committed on a device when
+// the first call there looks up its address, not when the library is loaded.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -50,13 +52,17 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache, 
                                  const int32_t* block_tables, const int32_t* seq_lens, int32_t num_seqs,
                                  int32_t num_q_heads, int32_t max_blocks_per_seq, const pa_cache_desc* cache,
                                  float scale, int32_t partition_size, int32_t* err_flag, void* stream) {
+  // cache-shape and partition errors are reported before any CUDA call, as pa_decode does
+  const int32_t part = pa_decode_partition_size(max_blocks_per_seq, cache, partition_size);
+  if (part < 0) return -part;
   const size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, max_blocks_per_seq, cache, partition_size);
   if (need > kScratchBytes) return PA_ERR_WORKSPACE;  // these sizes need more scratch than the array holds
-  void* scratch = nullptr;
-  if (need > 0) {
-    scratch = scratch_address();
-    if (scratch == nullptr) return PA_ERR_CUDA;
-  }
+  // Resolved on every call, also when this call needs no scratch: the first
+  // call on a device (a warm-up with short sequences, say) then does the
+  // one-time lookup, never a later call that may sit inside a stream capture.
+  // After the first call per device this is a cached read.
+  void* scratch = scratch_address();
+  if (scratch == nullptr) return PA_ERR_CUDA;
   // The decode kernels write every scratch slot they later read, so nothing
   // has to be cleared between calls.
   return pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_q_heads, max_blocks_per_seq,

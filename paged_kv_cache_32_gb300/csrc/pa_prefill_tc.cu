@@ -431,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* qbuf = smem + kQOff;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int n_s = 0, n_o = 0;  // S / P V commits (control thread)
+  int n_pub = 0;         // items published, i.e. phases of bar_qs started (scheduling thread)
   int n_issued = 0;      // tiles whose copies this producer warp has issued
 
   if (threadIdx.x == 0) {
@@ -557,6 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (pf_item(p, idx, it, true)) break;
         if (idx >= n_items) it.s = -1;
         items[k & 1] = it;
+        ++n_pub;
         if (idx < n_items) {
           uint8_t* qb = qbuf + (k & 1) * 2 * kHalf;
           mbar_arrive_expect_tx(bar_qs, 2 * kHalf);
@@ -913,8 +915,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t* ring_bar = warp >= kLoadWarp0 + 2 ? bar_v : bar_k;
       for (int t = max(0, n_issued - 2); t < n_issued; ++t) drain_wait(&ring_bar[t & 1], (t >> 1) & 1);
     }
-    if (warp == kSWarp && lane == 0)
+    if (warp == kSWarp && lane == 0) {
       for (int t = max(0, n_s - kSBufs); t < n_s; ++t) drain_wait(&bar_s[t % kSBufs], (t / kSBufs) & 1);
+      // the Q copy of the last item published (at most one phase of bar_qs is outstanding: an item is
+      // published only after the previous one's Q has been waited for; a completed phase returns at once)
+      if (n_pub > 0) drain_wait(bar_qs, (n_pub - 1) & 1);
+    }
     if (warp == kPVWarp && lane == 0)
       for (int t = max(0, n_o - kSBufs); t < n_o; ++t) drain_wait(&bar_o[t % kSBufs], (t / kSBufs) & 1);
     __syncthreads();

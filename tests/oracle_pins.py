@@ -530,10 +530,35 @@ def pin_fp8_append():
     assert np.array_equal(kc, k0) and np.array_equal(vc, v0)
 
 
+def pin_prefill_dense():
+    """The numpy float64 form of chunked prefill (library matmuls, used for the benchmark-size
+    GPU checks) equals the C oracle and the pure-Python brute force on small cases: GQA and
+    MHA, f16/bf16/f32, block sizes 4 and 16, chunks of one token, of a whole sequence and
+    ragged ones."""
+    from oracle import dense
+
+    def both(w, q, qs):
+        kw = dict(dtype=w.dtype, num_kv_heads=w.num_kv_heads, block_size=w.block_size, scale=w.scale)
+        return (dense.prefill_attention(q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, qs, **kw),
+                _prefill(w, q, qs))
+
+    w, q, qs = _prefill_case(141, "bf16", lens=(9, 20, 13), chunks=(9, 6, 1))
+    got, ref = both(w, q, qs)
+    assert np.max(np.abs(got - ref)) < 1e-12
+    tiny = np.array(brute.prefill_attention(q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, qs, dtype=w.dtype,
+                                            num_kv_heads=w.num_kv_heads, block_size=w.block_size, scale=w.scale))
+    assert np.max(np.abs(got - tiny)) < 1e-12
+    for seed, dtype, Hq, Hkv, B in ((142, "f16", 8, 2, 16), (143, "f32", 3, 3, 4), (144, "bf16", 16, 2, 16)):
+        w, q, qs = _prefill_case(seed, dtype, lens=(40, 70, 5, 33), chunks=(40, 17, 0, 1), Hq=Hq, Hkv=Hkv, D=16,
+                                 B=B)
+        got, ref = both(w, q, qs)
+        assert np.max(np.abs(got - ref)) < 1e-12
+
+
 ALL_PINS = [
     pin_f16_decoding, pin_bf16_decoding, pin_35_token_example, pin_worked_offset, pin_prior_layout_offsets,
     pin_prior_layout_attention, pin_slot_round_trip, pin_padding_slots_skipped, pin_identity_tables_vs_contiguous,
     pin_permutation_invariance, pin_shared_prefix_equals_private, pin_cow_isolation, pin_brute_force,
     pin_special_cases, pin_split_identity, pin_zero_length, pin_bad_block_rejected, pin_alibi, pin_prefill,
-    pin_prefill_contiguous, pin_e4m3_codes, pin_e4m3_rounding, pin_fp8_attention, pin_fp8_append,
+    pin_prefill_contiguous, pin_prefill_dense, pin_e4m3_codes, pin_e4m3_rounding, pin_fp8_attention, pin_fp8_append,
 ]

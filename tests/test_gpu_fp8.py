@@ -9,7 +9,7 @@ bytes go to the GPU.
 
 Bars: the append is bit-exact over the whole pools (untouched bytes included);
 attention outputs are within the per-element bound of ``harness.bound`` for
-fp16 outputs (3e-3, or half an output ulp + 1e-3 where |out| >= 1).
+fp16 outputs (3e-3, or half an output ulp + 2^-12 where |out| >= 1).
 """
 import numpy as np
 import pytest

@@ -83,6 +83,16 @@ SMALL = [
     ("f16", 4, 4, 64, 48, [47, 48, 49, 200]),          # B = 48: 16-token slabs, 3 per block
     ("f32", 8, 2, 128, 16, [1, 16, 17, 90, 600]),
     ("f32", 4, 4, 64, 8, [1, 7, 8, 9, 64]),           # fp32 takes any block size
+    # large blocks (8 and 16 slabs of 16 tokens per block), as the benchmark's block-size sweep
+    # times them: G = 1 and G = 8, ragged tails inside a block and across blocks
+    ("f16", 4, 4, 128, 128, [1, 127, 128, 129, 300, 1000]),
+    ("f16", 16, 2, 128, 128, [2, 127, 128, 129, 500, 1100]),
+    ("bf16", 4, 4, 128, 128, [3, 127, 128, 129, 260, 900]),
+    ("bf16", 16, 2, 128, 128, [1, 127, 128, 129, 450, 1200]),
+    ("f16", 4, 4, 128, 256, [1, 255, 256, 257, 700, 1300]),
+    ("f16", 8, 1, 128, 256, [2, 255, 256, 257, 600, 1500]),
+    ("bf16", 4, 4, 128, 256, [3, 255, 256, 257, 513, 1400]),
+    ("bf16", 16, 2, 128, 256, [1, 255, 256, 257, 800, 1600]),
 ]
 
 
