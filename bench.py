@@ -67,8 +67,8 @@ def measured_peaks():
 
 
 # sources that define the decode call's kernels and launch configuration
-KERNEL_SOURCES = ("pa_api.cu", "pa_decode_tc.cu", "pa_decode_epilogue.cuh", "pa_device.cuh", "pa_internal.h",
-                  "pa_merge.cu")
+KERNEL_SOURCES = ("pa_api.cu", "pa_decode_tc.cu", "pa_decode_slab.cuh", "pa_decode_epilogue.cuh", "pa_device.cuh",
+                  "pa_internal.h", "pa_merge.cu")
 
 
 # sources that define the prefill call's kernel

@@ -123,7 +123,8 @@ enum {
  *                than one partition are split across CTAs and merged with a
  *                log-sum-exp reduction [P4 "PagedAttention Kernel在做什麼？"].
  *   workspace    device scratch of at least pa_decode_workspace_size(...) bytes,
- *                256-byte aligned; may be NULL when that size is 0.
+ *                256-byte aligned; may be NULL when that size is 0.  Its
+ *                contents on entry do not matter.
  *   err_flag     nullable device int32 (see above).
  *   Launches: the decode kernel, then (when a sequence spans two partitions) the
  *   merge kernel, both with programmatic stream serialization.  Their CTAs may be

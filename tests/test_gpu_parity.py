@@ -142,6 +142,61 @@ def test_merge_many_partitions_garbage_workspace(case):
     assert ok, f"{case}: max abs err {err}, worst err/bound {ratio}"
 
 
+# ---------------------------------------------------------------- the default split at the extremes
+def _default_split_check(w):
+    """Decode at the default partition size on a workspace full of garbage, twice: bit-identical
+    calls, within the bound of the fp64 oracle, and no device error."""
+    import torch
+    g = GpuStep(w)
+    need = g.pa.pa_decode_workspace_size(w.num_seqs, w.num_q_heads, w.max_blocks_per_seq, g.desc, 0)
+    ws = torch.full((max(need, 1),), 0x7F, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):
+        out = torch.full_like(g.q, float("nan"))
+        g.pa.pa_decode(out, g.q, g.k, g.v, g.tables, g.lens, w.scale, partition_size=0, workspace=ws,
+                       err_flag=g.err, desc=g.desc)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    ref = O.paged_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, dtype=w.dtype,
+                            num_kv_heads=w.num_kv_heads, block_size=w.block_size, scale=w.scale)
+    ok, err, ratio = within_bound(out_f64(outs[1]), ref, w.dtype)
+    assert ok, f"{w.name}: max abs err {err}, worst err/bound {ratio}"
+
+
+def test_many_short_sequences():
+    """40 000 sequences of 0 to 40 tokens (1 in 8 empty), 2 q / 1 kv heads, D = 64: a grid of
+    40 000 work items of one to three slabs; empty sequences get zero rows."""
+    rng = np.random.default_rng(2024)
+    lens = rng.integers(1, 41, size=40000)
+    lens[::8] = 0
+    w = W.build_decode("short_many", seed=2024, dtype="bf16", seq_lens=lens, num_q_heads=2, num_kv_heads=1,
+                       head_size=64, block_size=16, pool_factor=1.1)
+    _default_split_check(w)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_long_sequences_default_partitions(dtype):
+    """Two sequences of 8192 and 6000 tokens, 32 q / 8 kv heads, B = 32: eight and six 1024-token
+    partitions per (sequence, kv head), merged."""
+    w = W.build_decode(f"long_default_{dtype}", seed=77, dtype=dtype, seq_lens=[8192, 6000], num_q_heads=32,
+                       num_kv_heads=8, head_size=128, block_size=32, pool_factor=1.1)
+    _default_split_check(w)
+
+
+@pytest.mark.parametrize("case", [
+    ("f16", 8, 8, 128, 16, [1, 15, 16, 17, 700, 0, 2048, 33]),
+    ("bf16", 64, 8, 128, 32, [5, 300, 1200, 4000, 64, 0, 999]),
+    ("bf16", 24, 2, 64, 64, [1, 130, 4096, 77]),        # G = 12: two head groups, the second of 4 heads
+], ids=lambda c: f"{c[0]}-Hq{c[1]}-Hkv{c[2]}-D{c[3]}-B{c[4]}")
+def test_default_split_garbage_workspace(case):
+    dtype, Hq, Hkv, D, B, lens = case
+    w = W.build_decode("default_mix", seed=zlib.crc32(repr(case).encode()) % 10000, dtype=dtype, seq_lens=lens,
+                       num_q_heads=Hq, num_kv_heads=Hkv, head_size=D, block_size=B, pool_factor=1.3)
+    _default_split_check(w)
+
+
 def test_permuted_block_ids_bit_identical():
     """Relabelling physical blocks leaves the GPU output bit-identical."""
     import torch
