@@ -374,8 +374,8 @@ def bench_secondary(device, steps: int, warmup: int, peak: float):
     lens = np.random.default_rng(1001).integers(128, 2048, size=64, endpoint=True)  # the mha_f16 lengths
     res = {}
 
-    def decode(name, block_size, shuffle, num_blocks=None):
-        w = W.build_decode(name, seed=1001, dtype="f16", seq_lens=lens, num_q_heads=32, num_kv_heads=32,
+    def decode(name, block_size, shuffle, num_blocks=None, dtype="f16"):
+        w = W.build_decode(name, seed=1001, dtype=dtype, seq_lens=lens, num_q_heads=32, num_kv_heads=32,
                            head_size=128, block_size=block_size, num_blocks=num_blocks, shuffle=shuffle,
                            materialize=False)
         ds = DeviceStep(w, device)
@@ -393,8 +393,13 @@ def bench_secondary(device, steps: int, warmup: int, peak: float):
     res["block_tables"] = {"workload": "mha_f16 sequences, B 16, pool 8192", "shuffled": shuffled,
                            "identity": identity,
                            "shuffled_over_identity_time": round(shuffled["decode_ms"] / identity["decode_ms"], 4)}
-    res["block_size_sweep"] = {"workload": "mha_f16 sequences, shuffled pool 1.2x needed",
-                               **{f"B{b}": decode(f"sweep_b{b}", b, True) for b in (16, 32, 64, 128, 256)}}
+    res["block_size_sweep"] = {"workload": "mha_f16 sequences, shuffled pool 1.2x needed (B 8: two 8-row copies "
+                                           "per 16-token slab)",
+                               **{f"B{b}": decode(f"sweep_b{b}", b, True) for b in (8, 16, 32, 64, 128, 256)}}
+    # the pages' claim that one-token blocks are catastrophic, on the one kernel that takes any block size (the
+    # fp32 CUDA-core kernel, a correctness path: one table entry and one dependent row load per token at B 1)
+    res["block_size_probe_fp32"] = {"workload": "mha_f16 sequences in fp32, shuffled pool 1.2x needed",
+                                    **{f"B{b}": decode(f"probe_f32_b{b}", b, True, dtype="f32") for b in (16, 1)}}
 
     # the write calls on an MHA fp16 pool (8192 blocks of 16 slots, 32 heads, D 128)
     gen = torch.Generator(device=device)

@@ -50,7 +50,8 @@ typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_FP8_E4M3 = 3 } pa_dtype;
 /* Shape of one layer's KV cache pair. */
 typedef struct {
   int32_t num_blocks;   /* physical blocks in the pool */
-  int32_t block_size;   /* tokens per block B: f16/bf16/fp8 need a multiple of 16 (<= 256); f32 any B >= 1 */
+  int32_t block_size;   /* tokens per block B: f16/bf16 8 or a multiple of 16 (<= 256); fp8 a multiple of 16
+                           (<= 256); f32 any B >= 1 */
   int32_t num_kv_heads; /* Hkv */
   int32_t head_size;    /* D: 64 or 128 (fp8: 128) */
   int32_t dtype;        /* pa_dtype of the cache, and of q/out and new key/value except for fp8 (see below) */
@@ -119,7 +120,8 @@ enum {
  *                on the device beyond the table width: longer values are clamped)
  *   scale        softmax scale (usually 1/sqrt(head_size))
  *   partition_size  0 = library default (1024 tokens); else tokens per partition, a
- *                multiple of block_size.  Sequences longer
+ *                multiple of block_size and, for f16/bf16/fp8 caches, of 16 (the
+ *                kernels' 16-token slabs never straddle a partition).  Sequences longer
  *                than one partition are split across CTAs and merged with a
  *                log-sum-exp reduction [P4 "PagedAttention Kernel在做什麼？"].
  *   workspace    device scratch of at least pa_decode_workspace_size(...) bytes,
@@ -206,7 +208,7 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t m
  *   A sequence whose chunk breaks these rules is skipped and PA_DEVERR_QUERY is
  *   reported; a bad block ID gives PA_DEVERR_BLOCK_ID and that sequence's
  *   output is undefined.
- *   Supported: dtype f16 / bf16, head_size 128, block_size 16, 32, 64 or 128.
+ *   Supported: dtype f16 / bf16, head_size 128, block_size 8, 16, 32, 64 or 128.
  *   Runs on the tcgen05 tensor cores: a persistent kernel, one CTA per SM,
  *   whose CTAs walk the work items (sequence, query head, tile of 128 queries).
  */

@@ -15,6 +15,7 @@ namespace pa {
 namespace host {
 
 constexpr int32_t kDefaultPartition = 1024;  // tokens per partition when the caller passes 0 (measured best)
+constexpr int32_t kTcSlab = 16;              // tokens per slab of the f16/bf16/fp8 decode kernels
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -29,7 +30,11 @@ int check_cache(const pa_cache_desc* c) {
     return PA_ERR_INVALID_ARG;
   if (c->head_size != 64 && c->head_size != 128) return PA_ERR_UNSUPPORTED;
   if (c->dtype == PA_FP8_E4M3 && c->head_size != 128) return PA_ERR_UNSUPPORTED;
-  if (c->dtype != PA_F32 && (c->block_size % 16 != 0 || c->block_size > 256)) return PA_ERR_UNSUPPORTED;
+  // fp8: whole 16-token value tiles; f16/bf16: 16-token slabs of one block, or of two 8-token blocks
+  if (c->dtype == PA_FP8_E4M3 && (c->block_size % 16 != 0 || c->block_size > 256)) return PA_ERR_UNSUPPORTED;
+  if ((c->dtype == PA_F16 || c->dtype == PA_BF16) &&
+      !(c->block_size == 8 || (c->block_size % 16 == 0 && c->block_size <= 256)))
+    return PA_ERR_UNSUPPORTED;
   // row index (block * Hkv + head) * B + slot must fit the kernels' int32 arithmetic
   if ((int64_t)c->num_blocks * c->num_kv_heads * c->block_size > kInt32Max) return PA_ERR_TOO_LARGE;
   return PA_OK;
@@ -49,6 +54,8 @@ int32_t resolve_partition(int32_t max_blocks_per_seq, const pa_cache_desc* c, in
   } else if (part % c->block_size != 0) {
     return -PA_ERR_INVALID_ARG;
   }
+  // the f16/bf16 kernel's 16-token slabs never straddle a partition boundary
+  if (c->dtype != PA_F32 && part % kTcSlab != 0) return -PA_ERR_INVALID_ARG;
   if (part >= max_len) part = max_len > 0 ? max_len : c->block_size;  // no split needed
   return (int32_t)part;
 }
@@ -227,8 +234,9 @@ int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_ca
     e = pa::launch_decode_fp8(cache->head_size, tk, tk32, v_cache, p, k_scale, v_scale, st);
   } else {
     CUtensorMap tk, tv;
-    if (!encode_cache_map(&tk, k_cache, cache, pa::kTcSlabTokens) ||
-        !encode_cache_map(&tv, v_cache, cache, pa::kTcSlabTokens))
+    // a slab is one 16-row box, or (8-token blocks) two 8-row boxes from two blocks
+    const int box_rows = cache->block_size < pa::kTcSlabTokens ? cache->block_size : pa::kTcSlabTokens;
+    if (!encode_cache_map(&tk, k_cache, cache, box_rows) || !encode_cache_map(&tv, v_cache, cache, box_rows))
       return PA_ERR_CUDA;
     e = pa::launch_decode_tc(cache->dtype, cache->head_size, cache->block_size, tk, tv, p, st);
   }

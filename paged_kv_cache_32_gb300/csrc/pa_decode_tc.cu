@@ -149,9 +149,20 @@ __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
   // ---- this warp's slabs: j = warp + k * NW, k < n_my
   const int n_my = it.nslabs > warp ? (it.nslabs - warp + NW - 1) / NW : 0;
   const int B = p.block_size;
+  const bool split = B < S::SB;  // 8-token blocks: a slab is two 8-row halves from two blocks
   const int32_t* table = p.block_tables + (size_t)it.s * p.max_blocks;
-  int pb_batch = 0;
-  int pb_reg = lane < n_my ? __ldg(table + ((it.j0 + warp + lane * NW) * S::SB) / B) : -1;
+  // lane l holds the table entries of this warp's slab 32 b + l: its (first) block, and with 8-token
+  // blocks that of its second half (-1 when the half lies past the partition)
+  auto fetch = [&](int kk, int& e0, int& e1) {
+    e0 = e1 = -1;
+    if (kk < n_my) {
+      const int tok0 = (it.j0 + warp + kk * NW) * S::SB;
+      e0 = __ldg(table + tok0 / B);
+      if (split && tok0 + B < it.t_end) e1 = __ldg(table + tok0 / B + 1);
+    }
+  };
+  int pb_batch = 0, pb_reg, pb_reg2;
+  fetch(lane, pb_reg, pb_reg2);
 
   // ---- query fragments (B operand of S^T = K Q^T): head g, dims 16j + 2q4 (+8)
   uint32_t qf[S::KSTEPS][2];
@@ -178,23 +189,39 @@ __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
   auto issue = [&](int k) {  // called by the whole warp, k increasing
     if ((k >> 5) != pb_batch) {
       pb_batch = k >> 5;
-      const int kk = k + lane;
-      pb_reg = kk < n_my ? __ldg(table + ((it.j0 + warp + kk * NW) * S::SB) / B) : -1;
+      fetch(k + lane, pb_reg, pb_reg2);
     }
     const int pb = __shfl_sync(0xffffffffu, pb_reg, k & 31);
-    const bool valid = pb >= 0 && pb < p.num_blocks;
+    const int pb2 = __shfl_sync(0xffffffffu, pb_reg2, k & 31);
+    const int tok0 = (it.j0 + warp + k * NW) * S::SB;
+    const bool has2 = split && tok0 + B < it.t_end;  // the second 8-token half holds tokens of the item
+    const bool valid = pb >= 0 && pb < p.num_blocks && (!has2 || (pb2 >= 0 && pb2 < p.num_blocks));
     const int stage = k % NS;
     valid_mask = valid ? (valid_mask | (1u << stage)) : (valid_mask & ~(1u << stage));
     if (lane == 0) {
       uint64_t* bar = &bars[stage];
-      if (valid) {
-        const int y = (pb * p.num_kv_heads + it.hkv) * B + ((it.j0 + warp + k * NW) * S::SB) % B;  // first row
-        uint8_t* dst = ring + stage * S::SLAB_BYTES;
+      uint8_t* dst = ring + stage * S::SLAB_BYTES;
+      if (valid && !split) {
+        const int y = (pb * p.num_kv_heads + it.hkv) * B + tok0 % B;  // first row
         mbar_arrive_expect_tx(bar, S::SLAB_BYTES);
 #pragma unroll
         for (int b = 0; b < S::NBOX; ++b) tma_load_2d(dst + b * S::BOX_BYTES, &tmap_k, b * 64, y, bar);
 #pragma unroll
         for (int b = 0; b < S::NBOX; ++b) tma_load_2d(dst + (S::NBOX + b) * S::BOX_BYTES, &tmap_v, b * 64, y, bar);
+      } else if (valid) {
+        // 8-row boxes: rows 8u .. 8u + 7 of each 16-row box region come from block pb (u = 0) or pb2 (u = 1),
+        // 1024 bytes apart, which keeps the 128-byte swizzle of a 16-row box.  Rows of an absent second half
+        // are left as they are: the slab step masks tokens past the item.
+        mbar_arrive_expect_tx(bar, has2 ? S::SLAB_BYTES : S::SLAB_BYTES / 2);
+        for (int u = 0; u < (has2 ? 2 : 1); ++u) {
+          const int y = ((u ? pb2 : pb) * p.num_kv_heads + it.hkv) * B;
+#pragma unroll
+          for (int b = 0; b < S::NBOX; ++b)
+            tma_load_2d(dst + b * S::BOX_BYTES + u * (S::BOX_BYTES / 2), &tmap_k, b * 64, y, bar);
+#pragma unroll
+          for (int b = 0; b < S::NBOX; ++b)
+            tma_load_2d(dst + (S::NBOX + b) * S::BOX_BYTES + u * (S::BOX_BYTES / 2), &tmap_v, b * 64, y, bar);
+        }
       } else {
         report_error(p.err_flag, PA_DEVERR_BLOCK_ID);
         mbar_arrive(bar);  // complete the phase without data; the slab is skipped

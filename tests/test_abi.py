@@ -58,7 +58,9 @@ def call_decode(lib, d, out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, sl=FAKE, n=2,
 def test_decode_argument_errors(lib):
     assert call_decode(lib, desc(d=96)) == 2                         # head_size unsupported
     assert call_decode(lib, desc(dtype=7)) == 2                      # dtype unsupported
-    assert call_decode(lib, desc(bs=8)) == 2                         # f16 needs B % 16 == 0
+    assert call_decode(lib, desc(bs=24)) == 2                        # f16: B = 8 or a multiple of 16
+    assert call_decode(lib, desc(bs=8, dtype=pa.PA_FP8_E4M3)) == 2   # fp8: B a multiple of 16
+    assert call_decode(lib, desc(bs=8), part=8) == 3                 # partitions are whole 16-token slabs
     assert call_decode(lib, desc(), hq=3) == 3                       # Hq % Hkv != 0
     assert call_decode(lib, desc(), n=-1) == 3
     assert call_decode(lib, desc(), scale=float("nan")) == 3

@@ -93,6 +93,12 @@ SMALL = [
     ("f16", 8, 1, 128, 256, [2, 255, 256, 257, 600, 1500]),
     ("bf16", 4, 4, 128, 256, [3, 255, 256, 257, 513, 1400]),
     ("bf16", 16, 2, 128, 256, [1, 255, 256, 257, 800, 1600]),
+    # 8-token blocks: a 16-token slab comes from two blocks (two 8-row copies), its second half
+    # absent when the sequence ends inside the first
+    ("f16", 4, 4, 128, 8, [1, 7, 8, 9, 15, 16, 17, 24, 300]),
+    ("bf16", 16, 2, 128, 8, [2, 8, 9, 23, 33, 1000]),
+    ("f16", 8, 1, 64, 8, [3, 8, 16, 25, 513]),
+    ("bf16", 4, 4, 64, 8, [1, 9, 40, 777]),
 ]
 
 
@@ -102,7 +108,8 @@ def test_small_cases(case, partition):
     dtype, Hq, Hkv, D, B, lens = case
     w = W.build_decode("small", seed=zlib.crc32(repr(case).encode()) % 10000, dtype=dtype, seq_lens=lens, num_q_heads=Hq, num_kv_heads=Hkv,
                        head_size=D, block_size=B, pool_factor=1.3, append_last=True)
-    part = {0: 0, "one_block": B, "big": 8 * max(B, 32)}[partition]
+    # the 16-bit kernels' partitions are whole 16-token slabs: with 8-token blocks, two blocks
+    part = {0: 0, "one_block": B if dtype == "f32" else max(B, 16), "big": 8 * max(B, 32)}[partition]
     check_step(w, partition_size=part)
 
 

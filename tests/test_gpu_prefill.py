@@ -100,7 +100,7 @@ def assert_close(got, ref, dtype, what):
 
 # ---------------------------------------------------------------- small cases, every output compared
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-@pytest.mark.parametrize("block_size", [16, 32, 64, 128])
+@pytest.mark.parametrize("block_size", [8, 16, 32, 64, 128])
 def test_prefill_small_gqa(dtype, block_size):
     w = small(dtype, block_size)
     g = PrefillStep(w)
