@@ -104,6 +104,84 @@ def ncu_traffic(workload: str):
     return entry.get("dram_bytes_per_launch")
 
 
+class NvmlClockSampler:
+    """SM clock, power and clock-event reasons read through NVML (the driver's libnvidia-ml, reads only)
+    about every 0.5 ms on a background thread, so that even a few-millisecond timed region gets several
+    samples.  Raises OSError at construction when NVML is unavailable."""
+    # clock-event reason bits of NVML's public API
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40}
+
+    def __init__(self, index: int):
+        import ctypes
+        self.ct = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib = lib
+        self.dev = ctypes.c_void_p()
+        handle = None
+        try:  # match the CUDA device by its PCI address when torch exposes it
+            import torch
+            pr = torch.cuda.get_device_properties(index)
+            bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0".encode()
+            if lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(self.dev)) == 0:
+                handle = self.dev
+        except (AttributeError, RuntimeError, ImportError):
+            handle = None
+        if handle is None and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.dev)) != 0:
+            raise OSError("no NVML handle")
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        mx = ctypes.c_uint()
+        self.max_mhz = float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(mx)) == 0 else None
+        self.samples = []
+        self.running = False
+        self.thread = None
+
+    def _read(self):
+        ct = self.ct
+        mhz, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        while self.running:
+            ok = self.lib.nvmlDeviceGetClockInfo(self.dev, 1, ct.byref(mhz)) == 0  # NVML_CLOCK_SM
+            okr = self.reasons_fn(self.dev, ct.byref(rs)) == 0
+            okp = self.lib.nvmlDeviceGetPowerUsage(self.dev, ct.byref(mw)) == 0
+            if ok:
+                self.samples.append((time.time(), float(mhz.value), int(rs.value) if okr else 0,
+                                     mw.value / 1000.0 if okp else None))
+            time.sleep(0.0005)
+
+    def start(self):
+        self.running = True
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self.running = False
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
+        if not inside and self.samples:  # nothing inside: the nearest sample
+            mid = 0.5 * (t0 + t1)
+            inside = [min(self.samples, key=lambda x: abs(x[0] - mid))]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"], "samples": 0}
+        reasons = sorted(n for n, b in self.REASON_BITS.items() if any(x[2] & b for x in inside))
+        pw = [x[3] for x in inside if x[3] is not None]
+        return {"sm_mhz": statistics.median(x[1] for x in inside), "sm_min_mhz": min(x[1] for x in inside),
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(inside),
+                "power_w_max": max(pw) if pw else None, "source": "nvml"}
+
+
+def clock_sampler(index: int):
+    """NVML sampling when the driver's library loads, else nvidia-smi."""
+    try:
+        return NvmlClockSampler(index)
+    except (OSError, AttributeError):
+        return ClockSampler(index)
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while the GPU works."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
@@ -568,7 +646,7 @@ def run_ours(args, world, rank, local):
     if args.partition is not None:
         w.partition_size = args.partition
     ds = DeviceStep(w, device)
-    sampler = ClockSampler(local)
+    sampler = clock_sampler(local)
     sampler.start()
     ms_step, decode_ms, write_ms, (t0, t1) = time_device(ds, args.steps, args.warmup, world)
     ms_step = all_max(ms_step, world)
@@ -616,7 +694,7 @@ def run_ours(args, world, rank, local):
     }
     if not args.no_extra and world == 1:
         line["other_workloads"] = {}
-        sampler_x = ClockSampler(local)
+        sampler_x = clock_sampler(local)
         sampler_x.start()
         for name in args.extra:
             if name == args.workload:
@@ -690,7 +768,7 @@ def bench_prefill(name: str, device, steps: int, warmup: int, peaks):
     import torch
     w = W.WORKLOADS[name](materialize=False)
     ps = PrefillDeviceStep(w, device)
-    sampler = ClockSampler(torch.cuda.current_device())
+    sampler = clock_sampler(torch.cuda.current_device())
     sampler.start()
     ms_step, att_ms, write_ms, (t0, t1) = time_device(ps, steps, warmup, 1)
     sampler.stop()
