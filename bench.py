@@ -37,7 +37,7 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
 WORKLOAD_DESC = {
     "mha_f16": "MHA fp16 decode: 64 seqs, seq_lens U[128,2048], 32 q = 32 kv heads, D 128, B 16, pool 8192 shuffled, "
-               "one reshape_and_cache append per seq, then attention",
+               "each seq's new token appended and attended in one pa_decode_append call",
     "gqa_bf16": "GQA bf16 decode: 128 seqs, 64 q / 8 kv heads, D 128, B 32, lognormal(ln 1200, 0.6) lens in "
                 "[64, 4096], pool 1.2x needed, shuffled",
     "shared_prefix_f16": "shared-prefix fp16: 16 prompts x 8 branches, 1024-token shared prefix, suffix U[1,256], "
@@ -317,10 +317,14 @@ class DeviceStep:
         self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
         self.ws_bytes = need
         self.pmax = 1 if need == 0 else -(-w.max_blocks_per_seq * w.block_size // self.part)
+        # a step whose writes are each sequence's new token at its last position, on a 16-bit cache:
+        # the append runs inside the decode call (pa_decode_append)
+        self.fused = bool(w.info.get("append_last")) and not self.fp8 and w.dtype in ("f16", "bf16") and \
+            self.pairs is None and self.slots is not None
         assert tdt == self.q.dtype
 
     def launches_per_step(self) -> int:
-        return (self.pairs is not None) + (self.slots is not None) + 1 + (self.pmax > 1)
+        return (self.pairs is not None) + (self.slots is not None and not self.fused) + 1 + (self.pmax > 1)
 
     def append(self, stream, nk, nv, slots):
         if self.fp8:
@@ -333,8 +337,19 @@ class DeviceStep:
     def writes(self, stream):
         if self.pairs is not None:
             self.pa.pa_copy_blocks(self.k, self.v, self.pairs, err_flag=self.err, stream=stream, desc=self.desc)
-        if self.slots is not None:
+        if self.slots is not None and not self.fused:
             self.append(stream, self.nk, self.nv, self.slots)
+
+    def step_decode(self, stream, q=None, tables=None, lens=None, nk=None, nv=None):
+        """The step's attention: with the append fused in when the step allows it."""
+        if not self.fused:
+            self.decode(stream, q=q, tables=tables, lens=lens)
+            return
+        self.pa.pa_decode_append(self.out, self.q if q is None else q, self.k, self.v, self.nk if nk is None else nk,
+                                 self.nv if nv is None else nv, self.tables if tables is None else tables,
+                                 self.lens if lens is None else lens, self.w.scale,
+                                 partition_size=self.w.partition_size, workspace=self.ws, err_flag=self.err,
+                                 stream=stream, desc=self.desc)
 
     def decode(self, stream, q=None, tables=None, lens=None, out=None):
         self.pa.pa_decode(self.out if out is None else out, self.q if q is None else q, self.k, self.v,
@@ -344,14 +359,17 @@ class DeviceStep:
                           k_scale=self.k_scale if self.fp8 else None, v_scale=self.v_scale if self.fp8 else None)
 
     def attend(self, stream):
-        self.decode(stream)
+        self.step_decode(stream)
 
     def decode_bytes(self) -> int:
         """Algorithmic HBM bytes of one pa_decode call: K+V of every token, q in,
-        out, table entries, and the split-KV partial results (written then read)."""
+        out, table entries, and the split-KV partial results (written then read);
+        with the append fused in, also the new tokens' K/V read and written."""
         w = self.w
         eb = W.ELEM_BYTES[w.dtype]
         b = w.kv_bytes() + 2 * w.num_seqs * w.num_q_heads * w.head_size * eb
+        if self.fused:
+            b += 2 * 2 * int(np.sum(w.seq_lens > 0)) * w.num_kv_heads * w.head_size * eb
         b += int(np.sum(-(-w.seq_lens.astype(np.int64) // w.block_size))) * 4 + w.num_seqs * 4
         if self.pmax > 1:
             nparts = -(-w.seq_lens.astype(np.int64) // self.part)
@@ -542,9 +560,9 @@ def time_e2e(ds: DeviceStep, steps: int, warmup: int, world: int):
         dev_buf.copy_(host_buf, non_blocking=True)
         if ds.pairs is not None:
             ds.pa.pa_copy_blocks(ds.k, ds.v, dev["pairs"], err_flag=ds.err, stream=stream, desc=ds.desc)
-        if ds.slots is not None:
+        if ds.slots is not None and not ds.fused:
             ds.append(stream, dev["nk"], dev["nv"], dev["slots"])
-        ds.decode(stream, q=dev["q"], tables=dev["tables"], lens=dev["lens"])
+        ds.step_decode(stream, q=dev["q"], tables=dev["tables"], lens=dev["lens"], nk=dev.get("nk"), nv=dev.get("nv"))
         out_host.copy_(ds.out, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -677,7 +695,9 @@ def run_ours(args, world, rank, local):
                    "partition_size": ds.part, "l2": "inputs larger than L2 (K/V working set "
                    f"{kv / 1e9:.2f} GB vs 0.13 GB L2); no flush", "parallelism": f"replicas x{world}"},
         "tokens_per_s": round(world * w.num_seqs / (ms_step * 1e-3), 1),
-        "roofline": {"bound": "hbm", "kernel": "pa_decode (decode_tc_kernel + merge_kernel when split)",
+        "roofline": {"bound": "hbm", "kernel": ("pa_decode_append (decode_tc_kernel with the append fused in + "
+                                                 "merge_kernel when split)" if ds.fused else
+                                                 "pa_decode (decode_tc_kernel + merge_kernel when split)"),
                      "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": dbytes, "launch_ms": round(dec_ms, 5),

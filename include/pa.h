@@ -173,6 +173,29 @@ int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_ca
                  const pa_cache_desc* cache, float scale, int32_t partition_size, void* workspace,
                  size_t workspace_bytes, int32_t* err_flag, void* stream, const pa_decode_options* options);
 
+/*
+ * pa_decode_append - one decode step with its append fused in: for every
+ *   sequence s with seq_lens[s] = L > 0, the new token's key[s][h][:] and
+ *   value[s][h][:] are stored at position L - 1 of both caches, i.e. at
+ *   offset (L - 1) % B of block block_tables[s][(L - 1) / B]
+ *   [P1 "写入新 K/V": slot = block * B + offset], and out is pa_decode's over
+ *   positions 0 .. L - 1, the new token included.  The result and the cache
+ *   contents equal pa_reshape_and_cache with those slots followed by pa_decode,
+ *   in one launch (plus the merge when a sequence spans two partitions): the
+ *   CTA that streams the new token's slab takes the token's rows from key and
+ *   value, and the first query-head group of each kv head stores them.
+ *
+ *   key, value   [num_seqs][num_kv_heads][head_size] of dtype, 16-byte aligned
+ *   other arguments as for pa_decode; f16 and bf16 caches (fp32 and fp8: use
+ *   pa_reshape_and_cache(_fp8) and pa_decode).  The slot at position L - 1 must
+ *   belong to this sequence alone (the block manager copies a shared partial
+ *   block on write first); a sequence's other slots are not written.
+ */
+int pa_decode_append(void* out, const void* q, void* k_cache, void* v_cache, const void* key, const void* value,
+                     const int32_t* block_tables, const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                     int32_t max_blocks_per_seq, const pa_cache_desc* cache, float scale, int32_t partition_size,
+                     void* workspace, size_t workspace_bytes, int32_t* err_flag, void* stream);
+
 /* Partition size pa_decode uses for these arguments (resolves 0 to the default);
  * returns a value >= max_blocks_per_seq * block_size when no split happens, or a
  * negative PA_ERR_* code for invalid arguments. */

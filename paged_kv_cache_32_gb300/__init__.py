@@ -22,8 +22,8 @@ PA_OK = 0
 PA_DEVERR = {0: "none", 1: "block id out of range", 2: "slot out of range", 3: "copy pair id out of range",
              4: "wait on an asynchronous copy timed out", 5: "prefill chunk inconsistent with q, grid or sequence"}
 
-EXPORTED = ("pa_decode", "pa_decode_ex", "pa_decode_partition_size", "pa_decode_workspace_size", "pa_reshape_and_cache",
-            "pa_copy_blocks", "pa_status_string", "pa_version", "pa_decode_noalloc", "pa_prefill",
+EXPORTED = ("pa_decode", "pa_decode_ex", "pa_decode_append", "pa_decode_partition_size", "pa_decode_workspace_size",
+            "pa_reshape_and_cache", "pa_copy_blocks", "pa_status_string", "pa_version", "pa_decode_noalloc", "pa_prefill",
             "pa_reshape_and_cache_fp8")
 
 
@@ -66,6 +66,9 @@ def lib() -> ctypes.CDLL:
         L.pa_decode.restype = ctypes.c_int
         L.pa_decode_ex.argtypes = L.pa_decode.argtypes + [ctypes.POINTER(pa_decode_options)]
         L.pa_decode_ex.restype = ctypes.c_int
+        L.pa_decode_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, desc_p, ctypes.c_float, i32, vp, sz,
+                                       vp, vp]
+        L.pa_decode_append.restype = ctypes.c_int
         L.pa_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, desc_p, ctypes.c_float, vp, vp]
         L.pa_prefill.restype = ctypes.c_int
         L.pa_decode_partition_size.argtypes = [i32, desc_p, i32]
@@ -193,6 +196,29 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale: float, pa
         _dense(alibi_slopes, "alibi_slopes")
         opts = pa_decode_options(_ptr(alibi_slopes), float(k_scale or 0.0), float(v_scale or 0.0), int(test_flags))
         _check(lib().pa_decode_ex(*args, ctypes.byref(opts)), "pa_decode_ex")
+
+
+def pa_decode_append(out, q, k_cache, v_cache, key, value, block_tables, seq_lens, scale: float,
+                     partition_size: int = 0, workspace=None, err_flag=None, stream=None,
+                     desc: pa_cache_desc | None = None) -> None:
+    """A decode step with its append: key/value [num_seqs, num_kv_heads, head_size] are each
+    sequence's new token, stored at position seq_lens[s] - 1 of both caches (through the block
+    table) and attended in the same call.  fp16/bf16 caches."""
+    desc = desc or cache_desc(k_cache)
+    for t, n in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (key, "key"), (value, "value"),
+                 (block_tables, "block_tables"), (seq_lens, "seq_lens")):
+        _dense(t, n)
+    num_seqs, num_q_heads = int(q.shape[0]), int(q.shape[1])
+    max_blocks = int(block_tables.shape[1]) if block_tables.dim() == 2 else 0
+    need = pa_decode_workspace_size(num_seqs, num_q_heads, max_blocks, desc, partition_size)
+    if workspace is None and need > 0:
+        import torch
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().pa_decode_append(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(key), _ptr(value),
+                                  _ptr(block_tables), _ptr(seq_lens), num_seqs, num_q_heads, max_blocks,
+                                  ctypes.byref(desc), float(scale), int(partition_size), _ptr(workspace), ws_bytes,
+                                  _ptr(err_flag), _stream(stream)), "pa_decode_append")
 
 
 def pa_prefill(out, q, k_cache, v_cache, block_tables, seq_lens, query_start, max_query_len: int, scale: float,

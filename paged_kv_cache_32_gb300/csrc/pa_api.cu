@@ -158,10 +158,14 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
                       cache, scale, partition_size, workspace, workspace_bytes, err_flag, stream, nullptr);
 }
 
-int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
-                 const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
-                 const pa_cache_desc* cache, float scale, int32_t partition_size, void* workspace,
-                 size_t workspace_bytes, int32_t* err_flag, void* stream, const pa_decode_options* options) {
+}  // extern "C"
+
+// pa_decode_ex, and pa_decode_append when new_key / new_value are given
+static int decode_call(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                       const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                       const pa_cache_desc* cache, float scale, int32_t partition_size, void* workspace,
+                       size_t workspace_bytes, int32_t* err_flag, void* stream, const pa_decode_options* options,
+                       const void* new_key, const void* new_value) {
   int rc = check_cache(cache);
   if (rc != PA_OK) return rc;
   if (num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq < 0) return PA_ERR_INVALID_ARG;
@@ -220,6 +224,10 @@ int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_ca
   p.alibi = alibi;
   p.test_expire_first_wait =
       (options != nullptr && (options->test_flags & PA_DECODE_TEST_EXPIRE_FIRST_WAIT) != 0u) ? 1 : 0;
+  p.new_k = new_key;
+  p.new_v = new_value;
+  p.k_cache_out = const_cast<void*>(k_cache);
+  p.v_cache_out = const_cast<void*>(v_cache);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -246,6 +254,30 @@ int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_ca
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;
+}
+
+extern "C" {
+
+int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                 const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                 const pa_cache_desc* cache, float scale, int32_t partition_size, void* workspace,
+                 size_t workspace_bytes, int32_t* err_flag, void* stream, const pa_decode_options* options) {
+  return decode_call(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_q_heads, max_blocks_per_seq,
+                     cache, scale, partition_size, workspace, workspace_bytes, err_flag, stream, options, nullptr,
+                     nullptr);
+}
+
+int pa_decode_append(void* out, const void* q, void* k_cache, void* v_cache, const void* key, const void* value,
+                     const int32_t* block_tables, const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                     int32_t max_blocks_per_seq, const pa_cache_desc* cache, float scale, int32_t partition_size,
+                     void* workspace, size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  int rc = check_cache(cache);
+  if (rc != PA_OK) return rc;
+  if (cache->dtype != PA_F16 && cache->dtype != PA_BF16) return PA_ERR_UNSUPPORTED;  // the tensor-core kernel
+  if (num_seqs > 0 && (key == nullptr || value == nullptr)) return PA_ERR_NULL_POINTER;
+  if (!aligned(key, 16) || !aligned(value, 16)) return PA_ERR_MISALIGNED;
+  return decode_call(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_q_heads, max_blocks_per_seq,
+                     cache, scale, partition_size, workspace, workspace_bytes, err_flag, stream, nullptr, key, value);
 }
 
 int pa_reshape_and_cache(void* k_cache, void* v_cache, const void* key, const void* value,

@@ -120,6 +120,38 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
   }
 }
 
+// The decode step's append (pa_decode_append): the sequence's new token sits at position L - 1,
+// in this slab's row r.  Its key and value rows replace that row of the slab's shared-memory tiles
+// (the copy brought whatever the slot held before), and the CTA of the first head group also stores
+// them into the cache at the slot the block table gives, for later steps; no other CTA of this
+// launch reads that slot ("PagedAttention 详解：缓存的存储结构", section "写入新 K/V": the new token's K/V
+// goes to slot block * B + offset).  Lane l moves 16-byte chunk l % CH of the key (l < CH) or the
+// value row; the async proxy refills the buffer later, so the lanes fence their generic writes.
+template <typename T, int D>
+__device__ __forceinline__ void append_token(const DecodeParams& p, const Item& it, uint8_t* kst, int r, int lane) {
+  constexpr int CH = D * (int)sizeof(T) / 16;  // 16-byte chunks per row
+  constexpr int BOX_BYTES = kTcSlabTokens * 128;
+  const int G = p.num_q_heads / p.num_kv_heads;
+  if (lane < 2 * CH) {
+    const bool is_v = lane >= CH;
+    const int c = lane % CH;
+    const size_t row = (size_t)it.s * p.num_kv_heads + it.hkv;
+    const uint4 x = __ldg(reinterpret_cast<const uint4*>(is_v ? p.new_v : p.new_k) + row * CH + c);
+    uint8_t* tile = kst + (is_v ? (D / 64) * BOX_BYTES : 0);
+    *reinterpret_cast<uint4*>(tile + (c / 8) * BOX_BYTES + swz128(r, c % 8)) = x;
+    if (it.hq0 == it.hkv * G) {  // the first head group of the kv head writes the cache
+      const int pos = it.L - 1;
+      const int pb = __ldg(p.block_tables + (size_t)it.s * p.max_blocks + pos / p.block_size);
+      if (pb >= 0 && pb < p.num_blocks) {
+        const size_t dst = (((size_t)pb * p.num_kv_heads + it.hkv) * p.block_size + pos % p.block_size) * CH + c;
+        reinterpret_cast<uint4*>(is_v ? p.v_cache_out : p.k_cache_out)[dst] = x;
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncwarp();
+}
+
 template <typename T, int D, int NW, int NS>
 __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
@@ -248,7 +280,8 @@ __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
     if ((valid_mask >> stage) & 1u) {
       const int tok0 = (it.j0 + warp + k * NW) * S::SB;
       const int nvalid = min(S::SB, it.t_end - tok0);
-      const uint8_t* kst = ring + stage * S::SLAB_BYTES;
+      uint8_t* kst = ring + stage * S::SLAB_BYTES;
+      if (p.new_k != nullptr && it.L - 1 < tok0 + S::SB && it.L - 1 >= tok0) append_token<T, D>(p, it, kst, it.L - 1 - tok0, lane);
       process_slab<T, D>(kst, kst + S::NBOX * S::BOX_BYTES, nvalid, qf, o, m_a, m_b, l_a, l_b, lane, p.scale_log2,
                          bias_a, bias_b, (float)(tok0 - (it.L - 1)));
     }

@@ -30,6 +30,12 @@ struct DecodeParams {
   float scale_log2;           // scale * log2(e)
   const float* alibi;         // nullable [Hq]: score_i += slope_h * (i - (L - 1))
   int32_t test_expire_first_wait;  // test hook: each ring's first slab is never requested (0 in normal use)
+  // pa_decode_append (nullable otherwise): the new token of each sequence, [N][Hkv][D], stored at position
+  // L - 1 of both caches and attended in the same launch
+  const void* new_k;
+  const void* new_v;
+  void* k_cache_out;
+  void* v_cache_out;
 };
 
 // Kernel launchers (return the cudaGetLastError of the launch).

@@ -74,6 +74,17 @@ def test_decode_argument_errors(lib):
     assert call_decode(lib, desc(), n=0, out=None) == 0              # nothing to do, nothing launched
 
 
+def test_decode_append_argument_errors(lib):
+    def call(d, key=FAKE, value=FAKE, m=1):
+        return lib.pa_decode_append(FAKE, FAKE, FAKE, FAKE, key, value, FAKE, FAKE, 2, 4, m, ctypes.byref(d), 0.1, 0,
+                                    None, 0, None, None)
+    assert call(desc(dtype=pa.PA_F32)) == 2                          # the fused append is f16/bf16 only
+    assert call(desc(dtype=pa.PA_FP8_E4M3)) == 2
+    assert call(desc(), key=None) == 1
+    assert call(desc(), value=FAKE + 4) == 5                         # 16-byte rows
+    assert call(desc(), m=100) == 4                                  # split partitions need a workspace
+
+
 def test_partition_and_workspace_sizes(lib):
     d = desc(nb=16384, bs=16, hkv=8, d=128, dtype=pa.PA_BF16)
     assert pa.pa_decode_partition_size(2048, d, 0) == 1024            # library default

@@ -204,6 +204,46 @@ def test_default_split_garbage_workspace(case):
     _default_split_check(w)
 
 
+# ---------------------------------------------------------------- the decode step with its append fused in
+APPEND = [  # dtype, Hq, Hkv, D, B, lens (the last token of each sequence is the step's new token)
+    ("f16", 32, 32, 128, 16, [1, 2, 15, 16, 17, 700, 2048, 0]),  # L = 1: the new token alone; L = 0: nothing
+    ("bf16", 64, 8, 128, 32, [64, 1200, 4096, 33, 1]),            # G = 8
+    ("bf16", 24, 2, 64, 64, [1, 130, 1500, 64, 65]),              # G = 12: two head groups, the first writes
+    ("f16", 8, 2, 128, 8, [1, 8, 9, 16, 17, 300]),                # 8-token blocks: the token in either half
+]
+
+
+@pytest.mark.parametrize("case", APPEND, ids=lambda c: f"{c[0]}-Hq{c[1]}-Hkv{c[2]}-D{c[3]}-B{c[4]}")
+@pytest.mark.parametrize("split", ["default", "smallest"])
+def test_decode_append_fused(case, split):
+    """pa_decode_append stores each sequence's new token at position L - 1 (its slot starts as NaN)
+    and attends over it in one launch: the caches equal the oracle's append bit for bit, the output
+    meets the oracle, and both equal pa_reshape_and_cache followed by pa_decode bit for bit.  The
+    smallest partition (one block, or one 16-token slab for 8-token blocks) puts the new token in
+    the last of many partitions."""
+    import torch
+    dtype, Hq, Hkv, D, B, lens = case
+    partition = 0 if split == "default" else max(B, 16)
+    w = W.build_decode("append", seed=zlib.crc32(repr(case).encode()) % 10000, dtype=dtype, seq_lens=lens,
+                       num_q_heads=Hq, num_kv_heads=Hkv, head_size=D, block_size=B, pool_factor=1.3,
+                       append_last=True, partition_size=partition)
+    g = GpuStep(w)
+    g.pa.pa_decode_append(g.out, g.q, g.k, g.v, g.nk, g.nv, g.tables, g.lens, w.scale, partition_size=partition,
+                          workspace=g.ws, err_flag=g.err, desc=g.desc)
+    torch.cuda.synchronize()
+    k_ref, v_ref, ref = oracle_step(w)
+    assert int(g.err.item()) == 0
+    assert np.array_equal(to_numpy_storage(g.k, dtype).view(np.uint8), k_ref.view(np.uint8))
+    assert np.array_equal(to_numpy_storage(g.v, dtype).view(np.uint8), v_ref.view(np.uint8))
+    ok, err, ratio = within_bound(out_f64(g.out), ref, dtype)
+    assert ok, f"max abs err {err}, worst err/bound {ratio}"
+    two = GpuStep(w)
+    two.writes()
+    two.decode()
+    torch.cuda.synchronize()
+    assert torch.equal(g.out.view(torch.int16), two.out.view(torch.int16))
+
+
 def test_permuted_block_ids_bit_identical():
     """Relabelling physical blocks leaves the GPU output bit-identical."""
     import torch

@@ -281,7 +281,7 @@ def build_decode(name: str, *, seed: int, dtype: str, seq_lens, num_q_heads: int
                     scale=1.0 / math.sqrt(head_size), q=q, k_cache=k_cache, v_cache=v_cache,
                     block_tables=tables, seq_lens=np.asarray(seq_lens, dtype=np.int32),
                     slot_mapping=slot_mapping, new_key=new_key, new_value=new_value,
-                    partition_size=partition_size, info={"seed": seed})
+                    partition_size=partition_size, info={"seed": seed, "append_last": append_last})
 
 
 # ---------------------------------------------------------------------------
