@@ -58,7 +58,8 @@ struct Shape {
   static constexpr int WARP_MERGE = 8 * OROW + 16;         // per warp: O[8][OROW], (m, l)[8]
   static constexpr int BAR_OFF = NW * RING_BYTES;
   static constexpr int FLAG_OFF = BAR_OFF + NW * NS * 8;   // the CTA's abort flag
-  static constexpr int SMEM_BYTES = FLAG_OFF + 16 + 1024;  // + alignment slack
+  static constexpr int STAGE_OFF = FLAG_OFF + 16;         // the appended token's K and V rows (16-bit)
+  static constexpr int SMEM_BYTES = STAGE_OFF + 2 * D * 2 + 1024;  // + alignment slack
   static constexpr int THREADS = NW * 32;
   static_assert(D % 64 == 0, "head_size must be a multiple of 64");
   static_assert(NS >= 2, "a ring needs at least two buffers");
@@ -126,17 +127,19 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
 // them into the cache at the slot the block table gives, for later steps; no other CTA of this
 // launch reads that slot ("PagedAttention 详解：缓存的存储结构", section "写入新 K/V": the new token's K/V
 // goes to slot block * B + offset).  Lane l moves 16-byte chunk l % CH of the key (l < CH) or the
-// value row; the async proxy refills the buffer later, so the lanes fence their generic writes.
+// value row, which it copied into stage_rows at the start of the kernel (so the global load's latency
+// is not paid here); the async proxy refills the buffer later, so the lanes fence their generic writes.
 template <typename T, int D>
-__device__ __forceinline__ void append_token(const DecodeParams& p, const Item& it, uint8_t* kst, int r, int lane) {
+__device__ __forceinline__ void append_token(const DecodeParams& p, const Item& it, uint8_t* kst, int r, int lane,
+                                             const uint8_t* stage_rows) {
   constexpr int CH = D * (int)sizeof(T) / 16;  // 16-byte chunks per row
   constexpr int BOX_BYTES = kTcSlabTokens * 128;
   const int G = p.num_q_heads / p.num_kv_heads;
   if (lane < 2 * CH) {
     const bool is_v = lane >= CH;
     const int c = lane % CH;
-    const size_t row = (size_t)it.s * p.num_kv_heads + it.hkv;
-    const uint4 x = __ldg(reinterpret_cast<const uint4*>(is_v ? p.new_v : p.new_k) + row * CH + c);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    const uint4 x = *reinterpret_cast<const uint4*>(stage_rows + 16 * lane);
     uint8_t* tile = kst + (is_v ? (D / 64) * BOX_BYTES : 0);
     *reinterpret_cast<uint4*>(tile + (c / 8) * BOX_BYTES + swz128(r, c % 8)) = x;
     if (it.hq0 == it.hkv * G) {  // the first head group of the kv head writes the cache
@@ -172,6 +175,21 @@ __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF) + warp * NS;
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + S::FLAG_OFF);
   if (threadIdx.x == 0) abort_flag[0] = 0;
+  // the appended token's rows: the warp whose slab holds position L - 1 starts copying them now,
+  // so that they are in shared memory when that slab is processed
+  uint8_t* stage_rows = smem + S::STAGE_OFF;
+  {
+    constexpr int CH = D * 2 / 16;
+    const int apos = it.L - 1;
+    if (p.new_k != nullptr && apos >= it.j0 * S::SB && apos < it.t_end && ((apos / S::SB - it.j0) % NW) == warp &&
+        lane < 2 * CH) {
+      const size_t row = (size_t)it.s * p.num_kv_heads + it.hkv;
+      const void* src = reinterpret_cast<const uint4*>(lane >= CH ? p.new_v : p.new_k) + row * CH + lane % CH;
+      const uint32_t dst = (uint32_t)__cvta_generic_to_shared(stage_rows + 16 * lane);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n\tcp.async.commit_group;" ::"r"(dst), "l"(src)
+                   : "memory");
+    }
+  }
   if (lane == 0) {
     for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
     fence_barrier_init();
@@ -281,13 +299,14 @@ __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
       const int tok0 = (it.j0 + warp + k * NW) * S::SB;
       const int nvalid = min(S::SB, it.t_end - tok0);
       uint8_t* kst = ring + stage * S::SLAB_BYTES;
-      if (p.new_k != nullptr && it.L - 1 < tok0 + S::SB && it.L - 1 >= tok0) append_token<T, D>(p, it, kst, it.L - 1 - tok0, lane);
+      if (p.new_k != nullptr && it.L - 1 < tok0 + S::SB && it.L - 1 >= tok0) append_token<T, D>(p, it, kst, it.L - 1 - tok0, lane, stage_rows);
       process_slab<T, D>(kst, kst + S::NBOX * S::BOX_BYTES, nvalid, qf, o, m_a, m_b, l_a, l_b, lane, p.scale_log2,
                          bias_a, bias_b, (float)(tok0 - (it.L - 1)));
     }
     __syncwarp();
     if (k + NS < n_my) issue(k + NS);
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");  // the staged rows' copy, if its slab was skipped
   if (k < n_my) {  // timed out: let this warp's copies already in flight land first
     report_error(p.err_flag, PA_DEVERR_TIMEOUT);
     const int issued = n_my < k + NS ? n_my : k + NS;
