@@ -16,10 +16,20 @@
  *       sequence, head and partition; partition reduction for long contexts).
  *
  * Conventions shared by every call
- *  - All data pointers are DEVICE pointers owned by the caller.  No call
- *    allocates memory.  Between calls the library keeps only a lazily resolved
- *    driver entry point, per-kernel launch attributes and, for
+ *  - All data pointers are DEVICE-ACCESSIBLE addresses owned by the caller.  No
+ *    call allocates memory.  Between calls the library keeps only a lazily
+ *    resolved driver entry point, per-kernel launch attributes and, for
  *    pa_decode_noalloc alone, one fixed scratch array per device (see there).
+ *  - The K/V caches, the workspace and err_flag must be device memory (the
+ *    caches are read by tensor-map copies).  For the decode calls, the appends
+ *    and pa_copy_blocks, the small per-step arrays (q, out, block_tables,
+ *    seq_lens, slot_mapping, new key/value, block_pairs, ALiBi slopes) may
+ *    instead be pinned host memory mapped into the device's address space, as
+ *    every cudaHostAlloc / cudaMallocHost allocation is under unified
+ *    addressing: the kernels then read and write them in place over the host
+ *    link (NVLink-C2C on GB300), with no copy in between, and the results are
+ *    the same bytes as with device buffers.  pa_prefill moves q and out by
+ *    tensor-map copies: those two must be device memory there.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Every call is asynchronous on that stream.
  *  - Cache layout (both K and V): [num_blocks][num_kv_heads][block_size][head_size],
