@@ -290,9 +290,12 @@ class DeviceStep:
         self.fp8 = w.info.get("kv_dtype") == "fp8"
         self.k_scale, self.v_scale = w.info.get("k_scale"), w.info.get("v_scale")
         self.k, self.v = W.device_caches(w, device)
-        if self.fp8:  # E4M3 codes of x / scale (torch's conversion: inputs only); values [blocks][heads][B/16][D][16]
-            self.k = (self.k.float() / self.k_scale).to(torch.float8_e4m3fn).view(torch.uint8)
-            self.v = (self.v.float() / self.v_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+        if self.fp8:
+            # E4M3 codes of x / scale (torch's conversion: inputs only), saturated at +-448 as the library's
+            # append does (torch's conversion turns values past the range into NaN codes, which a draw of
+            # a billion N(0, 1) values / 0.0123 reaches); values [blocks][heads][B/16][D][16]
+            self.k = (self.k.float() / self.k_scale).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+            self.v = (self.v.float() / self.v_scale).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
             nb, hkv, bs, d = self.v.shape
             self.v = self.v.view(nb, hkv, bs // 16, 16, d).transpose(3, 4).contiguous()
             torch.cuda.empty_cache()
@@ -744,6 +747,8 @@ def run_ours(args, world, rank, local):
     err = int(ds.err.item())
     if err:
         raise RuntimeError(f"device error flag {err}")
+    if not bool(torch.isfinite(ds.out.float()).all()):
+        raise RuntimeError("non-finite decode output")
 
     kv = w.kv_bytes()
     value = world * kv / (ms_step * 1e-3) / 1e9
@@ -803,6 +808,8 @@ def run_ours(args, world, rank, local):
             msx, callx, dmx, _, (tx0, tx1) = time_device(dx, steps_x, args.warmup, 1)
             if int(dx.err.item()):
                 raise RuntimeError(f"device error flag {int(dx.err.item())} in {name}")
+            if not bool(torch.isfinite(dx.out.float()).all()):
+                raise RuntimeError(f"non-finite decode output in {name}")
             dm = msx if dx.single_call else callx
             ab = dx.decode_bytes()
             line["other_workloads"][name] = {
@@ -874,6 +881,8 @@ def bench_prefill(name: str, device, steps: int, warmup: int, peaks):
     sampler.stop()
     if int(ps.err.item()):
         raise RuntimeError(f"device error flag {int(ps.err.item())} in prefill")
+    if not bool(torch.isfinite(ps.out.float()).all()):
+        raise RuntimeError(f"non-finite prefill output in {name}")
     flops = w.prefill_flops()
     tflops = flops / (att * 1e-3) / 1e12
     peak = (peaks or {}).get("bf16_tflops")  # fp16 and bf16 share the dense tensor rate
