@@ -17,6 +17,16 @@ from harness import GpuStep, oracle_step, out_f64, within_bound
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import paged_kv_cache_32_gb300 as pa
+    pa.build()
+    return pa
+
+
 def _pinned(t):
     import torch
     h = torch.empty(t.shape, dtype=t.dtype).pin_memory()
@@ -87,3 +97,46 @@ def test_gqa_bf16_decode_with_host_inputs():
     assert int(hst.err.item()) == 0
     assert _same(dev.out, out)
     assert np.isfinite(out_f64(out)).all()
+
+
+def test_fp8_append_and_decode_with_host_inputs():
+    """The quantising FP8 append (fp16 key/value rows and slots in host memory) and FP8 decode (q,
+    tables, lengths and out in host memory)."""
+    import torch
+    import oracle as O
+    from harness import to_torch
+    w = W.build_decode("host_fp8", seed=21, dtype="f16", seq_lens=[3, 64, 900, 2000], num_q_heads=16,
+                       num_kv_heads=2, head_size=128, block_size=32, pool_factor=1.3, append_last=True,
+                       partition_size=512)
+    ks, vs = 0.0123, 0.0117
+    kc = O.quantize_cache_fp8(w.k_cache, ks, values=False)
+    vc = O.quantize_cache_fp8(w.v_cache, vs, values=True)
+    import paged_kv_cache_32_gb300 as pa
+
+    def run(host):
+        k = torch.from_numpy(np.ascontiguousarray(kc)).cuda()
+        v = torch.from_numpy(np.ascontiguousarray(vc)).cuda()
+        desc = pa.cache_desc(k)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        q = to_torch(w.q, "f16", "cuda")
+        nk, nv = to_torch(w.new_key, "f16", "cuda"), to_torch(w.new_value, "f16", "cuda")
+        slots = torch.from_numpy(w.slot_mapping).cuda()
+        tables, lens = torch.from_numpy(w.block_tables).cuda(), torch.from_numpy(w.seq_lens).cuda()
+        out = torch.full(q.shape, float("nan"), dtype=q.dtype, device="cuda")
+        if host:
+            q, nk, nv, slots, tables, lens = (_pinned(t) for t in (q, nk, nv, slots, tables, lens))
+            out = torch.full(out.shape, float("nan"), dtype=out.dtype).pin_memory()
+        pa.pa_reshape_and_cache_fp8(k, v, nk, nv, slots, ks, vs, err_flag=err, desc=desc)
+        need = pa.pa_decode_workspace_size(w.num_seqs, w.num_q_heads, w.max_blocks_per_seq, desc, 512)
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+        pa.pa_decode(out, q, k, v, tables, lens, w.scale, partition_size=512, workspace=ws, err_flag=err, desc=desc,
+                     k_scale=ks, v_scale=vs)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        return k, v, out
+
+    kd, vd, od = run(False)
+    kh, vh, oh = run(True)
+    assert _same(kd, kh) and _same(vd, vh)
+    assert _same(od, oh)
+    assert np.isfinite(out_f64(oh)).all()

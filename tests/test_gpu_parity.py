@@ -56,6 +56,32 @@ def test_mha_f16_with_append():
     print("mha_f16 max abs err", err)
 
 
+def test_mha_f16_full_size_fused_append():
+    """The benchmarked form of the MHA fp16 step: one pa_decode_append call at full size.  Both pools
+    equal the oracle's after its append bit for bit, every output element meets the oracle, and the
+    output equals the two-call path (pa_reshape_and_cache, then pa_decode) bit for bit."""
+    import torch
+    w = W.mha_f16()
+    g = GpuStep(w)
+    g.pa.pa_decode_append(g.out, g.q, g.k, g.v, g.nk, g.nv, g.tables, g.lens, w.scale,
+                          partition_size=w.partition_size, workspace=g.ws, err_flag=g.err, desc=g.desc)
+    torch.cuda.synchronize()
+    k_ref, v_ref, ref = oracle_step(w)
+    assert int(g.err.item()) == 0
+    assert np.array_equal(to_numpy_storage(g.k, w.dtype).view(np.uint8), k_ref.view(np.uint8))
+    assert np.array_equal(to_numpy_storage(g.v, w.dtype).view(np.uint8), v_ref.view(np.uint8))
+    got = out_f64(g.out)
+    ok, err, ratio = within_bound(got, ref, w.dtype)
+    assert ok, f"max abs err {err}, worst err/bound {ratio}"
+    if np.max(np.abs(ref)) < 1.0:
+        assert err <= TOL[w.dtype]
+    two = GpuStep(w)
+    two.writes()
+    two.decode()
+    torch.cuda.synchronize()
+    assert torch.equal(g.out.view(torch.int16), two.out.view(torch.int16))
+
+
 def test_gqa_bf16():
     w = W.gqa_bf16()
     err, g = check_step(w)
