@@ -48,7 +48,8 @@ WORKLOAD_DESC = {
     "long_bf16_b32": "long bf16 split-KV: 8 seqs x 32768 tokens, 32 q / 8 kv heads, D 128, B 32, 512-token partitions",
     "long_bf16_b64": "long bf16 split-KV: 8 seqs x 32768 tokens, 32 q / 8 kv heads, D 128, B 64, 512-token partitions",
     "mha_fp8": "MHA decode over an FP8 E4M3 cache (scales 0.0123 / 0.0117, fp16 q/out): 64 seqs, seq_lens "
-               "U[128,2048], 32 heads, D 128, B 16, pool 8192 shuffled, one quantising append per seq",
+               "U[128,2048], 32 heads, D 128, B 16, pool 8192 shuffled; each seq's new token quantised, appended and "
+               "attended in one pa_decode_append call",
     "gqa_fp8": "GQA decode over an FP8 E4M3 cache (fp16 q/out): 128 seqs, 64 q / 8 kv heads, D 128, B 32, "
                "lognormal(ln 1200, 0.6) lens in [64, 4096], pool 1.2x needed",
     "prefill_bf16": "chunked prefill bf16: 16 seqs, cached prefix U[0,2048] + chunk U[256,2048] tokens, 32 q / 8 kv "
@@ -324,7 +325,7 @@ class DeviceStep:
         self.pmax = 1 if need == 0 else -(-w.max_blocks_per_seq * w.block_size // self.part)
         # a step whose writes are each sequence's new token at its last position, on a 16-bit cache:
         # the append runs inside the decode call (pa_decode_append)
-        self.fused = bool(w.info.get("append_last")) and not self.fp8 and w.dtype in ("f16", "bf16") and \
+        self.fused = bool(w.info.get("append_last")) and w.dtype in ("f16", "bf16") and \
             self.pairs is None and self.slots is not None
         assert tdt == self.q.dtype
 
@@ -360,7 +361,9 @@ class DeviceStep:
                                  self.nv if nv is None else nv, self.tables if tables is None else tables,
                                  self.lens if lens is None else lens, self.w.scale,
                                  partition_size=self.w.partition_size, workspace=self.ws, err_flag=self.err,
-                                 stream=stream, desc=self.desc)
+                                 stream=stream, desc=self.desc,
+                                 alibi_slopes=self.alibi, k_scale=self.k_scale if self.fp8 else None,
+                                 v_scale=self.v_scale if self.fp8 else None)
 
     def decode(self, stream, q=None, tables=None, lens=None, out=None):
         self.pa.pa_decode(self.out if out is None else out, self.q if q is None else q, self.k, self.v,
@@ -372,15 +375,16 @@ class DeviceStep:
     def attend(self, stream):
         self.step_decode(stream)
 
-    def decode_bytes(self) -> int:
+    def decode_bytes(self, with_append: bool | None = None) -> int:
         """Algorithmic HBM bytes of one pa_decode call: K+V of every token, q in,
         out, table entries, and the split-KV partial results (written then read);
-        with the append fused in, also the new tokens' K/V read and written."""
+        with the append fused in (default: when the step fuses it), also the new
+        tokens' K/V read and written."""
         w = self.w
         eb = W.ELEM_BYTES[w.dtype]
         b = w.kv_bytes() + 2 * w.num_seqs * w.num_q_heads * w.head_size * eb
-        if self.fused:
-            b += 2 * 2 * int(np.sum(w.seq_lens > 0)) * w.num_kv_heads * w.head_size * eb
+        if self.fused if with_append is None else with_append:  # each new row read (key and value, the workload dtype) and written (the cache's codes)
+            b += int(np.sum(w.seq_lens > 0)) * w.num_kv_heads * w.head_size * 2 * (eb + (1 if self.fp8 else eb))
         b += int(np.sum(-(-w.seq_lens.astype(np.int64) // w.block_size))) * 4 + w.num_seqs * 4
         if self.pmax > 1:
             nparts = -(-w.seq_lens.astype(np.int64) // self.part)
@@ -425,14 +429,15 @@ class PrefillDeviceStep:
                            err_flag=self.err, stream=stream, desc=self.desc)
 
 
-def time_device(ds, steps: int, warmup: int, world: int):
+def time_device(ds, steps: int, warmup: int, world: int, call=None):
     """Device times of a step (ds.writes, then ds.attend), in three loops of `steps` each.
 
     1. The timed region: the steps back to back on one stream between two CUDA events, with a
        barrier and a device synchronisation on both sides and nothing else on the stream.  An
        event recorded between two launches ends the overlap of a launch with the previous one's
        end (programmatic dependent launch), so per-call events would slow the loop they time.
-    2. The attention call alone, back to back between two events: its mean duration.
+    2. The attention call alone (`call`, default ds.attend), back to back between two events: its
+       mean duration.
     3. Per-step event pairs around the writes and the call, for medians; each call there pays
        its launch's own start-up.
     Returns (mean step ms of 1, mean call ms of 2, call ms list of 3, writes ms list of 3,
@@ -457,10 +462,11 @@ def time_device(ds, steps: int, warmup: int, world: int):
         torch.cuda.synchronize()
         barrier(world)
         ms_step = start.elapsed_time(end) / steps
+        call = call or ds.attend
         a, b = ev_pair()
         a.record(stream)
         for _ in range(steps):
-            ds.attend(stream)
+            call(stream)
         b.record(stream)
         stream.synchronize()
         call_ms = a.elapsed_time(b) / steps
@@ -805,17 +811,25 @@ def run_ours(args, world, rank, local):
             wx = W.WORKLOADS[base](materialize=False)
             dx = DeviceStep(wx, device, alibi=suffix == "alibi")
             steps_x = max(EXTRA_STEPS, args.steps)
-            msx, callx, dmx, _, (tx0, tx1) = time_device(dx, steps_x, args.warmup, 1)
+            # the decode call's own fraction: a step that fuses its append is timed as a step, and its
+            # attention alone as back-to-back pa_decode calls
+            msx, callx, dmx, _, (tx0, tx1) = time_device(dx, steps_x, args.warmup, 1,
+                                                         call=dx.decode if dx.fused else None)
             if int(dx.err.item()):
                 raise RuntimeError(f"device error flag {int(dx.err.item())} in {name}")
             if not bool(torch.isfinite(dx.out.float()).all()):
                 raise RuntimeError(f"non-finite decode output in {name}")
-            dm = msx if dx.single_call else callx
-            ab = dx.decode_bytes()
+            dm = msx if dx.single_call and not dx.fused else callx
+            ab = dx.decode_bytes(with_append=False)
             line["other_workloads"][name] = {
                 "kv_gbs_step": round(wx.kv_bytes() / (msx * 1e-3) / 1e9, 1), "ms_per_step": round(msx, 5),
                 "steps": steps_x, "decode_ms": round(dm, 5),
-                "decode_ms_stat": "mean step of the timed region" if dx.single_call else "mean of back-to-back calls",
+                "decode_ms_stat": ("mean step of the timed region" if dx.single_call and not dx.fused else
+                                   "mean of back-to-back pa_decode calls"),
+                "step": "pa_decode_append (append fused)" if dx.fused else
+                        "+".join(x for x, t in (("pa_copy_blocks", dx.pairs), ("pa_reshape_and_cache", dx.slots))
+                                 if t is not None) + ("+" if dx.pairs is not None or dx.slots is not None else "") +
+                        "pa_decode",
                 "decode_ms_events_median": round(statistics.median(dmx), 5),
                 "decode_achieved_gbs": round(ab / (dm * 1e-3) / 1e9, 1),
                 "decode_frac": round(ab / (dm * 1e-3) / 1e9 / peak, 4), "tokens_per_s": round(wx.num_seqs / (msx * 1e-3), 1),

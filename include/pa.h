@@ -195,16 +195,22 @@ int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_ca
  *   CTA that streams the new token's slab takes the token's rows from key and
  *   value, and the first query-head group of each kv head stores them.
  *
- *   key, value   [num_seqs][num_kv_heads][head_size] of dtype, 16-byte aligned
- *   other arguments as for pa_decode; f16 and bf16 caches (fp32 and fp8: use
- *   pa_reshape_and_cache(_fp8) and pa_decode).  The slot at position L - 1 must
- *   belong to this sequence alone (the block manager copies a shared partial
- *   block on write first); a sequence's other slots are not written.
+ *   key, value   [num_seqs][num_kv_heads][head_size] of dtype (fp16 for an FP8 cache),
+ *                16-byte aligned
+ *   options      nullable, as for pa_decode_ex (ALiBi slopes, FP8 scales)
+ *   other arguments as for pa_decode; f16, bf16 and FP8 caches (fp32: use
+ *   pa_reshape_and_cache and pa_decode).  Over an FP8 cache the rows are
+ *   quantised as pa_reshape_and_cache_fp8 does (code of x / scale, fp32
+ *   division, ties to even, saturating at +-448), bit for bit.  The slot at
+ *   position L - 1 must belong to this sequence alone (the block manager copies
+ *   a shared partial block on write first); a sequence's other slots are not
+ *   written.
  */
 int pa_decode_append(void* out, const void* q, void* k_cache, void* v_cache, const void* key, const void* value,
                      const int32_t* block_tables, const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads,
                      int32_t max_blocks_per_seq, const pa_cache_desc* cache, float scale, int32_t partition_size,
-                     void* workspace, size_t workspace_bytes, int32_t* err_flag, void* stream);
+                     void* workspace, size_t workspace_bytes, int32_t* err_flag, void* stream,
+                     const pa_decode_options* options);
 
 /* Partition size pa_decode uses for these arguments (resolves 0 to the default);
  * returns a value >= max_blocks_per_seq * block_size when no split happens, or a

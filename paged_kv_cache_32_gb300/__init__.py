@@ -67,7 +67,7 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_ex.argtypes = L.pa_decode.argtypes + [ctypes.POINTER(pa_decode_options)]
         L.pa_decode_ex.restype = ctypes.c_int
         L.pa_decode_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, desc_p, ctypes.c_float, i32, vp, sz,
-                                       vp, vp]
+                                       vp, vp, ctypes.POINTER(pa_decode_options)]
         L.pa_decode_append.restype = ctypes.c_int
         L.pa_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, desc_p, ctypes.c_float, vp, vp]
         L.pa_prefill.restype = ctypes.c_int
@@ -200,10 +200,12 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale: float, pa
 
 def pa_decode_append(out, q, k_cache, v_cache, key, value, block_tables, seq_lens, scale: float,
                      partition_size: int = 0, workspace=None, err_flag=None, stream=None,
-                     desc: pa_cache_desc | None = None) -> None:
+                     desc: pa_cache_desc | None = None, alibi_slopes=None, k_scale: float | None = None,
+                     v_scale: float | None = None) -> None:
     """A decode step with its append: key/value [num_seqs, num_kv_heads, head_size] are each
     sequence's new token, stored at position seq_lens[s] - 1 of both caches (through the block
-    table) and attended in the same call.  fp16/bf16 caches."""
+    table) and attended in the same call.  fp16/bf16 caches, and FP8 caches (key/value fp16,
+    quantised with k_scale / v_scale as pa_reshape_and_cache_fp8 does)."""
     desc = desc or cache_desc(k_cache)
     for t, n in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (key, "key"), (value, "value"),
                  (block_tables, "block_tables"), (seq_lens, "seq_lens")):
@@ -215,10 +217,14 @@ def pa_decode_append(out, q, k_cache, v_cache, key, value, block_tables, seq_len
         import torch
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    opts = None
+    if alibi_slopes is not None or k_scale is not None or v_scale is not None:
+        _dense(alibi_slopes, "alibi_slopes")
+        opts = ctypes.byref(pa_decode_options(_ptr(alibi_slopes), float(k_scale or 0.0), float(v_scale or 0.0), 0))
     _check(lib().pa_decode_append(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(key), _ptr(value),
                                   _ptr(block_tables), _ptr(seq_lens), num_seqs, num_q_heads, max_blocks,
                                   ctypes.byref(desc), float(scale), int(partition_size), _ptr(workspace), ws_bytes,
-                                  _ptr(err_flag), _stream(stream)), "pa_decode_append")
+                                  _ptr(err_flag), _stream(stream), opts), "pa_decode_append")
 
 
 def pa_prefill(out, q, k_cache, v_cache, block_tables, seq_lens, query_start, max_query_len: int, scale: float,

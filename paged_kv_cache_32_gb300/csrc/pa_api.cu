@@ -270,14 +270,15 @@ int pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_ca
 int pa_decode_append(void* out, const void* q, void* k_cache, void* v_cache, const void* key, const void* value,
                      const int32_t* block_tables, const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads,
                      int32_t max_blocks_per_seq, const pa_cache_desc* cache, float scale, int32_t partition_size,
-                     void* workspace, size_t workspace_bytes, int32_t* err_flag, void* stream) {
+                     void* workspace, size_t workspace_bytes, int32_t* err_flag, void* stream,
+                     const pa_decode_options* options) {
   int rc = check_cache(cache);
   if (rc != PA_OK) return rc;
-  if (cache->dtype != PA_F16 && cache->dtype != PA_BF16) return PA_ERR_UNSUPPORTED;  // the tensor-core kernel
+  if (cache->dtype == PA_F32) return PA_ERR_UNSUPPORTED;  // the tensor-core and FP8 kernels append
   if (num_seqs > 0 && (key == nullptr || value == nullptr)) return PA_ERR_NULL_POINTER;
   if (!aligned(key, 16) || !aligned(value, 16)) return PA_ERR_MISALIGNED;
   return decode_call(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_q_heads, max_blocks_per_seq,
-                     cache, scale, partition_size, workspace, workspace_bytes, err_flag, stream, nullptr, key, value);
+                     cache, scale, partition_size, workspace, workspace_bytes, err_flag, stream, options, key, value);
 }
 
 int pa_reshape_and_cache(void* k_cache, void* v_cache, const void* key, const void* value,

@@ -67,7 +67,8 @@ struct Fp8Shape {
   static constexpr int WARP_MERGE = 8 * OROW + 16;
   static constexpr int BAR_OFF = NW * RING_BYTES;
   static constexpr int FLAG_OFF = BAR_OFF + NW * NS * 8;
-  static constexpr int SMEM_BYTES = FLAG_OFF + 16 + 1024;
+  static constexpr int STAGE_OFF = FLAG_OFF + 16;  // pa_decode_append: the new token's fp16 K and V rows
+  static constexpr int SMEM_BYTES = STAGE_OFF + 2 * D * 2 + 1024;
   static constexpr int THREADS = NW * 32;
   static_assert(D == 128, "the FP8 key box is one 128-byte swizzle row per token");
   static_assert(RING_BYTES >= WARP_MERGE * 4, "a warp's ring holds its partial result at the end");
@@ -142,6 +143,53 @@ __device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t r, uint32_t& lo, uint32_
       "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
       : "=r"(lo), "=r"(hi)
       : "r"(r));
+}
+
+// The decode step's append over an FP8 cache (pa_decode_append): the sequence's new token sits at
+// position L - 1, in row r (0..31) of this slab.  Its fp16 key and value rows, copied into stage_rows
+// when the CTA started, are quantised exactly as the quantising append does (code of x / scale, fp32
+// division, ties to even, saturating), replace that token's codes in the slab's shared-memory tiles (the
+// copy brought whatever the slot held), and the CTA of the first head group also stores them into the
+// caches at the slot the block table gives ("PagedAttention 详解：缓存的存储结构", section "写入新
+// K/V").  Lane l handles dimensions 4l .. 4l + 3: one 32-bit word of the key row, four bytes of the value
+// tile.  The async proxy refills the buffer later, so the lanes fence their generic writes.
+template <int D>
+__device__ __forceinline__ void append_token_fp8(const DecodeParams& p, const Fp8Item& it, uint8_t* kst, int r,
+                                                 int lane, const uint8_t* stage_rows, float k_scale, float v_scale) {
+  static_assert(D == 128, "one 32-bit word of key codes per lane");
+  constexpr int KBOX = 16 * D, VBOX = D * 16;
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  const uint2 kh = *reinterpret_cast<const uint2*>(stage_rows + 8 * lane);
+  const uint2 vh = *reinterpret_cast<const uint2*>(stage_rows + 2 * D + 8 * lane);
+  auto quant4 = [](uint2 h, float scale) -> uint32_t {
+    const __half2 a = *reinterpret_cast<const __half2*>(&h.x), b = *reinterpret_cast<const __half2*>(&h.y);
+    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+        make_float2(__fdiv_rn(__low2float(a), scale), __fdiv_rn(__high2float(a), scale)), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+        make_float2(__fdiv_rn(__low2float(b), scale), __fdiv_rn(__high2float(b), scale)), __NV_SATFINITE, __NV_E4M3);
+    return (uint32_t)lo | ((uint32_t)hi << 16);
+  };
+  const uint32_t kc = quant4(kh, k_scale), vc = quant4(vh, v_scale);
+  const int u = r >> 4, rr = r & 15;
+  *reinterpret_cast<uint32_t*>(kst + u * KBOX + swz128(rr, lane >> 2) + 4 * (lane & 3)) = kc;
+  uint8_t* vt = kst + 2 * KBOX + u * VBOX + rr;  // value tile of sub-slab u: byte d * 16 + token
+#pragma unroll
+  for (int i = 0; i < 4; ++i) vt[(4 * lane + i) * 16] = (uint8_t)(vc >> (8 * i));
+  const int G = p.num_q_heads / p.num_kv_heads;
+  if (it.hq0 == it.hkv * G) {  // the first head group of the kv head writes the caches
+    const int pos = it.L - 1;
+    const int pb = __ldg(p.block_tables + (size_t)it.s * p.max_blocks + pos / p.block_size);
+    if (pb >= 0 && pb < p.num_blocks) {
+      const int off = pos % p.block_size;
+      const size_t head_base = ((size_t)pb * p.num_kv_heads + it.hkv) * (size_t)p.block_size * D;
+      *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(p.k_cache_out) + head_base + (size_t)off * D + 4 * lane) = kc;
+      uint8_t* vg = static_cast<uint8_t*>(p.v_cache_out) + head_base + (size_t)(off / 16) * D * 16 + off % 16;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) vg[(size_t)(4 * lane + i) * 16] = (uint8_t)(vc >> (8 * i));
+    }
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
 }
 
 // key row of the S MMA's A row r: tau(r) (see the file comment)
@@ -286,6 +334,20 @@ __global__ void __launch_bounds__(Fp8Shape<D, NW, NS>::THREADS)
     for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
     fence_barrier_init();
   }
+  // pa_decode_append: the warp whose slab holds position L - 1 starts copying the new token's fp16 rows
+  // (lanes 0..15 the key, 16..31 the value, 16 bytes each) into the stage
+  uint8_t* stage_rows = smem + S::STAGE_OFF;
+  {
+    const int apos = it.L - 1;
+    if (p.new_k != nullptr && apos >= it.j0 && apos < it.t_end && ((apos - it.j0) / S::SB) % NW == warp) {
+      constexpr int CH = D * 2 / 16;
+      const size_t row = (size_t)it.s * p.num_kv_heads + it.hkv;
+      const void* src = reinterpret_cast<const uint4*>(lane >= CH ? p.new_v : p.new_k) + row * CH + lane % CH;
+      const uint32_t dst = smem_u32(stage_rows + 16 * lane);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n\tcp.async.commit_group;" ::"r"(dst), "l"(src)
+                   : "memory");
+    }
+  }
   __syncthreads();
 
   const int n_my = it.nslabs > warp ? (it.nslabs - warp + NW - 1) / NW : 0;
@@ -388,13 +450,17 @@ __global__ void __launch_bounds__(Fp8Shape<D, NW, NS>::THREADS)
     if ((valid_mask >> stage) & 1u) {
       const int tok0 = sub_tok(k, 0);
       const int nvalid = min(S::SB, it.t_end - tok0);
-      const uint8_t* kst = ring + stage * S::SLAB_BYTES;
+      uint8_t* kst = ring + stage * S::SLAB_BYTES;
+      // (a 16-token partition ends inside its last slab: the token must lie in this partition's part of it)
+      if (p.new_k != nullptr && it.L - 1 >= tok0 && it.L - 1 < tok0 + nvalid)
+        append_token_fp8<D>(p, it, kst, it.L - 1 - tok0, lane, stage_rows, k_scale, v_scale);
       fp8_slab<D>(kst, kst + S::NSUB * S::KBOX, nvalid, qf, o, m_a, m_b, l_a, l_b, lane, sl2, bias_a, bias_b,
                   (float)(tok0 - (it.L - 1)));
     }
     __syncwarp();
     if (k + NS < n_my) issue(k + NS);
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");  // the staged rows' copy, if its slab was skipped
   if (k < n_my) {  // timed out: let this warp's copies already in flight land first
     report_error(p.err_flag, PA_DEVERR_TIMEOUT);
     const int issued = n_my < k + NS ? n_my : k + NS;

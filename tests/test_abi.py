@@ -77,9 +77,9 @@ def test_decode_argument_errors(lib):
 def test_decode_append_argument_errors(lib):
     def call(d, key=FAKE, value=FAKE, m=1):
         return lib.pa_decode_append(FAKE, FAKE, FAKE, FAKE, key, value, FAKE, FAKE, 2, 4, m, ctypes.byref(d), 0.1, 0,
-                                    None, 0, None, None)
-    assert call(desc(dtype=pa.PA_F32)) == 2                          # the fused append is f16/bf16 only
-    assert call(desc(dtype=pa.PA_FP8_E4M3)) == 2
+                                    None, 0, None, None, None)
+    assert call(desc(dtype=pa.PA_F32)) == 2                          # no fused append over an fp32 cache
+    assert call(desc(dtype=pa.PA_FP8_E4M3), key=None) == 1           # FP8 caches take it (arguments checked)
     assert call(desc(), key=None) == 1
     assert call(desc(), value=FAKE + 4) == 5                         # 16-byte rows
     assert call(desc(), m=100) == 4                                  # split partitions need a workspace

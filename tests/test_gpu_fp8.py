@@ -241,3 +241,37 @@ def test_fp8_full_workload(name):
     if np.max(np.abs(ref)) < 1.0:
         assert err <= 3e-3
     print(name, "max abs err", err)
+
+
+# ---------------------------------------------------------------- the decode step with its quantising append fused in
+APPEND_FP8 = [  # Hq, Hkv, B, lens (the last token of each sequence is the step's new token)
+    (32, 32, 16, [1, 2, 15, 16, 17, 31, 32, 33, 700, 2048, 0]),  # B 16: a slab's halves in two blocks
+    (64, 8, 32, [1, 33, 64, 65, 1500, 4096]),                     # B 32: whole slabs, G 8
+    (24, 2, 48, [1, 47, 48, 49, 300]),                            # B 48, G 12: two head groups, the first writes
+]
+
+
+@pytest.mark.parametrize("case", APPEND_FP8, ids=lambda c: f"Hq{c[0]}-Hkv{c[1]}-B{c[2]}")
+@pytest.mark.parametrize("split", ["default", "smallest"])
+def test_fp8_decode_append_fused(case, split):
+    """pa_decode_append over an FP8 cache quantises each sequence's new fp16 row into the slot at
+    position L - 1 (which starts as NaN codes) and attends over it in one launch: both pools equal the
+    oracle's quantising append bit for bit, the output meets the oracle, and it equals
+    pa_reshape_and_cache_fp8 followed by pa_decode bit for bit."""
+    import torch
+    hq, hkv, B, lens = case
+    w = W.build_decode(f"fp8_append_{hq}x{hkv}_b{B}", seed=401 + B + hq, dtype="f16", seq_lens=lens, num_q_heads=hq,
+                       num_kv_heads=hkv, head_size=128, block_size=B, pool_factor=1.3, append_last=True)
+    part = 0 if split == "default" else B
+    fused, two = Fp8Step(w, 0.0123, 0.0117), Fp8Step(w, 0.0123, 0.0117)
+    fused.pa.pa_decode_append(fused.out, fused.q, fused.k, fused.v, fused.nk, fused.nv, fused.tables, fused.lens,
+                              w.scale, partition_size=part, err_flag=fused.err, desc=fused.desc, k_scale=fused.ks,
+                              v_scale=fused.vs)
+    torch.cuda.synchronize()
+    assert int(fused.err.item()) == 0
+    k, v = fused.host_after_append()
+    assert np.array_equal(fused.k.cpu().numpy(), k) and np.array_equal(fused.v.cpu().numpy(), v)
+    assert_close(out_f64(fused.out), fused.oracle(k, v), f"{w.name} fused, partition {part}")
+    two.append()
+    two.decode(partition_size=part)
+    assert torch.equal(fused.out.view(torch.int16), two.out.view(torch.int16))
