@@ -52,7 +52,9 @@
 //    significant bits alone would cost up to 2^-8 of a weight.
 //  * Rescaling: a row's reference max moves only when the tile max exceeds it
 //    by more than 8 (log2 units), so P <= 2^8 and O is rescaled in place
-//    (tcgen05.ld / st of the warp's 16 rows) on few tiles.
+//    (tcgen05.ld / st of the warp's 16 rows) on few tiles.  fp16 takes an
+//    unmasked tile's weights with the current reference maxima first and
+//    computes the tile maxima only when a weight could exceed 2^8 (same bits).
 //  * Epilogue: each warp reads its 16 rows of O (16x256b layout), releases O
 //    to the next item's first P V and normalises them (out = O / l).  bf16
 //    stores them from registers.  fp16, whose softmax warps set the pace,
@@ -93,6 +95,10 @@ constexpr int kSWarp = kSoftmaxWarps + 1;      // issues S = Q K^T
 constexpr int kLoadWarp0 = kSoftmaxWarps + 2;  // four producers: K half 0, K half 1, V half 0, V half 1
 constexpr int kThreads = (kSoftmaxWarps + 6) * 32;
 constexpr float kRescaleThreshold = 8.f;  // log2 units: P <= 2^8 between rescales
+// A tile's weights taken with the current reference maxima stand when no thread's share of a row's tile
+// sum exceeds this (so no weight does): then no weight is above 2^(threshold) - 1, no reference max would
+// move, and the tile's maxima are not needed.
+constexpr float kLazyBound = 255.f;
 constexpr long long kWaitCyclesPf = 500ll * 1000 * 1000;
 
 // bf16 keeps 8 significant bits, so P is fed to the tensor cores as two bf16
@@ -709,79 +715,104 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int key0 = kt * kTile + 2 * c4;          // key of this thread's pair 0
       const int e0 = lim0 - key0, e1 = lim1 - key0;  // pair j's keys 8j, 8j + 1 are visible up to e
       const bool unmasked = __all_sync(0xffffffffu, min(lim0, lim1) >= kt * kTile + kTile - 1);
-      // ---- the rows' tile maxima, and the reference maxima they imply
-      float a0 = -INFINITY, b0 = -INFINITY, a1 = -INFINITY, b1 = -INFINITY;  // two chains per row
+      // ---- fp16, an unmasked tile after the item's first: P with the current reference maxima, kept
+      //      when no weight can exceed 2^threshold (each thread's share of a row's tile sum is at most
+      //      kLazyBound).  The exact path below would then move no reference max and compute the same
+      //      words and sums, so the result is the same bit for bit; otherwise it runs and stores P again.
+      //      (bf16, whose P has two terms, would hold both paths' words and spill.)
+      bool lazy = !split_p<T>() && unmasked && kt > 0;
+      if (lazy) {
+        float n0 = l0, n1 = l1;
 #pragma unroll
-      for (int j = 0; j < 16; j += 2) {
-        a0 = max3(a0, v[4 * j], v[4 * j + 1]);
-        a1 = max3(a1, v[4 * j + 2], v[4 * j + 3]);
-        b0 = max3(b0, v[4 * j + 4], v[4 * j + 5]);
-        b1 = max3(b1, v[4 * j + 6], v[4 * j + 7]);
-      }
-      if (!unmasked) {
-        // The maxima over all 128 keys bound the visible keys' maxima from above.  A bound that moves
-        // no row's reference max decides as the visible maxima would, so those are taken only when
-        // the bound would move one (rare after an item's first tiles).
-        float u0 = fmaxf(a0, b0), u1 = fmaxf(a1, b1);
-        u0 = fmaxf(u0, __shfl_xor_sync(0xffffffffu, u0, 1));
-        u1 = fmaxf(u1, __shfl_xor_sync(0xffffffffu, u1, 1));
-        u0 = fmaxf(u0, __shfl_xor_sync(0xffffffffu, u0, 2));
-        u1 = fmaxf(u1, __shfl_xor_sync(0xffffffffu, u1, 2));
-        if (__any_sync(0xffffffffu, u0 * sl2 > m0 + kRescaleThreshold || u1 * sl2 > m1 + kRescaleThreshold)) {
-          a0 = b0 = a1 = b1 = -INFINITY;
-#pragma unroll
-          for (int j = 0; j < 16; j += 2) {
-            a0 = max3(a0, 8 * j <= e0 ? v[4 * j] : -INFINITY, 8 * j + 1 <= e0 ? v[4 * j + 1] : -INFINITY);
-            a1 = max3(a1, 8 * j <= e1 ? v[4 * j + 2] : -INFINITY, 8 * j + 1 <= e1 ? v[4 * j + 3] : -INFINITY);
-            b0 = max3(b0, 8 * j + 8 <= e0 ? v[4 * j + 4] : -INFINITY, 8 * j + 9 <= e0 ? v[4 * j + 5] : -INFINITY);
-            b1 = max3(b1, 8 * j + 8 <= e1 ? v[4 * j + 6] : -INFINITY, 8 * j + 9 <= e1 ? v[4 * j + 7] : -INFINITY);
-          }
+        for (int j0 = 0; j0 < 16; j0 += 8) {
+          uint32_t hi[16], lo[16];
+          make_p<T, false>(v, j0, sl2, m0, m1, e0, e1, hi, lo, n0, n1);
+          tmem_st16x128_x8(s_addr + 4 * j0, hi);
+          if constexpr (split_p<T>()) tmem_st16x128_x8(s_addr + 64 + 4 * j0, lo);
+        }
+        lazy = !__any_sync(0xffffffffu, n0 - l0 > kLazyBound || n1 - l1 > kLazyBound);
+        if (lazy) {
+          l0 = n0;
+          l1 = n1;
+        } else {
+          tmem_wait_st();  // the words stored above land before the exact path's stores
         }
       }
-      a0 = fmaxf(a0, b0);
-      a1 = fmaxf(a1, b1);
-      a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, 1));
-      a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
-      a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, 2));
-      a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 2));
-      const float mx0 = a0 * sl2, mx1 = a1 * sl2;  // scale > 0
-      const bool upd0 = mx0 > m0 + kRescaleThreshold, upd1 = mx1 > m1 + kRescaleThreshold;
-      const float al0 = upd0 ? fast_exp2(m0 - mx0) : 1.f, al1 = upd1 ? fast_exp2(m1 - mx1) : 1.f;
-      if (__any_sync(0xffffffffu, upd0 || upd1) && kt > 0 && ok) {
-        // O of these rows is rescaled between P V of tile tg - 1 and that of tile tg.  The barrier
-        // of its S buffer finished tile tg - 4 before S(tg - 1) was issued and its next phase (tile
-        // tg + 2) needs this warp's P, so the parity wait below is exact.
-        ok = warp_wait(&bar_o[(tg - 1) % kSBufs], ((tg - 1) / kSBufs) & 1);
-        tc_fence_after();
+      if (!lazy) {
+        // ---- the rows' tile maxima, and the reference maxima they imply
+        float a0 = -INFINITY, b0 = -INFINITY, a1 = -INFINITY, b1 = -INFINITY;  // two chains per row
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+          a0 = max3(a0, v[4 * j], v[4 * j + 1]);
+          a1 = max3(a1, v[4 * j + 2], v[4 * j + 3]);
+          b0 = max3(b0, v[4 * j + 4], v[4 * j + 5]);
+          b1 = max3(b1, v[4 * j + 6], v[4 * j + 7]);
+        }
+        if (!unmasked) {
+          // The maxima over all 128 keys bound the visible keys' maxima from above.  A bound that moves
+          // no row's reference max decides as the visible maxima would, so those are taken only when
+          // the bound would move one (rare after an item's first tiles).
+          float u0 = fmaxf(a0, b0), u1 = fmaxf(a1, b1);
+          u0 = fmaxf(u0, __shfl_xor_sync(0xffffffffu, u0, 1));
+          u1 = fmaxf(u1, __shfl_xor_sync(0xffffffffu, u1, 1));
+          u0 = fmaxf(u0, __shfl_xor_sync(0xffffffffu, u0, 2));
+          u1 = fmaxf(u1, __shfl_xor_sync(0xffffffffu, u1, 2));
+          if (__any_sync(0xffffffffu, u0 * sl2 > m0 + kRescaleThreshold || u1 * sl2 > m1 + kRescaleThreshold)) {
+            a0 = b0 = a1 = b1 = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+              a0 = max3(a0, 8 * j <= e0 ? v[4 * j] : -INFINITY, 8 * j + 1 <= e0 ? v[4 * j + 1] : -INFINITY);
+              a1 = max3(a1, 8 * j <= e1 ? v[4 * j + 2] : -INFINITY, 8 * j + 1 <= e1 ? v[4 * j + 3] : -INFINITY);
+              b0 = max3(b0, 8 * j + 8 <= e0 ? v[4 * j + 4] : -INFINITY, 8 * j + 9 <= e0 ? v[4 * j + 5] : -INFINITY);
+              b1 = max3(b1, 8 * j + 8 <= e1 ? v[4 * j + 6] : -INFINITY, 8 * j + 9 <= e1 ? v[4 * j + 7] : -INFINITY);
+            }
+          }
+        }
+        a0 = fmaxf(a0, b0);
+        a1 = fmaxf(a1, b1);
+        a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, 1));
+        a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
+        a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, 2));
+        a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 2));
+        const float mx0 = a0 * sl2, mx1 = a1 * sl2;  // scale > 0
+        const bool upd0 = mx0 > m0 + kRescaleThreshold, upd1 = mx1 > m1 + kRescaleThreshold;
+        const float al0 = upd0 ? fast_exp2(m0 - mx0) : 1.f, al1 = upd1 ? fast_exp2(m1 - mx1) : 1.f;
+        if (__any_sync(0xffffffffu, upd0 || upd1) && kt > 0 && ok) {
+          // O of these rows is rescaled between P V of tile tg - 1 and that of tile tg.  The barrier
+          // of its S buffer finished tile tg - 4 before S(tg - 1) was issued and its next phase (tile
+          // tg + 2) needs this warp's P, so the parity wait below is exact.
+          ok = warp_wait(&bar_o[(tg - 1) % kSBufs], ((tg - 1) / kSBufs) & 1);
+          tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          float o[32];
-          tmem_ld16x256_x8(tmem + half_base + kOCol + 64 * c, o);
-          tmem_wait_ld<32>(o);
+          for (int c = 0; c < 2; ++c) {
+            float o[32];
+            tmem_ld16x256_x8(tmem + half_base + kOCol + 64 * c, o);
+            tmem_wait_ld<32>(o);
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            o[i] *= al0, o[i + 1] *= al0;
-            o[i + 2] *= al1, o[i + 3] *= al1;
+            for (int i = 0; i < 32; i += 4) {
+              o[i] *= al0, o[i + 1] *= al0;
+              o[i + 2] *= al1, o[i + 3] *= al1;
+            }
+            tmem_st16x256_x8(tmem + half_base + kOCol + 64 * c, reinterpret_cast<const uint32_t*>(o));
           }
-          tmem_st16x256_x8(tmem + half_base + kOCol + 64 * c, reinterpret_cast<const uint32_t*>(o));
+          tmem_wait_st();
         }
-        tmem_wait_st();
-      }
-      if (upd0) m0 = mx0;
-      if (upd1) m1 = mx1;
-      // ---- P into the buffer, 8 pairs (32 columns of packed words) at a time: hi words in columns
-      //      0..63, lo words in 64..127
-      l0 *= al0;
-      l1 *= al1;
+        if (upd0) m0 = mx0;
+        if (upd1) m1 = mx1;
+        // ---- P into the buffer, 8 pairs (32 columns of packed words) at a time: hi words in columns
+        //      0..63, lo words in 64..127
+        l0 *= al0;
+        l1 *= al1;
 #pragma unroll
-      for (int j0 = 0; j0 < 16; j0 += 8) {
-        uint32_t hi[16], lo[16];
-        if (unmasked)
-          make_p<T, false>(v, j0, sl2, m0, m1, e0, e1, hi, lo, l0, l1);
-        else
-          make_p<T, true>(v, j0, sl2, m0, m1, e0, e1, hi, lo, l0, l1);
-        tmem_st16x128_x8(s_addr + 4 * j0, hi);
-        if constexpr (split_p<T>()) tmem_st16x128_x8(s_addr + 64 + 4 * j0, lo);
+        for (int j0 = 0; j0 < 16; j0 += 8) {
+          uint32_t hi[16], lo[16];
+          if (unmasked)
+            make_p<T, false>(v, j0, sl2, m0, m1, e0, e1, hi, lo, l0, l1);
+          else
+            make_p<T, true>(v, j0, sl2, m0, m1, e0, e1, hi, lo, l0, l1);
+          tmem_st16x128_x8(s_addr + 4 * j0, hi);
+          if constexpr (split_p<T>()) tmem_st16x128_x8(s_addr + 64 + 4 * j0, lo);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
