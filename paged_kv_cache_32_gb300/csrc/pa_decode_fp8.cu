@@ -244,14 +244,25 @@ __device__ __forceinline__ void fp8_slab(const uint8_t* kst, const uint8_t* vst,
       if (16 * u + tok_hi >= nvalid) s[u][2] = s[u][3] = -INFINITY;
     }
   }
-  float mx_a = fmaxf(fmaxf(s[0][0], s[0][2]), fmaxf(s[1][0], s[1][2]));
-  float mx_b = fmaxf(fmaxf(s[0][1], s[0][3]), fmaxf(s[1][1], s[1][3]));
+  // the running maxima stay while no score exceeds them by more than kSlabSlack (log2 units), as in the
+  // fp16/bf16 slab: then the slab's maxima and their shuffles are skipped
+  bool over = false;
 #pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, off));
-    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, off));
+  for (int u = 0; u < 2; ++u)
+    over = over || s[u][0] - m_a > kSlabSlack || s[u][1] - m_b > kSlabSlack || s[u][2] - m_a > kSlabSlack ||
+           s[u][3] - m_b > kSlabSlack;
+  float mn_a = m_a, mn_b = m_b;
+  if (__any_sync(0xffffffffu, over)) {
+    float mx_a = fmaxf(fmaxf(s[0][0], s[0][2]), fmaxf(s[1][0], s[1][2]));
+    float mx_b = fmaxf(fmaxf(s[0][1], s[0][3]), fmaxf(s[1][1], s[1][3]));
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, off));
+      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, off));
+    }
+    mn_a = fmaxf(m_a, mx_a);
+    mn_b = fmaxf(m_b, mx_b);
   }
-  const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
   if (__any_sync(0xffffffffu, mn_a != m_a || mn_b != m_b)) {  // a running max moved: rescale (rare after a while)
     const float al_a = fast_exp2(m_a - mn_a), al_b = fast_exp2(m_b - mn_b);
     l_a *= al_a;

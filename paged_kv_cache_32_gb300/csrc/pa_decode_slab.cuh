@@ -55,18 +55,33 @@ __device__ __forceinline__ void process_slab(const uint8_t* kst, const uint8_t* 
     if (g >= nvalid) s0 = s1 = -INFINITY;
     if (g + 8 >= nvalid) s2 = s3 = -INFINITY;
   }
-  float mx_a = fmaxf(s0, s2), mx_b = fmaxf(s1, s3);
+  // The running maxima stay while no score of the slab exceeds them by more than kSlabSlack (log2 units):
+  // the weights are then at most 2^kSlabSlack, and the slab's maxima, their shuffles and the rescale of O
+  // are skipped.  Otherwise the maxima move to the slab's (the first slab always: they start at -inf).
+  if (__any_sync(0xffffffffu, s0 - m_a > kSlabSlack || s1 - m_b > kSlabSlack || s2 - m_a > kSlabSlack ||
+                                  s3 - m_b > kSlabSlack)) {
+    float mx_a = fmaxf(s0, s2), mx_b = fmaxf(s1, s3);
 #pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, off));
-    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, off));
+    for (int off = 4; off < 32; off <<= 1) {
+      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, off));
+      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, off));
+    }
+    const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+    const float al_a = fast_exp2(m_a - mn_a), al_b = fast_exp2(m_b - mn_b);
+    m_a = mn_a;
+    m_b = mn_b;
+    l_a *= al_a;
+    l_b *= al_b;
+#pragma unroll
+    for (int i = 0; i < KSTEPS; ++i) {
+      o[i][0] *= al_a;
+      o[i][1] *= al_b;
+      o[i][2] *= al_a;
+      o[i][3] *= al_b;
+    }
   }
-  const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-  const float al_a = fast_exp2(m_a - mn_a), al_b = fast_exp2(m_b - mn_b);
-  m_a = mn_a;
-  m_b = mn_b;
-  const float p0 = fast_exp2(s0 - mn_a), p1 = fast_exp2(s1 - mn_b);
-  const float p2 = fast_exp2(s2 - mn_a), p3 = fast_exp2(s3 - mn_b);
+  const float p0 = fast_exp2(s0 - m_a), p1 = fast_exp2(s1 - m_b);
+  const float p2 = fast_exp2(s2 - m_a), p3 = fast_exp2(s3 - m_b);
   const uint32_t x0 = Mma<T>::pack(p0, p1);
   const uint32_t x1 = Mma<T>::pack(p2, p3);
   // bf16 keeps only 8 significant bits of P; its rounding residual goes
@@ -75,18 +90,11 @@ __device__ __forceinline__ void process_slab(const uint8_t* kst, const uint8_t* 
   if constexpr (kSplitP<T>) {
     y0 = Mma<T>::pack(p0 - Mma<T>::lo(x0), p1 - Mma<T>::hi(x0));
     y1 = Mma<T>::pack(p2 - Mma<T>::lo(x1), p3 - Mma<T>::hi(x1));
-    l_a = l_a * al_a + (p0 + p2);
-    l_b = l_b * al_b + (p1 + p3);
+    l_a += p0 + p2;
+    l_b += p1 + p3;
   } else {  // fp16: the sums use the rounded probabilities the value MMA multiplies with
-    l_a = l_a * al_a + (Mma<T>::lo(x0) + Mma<T>::lo(x1));
-    l_b = l_b * al_b + (Mma<T>::hi(x0) + Mma<T>::hi(x1));
-  }
-#pragma unroll
-  for (int i = 0; i < KSTEPS; ++i) {
-    o[i][0] *= al_a;
-    o[i][1] *= al_b;
-    o[i][2] *= al_a;
-    o[i][3] *= al_b;
+    l_a += Mma<T>::lo(x0) + Mma<T>::lo(x1);
+    l_b += Mma<T>::hi(x0) + Mma<T>::hi(x1);
   }
   // P^T fragments: (tokens 2q4, 2q4+1 | +8, +9 ; head g)
   const uint32_t pb0 = movmatrix_trans(x0);

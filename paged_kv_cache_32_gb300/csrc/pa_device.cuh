@@ -153,6 +153,10 @@ struct Mma<__nv_bfloat16> {
 
 // ---------------------------------------------------------------- math
 // 2^x via the hardware approximation (relative error ~2^-22); exp2(-inf) = +0.
+// Decode: log2 units a score may exceed its head's running max by before the max moves (the weights
+// stay at most 2^8, well inside fp16 and bf16)
+constexpr float kSlabSlack = 8.f;
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
