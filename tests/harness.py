@@ -27,6 +27,37 @@ MANTISSA_BITS = {"f16": 10, "bf16": 7}
 PRE_ROUNDING_EXCESS = 2.0 ** -12
 
 
+def rising_keys(w: W.Workload, c: float, seed: int, positions=None) -> None:
+    """Make a decode workload's scores rise along each sequence (in place): every query
+    becomes one vector u (N(0,1) entries) and key i of each sequence gains c * i * u,
+    so a query's score for key i grows by about c * |u|^2 per token.  The kernels' running
+    maxima then move on some slabs or tiles and stay on others.  ``positions``: for a
+    prefill workload, the number of cached tokens before each chunk (keys of the chunk
+    are the new_key rows, in query order)."""
+    rng = np.random.default_rng(seed)
+    u = rng.standard_normal(w.head_size)
+    B = w.block_size
+    k = O.to_f64(w.k_cache, w.dtype)
+    nk = O.to_f64(w.new_key, w.dtype) if w.new_key is not None else None
+    for s, L in enumerate(w.seq_lens):
+        L = int(L)
+        if positions is None:  # decode: with an append, position L - 1 arrives as new_key[s]
+            cached = L - 1 if (nk is not None and L > 0) else L
+            if nk is not None and L > 0:
+                nk[s] += c * (L - 1) * u
+        else:  # prefill: chunk token j (position cached + j) is new_key[query_start[s] + j]
+            cached = int(positions[s])
+            q0 = int(w.query_start[s])
+            for j in range(L - cached):
+                nk[q0 + j] += c * (cached + j) * u
+        for i in range(cached):
+            k[w.block_tables[s][i // B], :, i % B, :] += c * i * u
+    w.k_cache = W.to_storage(k, w.dtype)
+    if nk is not None:
+        w.new_key = W.to_storage(nk, w.dtype)
+    w.q = W.to_storage(np.broadcast_to(u, w.q.shape), w.dtype)
+
+
 def bound(ref: np.ndarray, dtype: str) -> np.ndarray:
     """Per-element error bound against the fp64 result.
 

@@ -16,7 +16,7 @@ import pytest
 
 import oracle as O
 import workloads as W
-from harness import out_f64, to_numpy_storage, to_torch, within_bound
+from harness import out_f64, rising_keys, to_numpy_storage, to_torch, within_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -93,6 +93,22 @@ def assert_close(got, ref, what):
     ok, err, ratio = within_bound(got, ref, "f16")
     assert ok, f"{what}: max abs err {err}, worst err/bound {ratio}"
     return err
+
+
+# ---------------------------------------------------------------- running maxima that move and stay
+@pytest.mark.parametrize("partition", [0, 64])
+def test_fp8_rising_scores_running_max(partition):
+    """Scores rising along each sequence by about 8 (log2 units) per 32-token slab: the FP8 kernel's
+    running maxima move on the slabs whose scores exceed them by more than 8 and stay on the others."""
+    w = W.build_decode("fp8_rising", seed=7710, dtype="f16", seq_lens=[1, 32, 33, 300, 1000, 2100],
+                       num_q_heads=16, num_kv_heads=2, head_size=128, block_size=32, append_last=True)
+    rising_keys(w, 0.015, seed=7711)
+    g = Fp8Step(w, 0.5, 0.02)
+    g.append()
+    k, v = g.host_after_append()
+    got = g.decode(partition_size=partition)
+    assert int(g.err.item()) == 0
+    assert_close(got, g.oracle(k, v), f"fp8 rising, partition {partition}")
 
 
 # ---------------------------------------------------------------- the append, bit-exact

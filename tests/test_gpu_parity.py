@@ -12,7 +12,7 @@ import pytest
 
 import oracle as O
 import workloads as W
-from harness import TOL, GpuStep, max_abs_err, oracle_step, out_f64, to_numpy_storage, within_bound
+from harness import TOL, GpuStep, max_abs_err, oracle_step, out_f64, rising_keys, to_numpy_storage, within_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -137,6 +137,19 @@ def test_small_cases(case, partition):
     # the 16-bit kernels' partitions are whole 16-token slabs: with 8-token blocks, two blocks
     part = {0: 0, "one_block": B if dtype == "f32" else max(B, 16), "big": 8 * max(B, 32)}[partition]
     check_step(w, partition_size=part)
+
+
+# ---------------------------------------------------------------- running maxima that move and stay
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("partition", [0, 64])
+def test_rising_scores_running_max(dtype, partition):
+    """Scores rising along each sequence by about 8 (log2 units) per 16-token slab: a head's running
+    max moves on the slabs whose scores exceed it by more than 8 and stays on the others, so both the
+    kept weights (up to 2^8) and the rescale of O run, within partitions and across the merge."""
+    w = W.build_decode(f"rising_{dtype}", seed=7700, dtype=dtype, seq_lens=[1, 16, 17, 300, 1000, 2100],
+                       num_q_heads=16, num_kv_heads=2, head_size=128, block_size=16, append_last=True)
+    rising_keys(w, 0.03, seed=7701)
+    check_step(w, partition_size=partition)
 
 
 # ---------------------------------------------------------------- the partition merge

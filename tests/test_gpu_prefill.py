@@ -18,7 +18,7 @@ import pytest
 
 import oracle as O
 import workloads as W
-from harness import out_f64, to_numpy_storage, to_torch, within_bound
+from harness import out_f64, rising_keys, to_numpy_storage, to_torch, within_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -166,6 +166,22 @@ def test_prefill_large_scores_rescale():
     assert int(g.err.item()) == 0
     k, v = host_pools(w)
     assert_close(got, oracle_prefill(w, k, v), "bf16", w.name)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_prefill_rising_scores(dtype):
+    """Scores rising along each sequence by about 9 (log2 units) per 128-key tile: fp16 keeps the
+    weights it took with the current reference maxima on some tiles and takes the exact path (tile
+    maxima, rescale of O, P stored again) on others; bf16 always takes the exact path."""
+    w = W.build_prefill(f"prefill_rising_{dtype}", seed=7720, dtype=dtype, prefix_lens=[700, 1500, 0, 64],
+                        chunk_lens=[300, 129, 260, 1], num_q_heads=4, num_kv_heads=2, head_size=128,
+                        block_size=16)
+    rising_keys(w, 0.0045, seed=7721, positions=[700, 1500, 0, 64])
+    g = PrefillStep(w)
+    got = g.run()
+    assert int(g.err.item()) == 0
+    k, v = host_pools(w)
+    assert_close(got, oracle_prefill(w, k, v), dtype, w.name)
 
 
 # ---------------------------------------------------------------- the full-size workloads, every row
