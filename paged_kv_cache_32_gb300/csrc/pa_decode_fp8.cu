@@ -26,8 +26,9 @@
 // one block, and a slab is one 32-row key box and one 4 KB run of values: two
 // copies instead of four, the same shared-memory image;
 // 32 tokens per slab halve the fixed per-slab work (barrier wait, block-table
-// shuffle, row-max shuffles) per byte against 16.  The output rescale is
-// skipped when no running max of the warp moved.  E4M3 values convert exactly to fp16 (cvt e4m3x2 -> f16x2), so
+// shuffle, row-max shuffles) per byte against 16.  A head's running max moves
+// only when a score exceeds it by more than 8 (log2 units); on the other slabs
+// the row maxima, their shuffles and the output rescale are skipped.  E4M3 values convert exactly to fp16 (cvt e4m3x2 -> f16x2), so
 // both contractions run on mma.m16n8k16 in fp16 with fp32 accumulation.  One
 // 32-bit ldmatrix element holds four FP8 codes, which fixes the k order inside
 // an MMA: slot 2c <- element 4c, 2c+1 <- 4c+1, 2c+8 <- 4c+2, 2c+9 <- 4c+3.

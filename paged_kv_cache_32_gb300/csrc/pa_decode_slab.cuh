@@ -1,7 +1,8 @@
 // pa_decode_slab.cuh - the per-slab step of the fp16/bf16 decode kernels: one
 // 16-token slab of one kv head against up to eight query heads, on mma.sync
 // tensor-core tiles, with the online softmax of "vLLM 核心工程深度剖析", section
-// "3.1 Kernel 签名与分块策略" (running max and sum, rescaled when the max grows).
+// "3.1 Kernel 签名与分块策略" (running max and sum, rescaled when the max grows;
+// here the max grows only by more than 8 in log2 units at a time).
 #pragma once
 
 #include <math.h>

@@ -26,7 +26,8 @@
 //    O^T[D x 8 heads] += V^T P^T on the tensor cores (mma.m16n8k16, fp32
 //    accumulate) from ldmatrix reads of the swizzled tiles, with movmatrix
 //    turning the probability tile from accumulator into operand layout, and an
-//    online softmax (running max and sum per head, fp32).  The warps' partial
+//    online softmax (running max and sum per head, fp32; the max moves only when
+//    a score exceeds it by more than 8 in log2 units).  The warps' partial
 //    results are merged through shared memory once, at the end of the item.
 //  The path is bound by HBM bandwidth (1 to 8 flop per byte); the tensor cores
 //  only keep the instruction count per byte low.
