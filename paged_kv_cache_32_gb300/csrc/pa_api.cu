@@ -65,6 +65,30 @@ int32_t num_partitions(int32_t max_blocks_per_seq, int32_t block_size, int32_t p
   return max_len <= part ? 1 : (int32_t)((max_len + part - 1) / part);
 }
 
+// The last sixteenth of the sequences, the last items of the grid, are cut into partitions of half the
+// size, so that the grid ends on shorter items.  Only for calls with a few partitions a sequence (longer
+// splits are uniform already) on the tensor-core kernels, and when the half partition still holds whole
+// blocks and whole 32-token slabs.  Measured against an eighth and a quarter of the sequences, and quarter
+// partitions: a sixteenth in halves was the best common choice for the GQA and FP8 steps.
+struct TailPlan {
+  int32_t seq0, ps, pmax;  // first tail sequence (num_seqs: none), its partition size, partition slots a row
+};
+constexpr int32_t kTailMaxPartitions = 8;
+constexpr int32_t kTailShare = 16;  // 1 / kTailShare of the sequences
+constexpr int32_t kTailCut = 2;    // partitions cut into kTailCut
+TailPlan tail_plan(int32_t num_seqs, int32_t pmax, int32_t part, const pa_cache_desc* c) {
+  const TailPlan none = {num_seqs, part, pmax};
+  const int32_t n = num_seqs / kTailShare, ps = part / kTailCut;
+  if (c->dtype == PA_F32 || pmax < 2 || pmax > kTailMaxPartitions || n == 0) return none;
+  if (part % kTailCut != 0 || ps % c->block_size != 0 || ps % 32 != 0) return none;
+  return {num_seqs - n, ps, kTailCut * pmax};
+}
+
+// Partition slots of a split call's workspace (one per row and partition slot).
+size_t workspace_slots(int32_t num_seqs, int32_t num_q_heads, int32_t pmax, const TailPlan& t) {
+  return ((size_t)t.seq0 * pmax + (size_t)(num_seqs - t.seq0) * t.pmax) * num_q_heads;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -144,10 +168,10 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t m
   if (part <= 0 || num_seqs < 0 || num_q_heads <= 0) return 0;
   const int32_t pmax = num_partitions(max_blocks_per_seq, cache->block_size, part);
   if (pmax <= 1) return 0;
-  const size_t rows = (size_t)num_seqs * num_q_heads * pmax;
-  const size_t o_bytes = rows * cache->head_size * sizeof(float);
+  const size_t slots = workspace_slots(num_seqs, num_q_heads, pmax, tail_plan(num_seqs, pmax, part, cache));
+  const size_t o_bytes = slots * cache->head_size * sizeof(float);
   const size_t o_padded = (o_bytes + 255) / 256 * 256;
-  return o_padded + rows * 2 * sizeof(float);
+  return o_padded + slots * 2 * sizeof(float);
 }
 
 int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
@@ -194,7 +218,9 @@ static int decode_call(void* out, const void* q, const void* k_cache, const void
     return PA_ERR_INVALID_ARG;
   const int G = num_q_heads / cache->num_kv_heads;
   const int head_groups = (G + 7) / 8;
-  const long long grid = (long long)num_seqs * cache->num_kv_heads * head_groups * pmax;
+  const TailPlan tail = tail_plan(num_seqs, pmax, part, cache);
+  const long long grid = (long long)tail.seq0 * cache->num_kv_heads * head_groups * pmax +
+                         (long long)(num_seqs - tail.seq0) * cache->num_kv_heads * head_groups * tail.pmax;
   if (grid > kInt32Max || (long long)num_seqs * num_q_heads > kInt32Max) return PA_ERR_TOO_LARGE;
 
   pa::DecodeParams p;
@@ -205,8 +231,8 @@ static int decode_call(void* out, const void* q, const void* k_cache, const void
   p.ws_o = nullptr;
   p.ws_ml = nullptr;
   if (need > 0) {
-    const size_t rows = (size_t)num_seqs * num_q_heads * pmax;
-    const size_t o_padded = (rows * cache->head_size * sizeof(float) + 255) / 256 * 256;
+    const size_t slots = workspace_slots(num_seqs, num_q_heads, pmax, tail);
+    const size_t o_padded = (slots * cache->head_size * sizeof(float) + 255) / 256 * 256;
     p.ws_o = static_cast<float*>(workspace);
     p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_padded);
   }
@@ -220,6 +246,9 @@ static int decode_call(void* out, const void* q, const void* k_cache, const void
   p.num_blocks = cache->num_blocks;
   p.partition_size = part;
   p.pmax = pmax;
+  p.tail_seq0 = tail.seq0;
+  p.tail_ps = tail.ps;
+  p.tail_pmax = tail.pmax;
   p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
   p.alibi = alibi;
   p.test_expire_first_wait =

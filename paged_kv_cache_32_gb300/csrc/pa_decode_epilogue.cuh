@@ -21,10 +21,12 @@ namespace pa {
 
 // Called by all NW * 32 threads after the CTA barrier that follows the warps'
 // partial stores.  Writes the normalised rows of out (TOut) when the item is a
-// whole sequence, else the unnormalised partial (o, m*, l) of partition `part`.
+// whole sequence, else the unnormalised partial (o, m*, l) of the item's
+// partition: workspace slot slot0 for the first of its rows, slot0 + g * stride
+// for row g.
 template <typename TOut, int D, int NW, int OROW, int RING_BYTES>
 __device__ __forceinline__ void finish_item(const uint8_t* smem, const DecodeParams& p, size_t row0, int gcount,
-                                            bool final_out, int part) {
+                                            bool final_out, size_t slot0, int stride) {
   constexpr int WARP_MERGE = 8 * OROW + 16;  // floats of one warp's partial
   static_assert(RING_BYTES >= (WARP_MERGE + 8 * NW + 16) * 4, "warp 0's ring also holds the head weights");
   const float* rings = reinterpret_cast<const float*>(smem);
@@ -64,7 +66,7 @@ __device__ __forceinline__ void finish_item(const uint8_t* smem, const DecodePar
       const float l = lsum[gh];
       reinterpret_cast<TOut*>(p.out)[(row0 + gh) * D + d] = from_float<TOut>(l > 0.f ? acc / l : 0.f);
     } else {
-      const size_t slot = (row0 + gh) * p.pmax + part;
+      const size_t slot = slot0 + (size_t)gh * stride;
       p.ws_o[slot * D + d] = acc;
       if (d == 0) {
         p.ws_ml[slot * 2] = mst[gh];

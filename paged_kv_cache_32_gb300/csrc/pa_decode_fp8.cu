@@ -81,10 +81,9 @@ struct Fp8Item {
 };
 
 __device__ __forceinline__ bool fp8_item(const DecodeParams& p, int id, Fp8Item& it) {
-  const int per_seq = p.num_kv_heads * p.head_groups;
-  it.part = id % p.pmax;
-  const int hh = (id / p.pmax) % per_seq;
-  it.s = id / (p.pmax * per_seq);
+  int hh;
+  decode_item_ids(p, id, it.s, hh, it.part);
+  const int ps = seq_partition_size(p, it.s);
   it.hkv = hh / p.head_groups;
   const int hg = hh % p.head_groups;
   const int G = p.num_q_heads / p.num_kv_heads;
@@ -93,17 +92,17 @@ __device__ __forceinline__ bool fp8_item(const DecodeParams& p, int id, Fp8Item&
   int L = __ldg(p.seq_lens + it.s);
   L = max(0, min(L, p.max_blocks * p.block_size));
   it.L = L;
-  const int t_begin = it.part * p.partition_size;
+  const int t_begin = it.part * ps;
   if (L == 0) {
     it.t_end = it.j0 = it.nslabs = 0;
     it.final_out = true;
     return it.part == 0;
   }
   if (t_begin >= L) return false;
-  it.t_end = min(L, t_begin + p.partition_size);
+  it.t_end = min(L, t_begin + ps);
   it.j0 = t_begin;  // slabs of 2 x 16 tokens are counted from the partition's first token
   it.nslabs = (it.t_end - t_begin + 2 * kTcSlabTokens - 1) / (2 * kTcSlabTokens);
-  it.final_out = L <= p.partition_size;
+  it.final_out = L <= ps;
   return true;
 }
 
@@ -505,7 +504,8 @@ __global__ void __launch_bounds__(Fp8Shape<D, NW, NS>::THREADS)
   __syncthreads();
 
   finish_item<__half, D, NW, S::OROW, S::RING_BYTES>(smem, p, (size_t)it.s * p.num_q_heads + it.hq0, it.gcount,
-                                                     it.final_out, it.part);
+                                                     it.final_out, ws_row_slot(p, it.s, it.hq0) + it.part,
+                                                     seq_partition_slots(p, it.s));
 }
 
 // The quantising append: block (token, kv head); thread d handles element d.
@@ -551,7 +551,7 @@ cudaError_t launch_decode_fp8(int head_size, const CUtensorMap& tk, const CUtens
   auto kernel = decode_fp8_kernel<128, 4, 2>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const long long items = (long long)p.num_seqs * p.num_kv_heads * p.head_groups * p.pmax;
+  const long long items = decode_grid_size(p);
   if (items == 0) return cudaSuccess;
   return launch_dependent(kernel, dim3((unsigned)items), dim3(S::THREADS), S::SMEM_BYTES, stream, tk, tk32,
                           static_cast<const uint8_t*>(v_cache), p, k_scale, v_scale);

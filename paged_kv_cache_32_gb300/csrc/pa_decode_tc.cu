@@ -78,10 +78,9 @@ struct Item {
 };
 
 __device__ __forceinline__ bool decode_item(const DecodeParams& p, int id, Item& it) {
-  const int per_seq = p.num_kv_heads * p.head_groups;
-  it.part = id % p.pmax;
-  const int hh = (id / p.pmax) % per_seq;
-  it.s = id / (p.pmax * per_seq);
+  int hh;
+  decode_item_ids(p, id, it.s, hh, it.part);
+  const int ps = seq_partition_size(p, it.s);
   it.hkv = hh / p.head_groups;
   const int hg = hh % p.head_groups;
   const int G = p.num_q_heads / p.num_kv_heads;
@@ -90,7 +89,7 @@ __device__ __forceinline__ bool decode_item(const DecodeParams& p, int id, Item&
   int L = __ldg(p.seq_lens + it.s);
   L = max(0, min(L, p.max_blocks * p.block_size));
   it.L = L;
-  const int t_begin = it.part * p.partition_size;
+  const int t_begin = it.part * ps;
   if (L == 0) {  // an empty sequence: partition 0 writes a zero row
     it.t_end = 0;
     it.j0 = 0;
@@ -99,10 +98,10 @@ __device__ __forceinline__ bool decode_item(const DecodeParams& p, int id, Item&
     return it.part == 0;
   }
   if (t_begin >= L) return false;
-  it.t_end = min(L, t_begin + p.partition_size);
+  it.t_end = min(L, t_begin + ps);
   it.j0 = t_begin / kTcSlabTokens;
   it.nslabs = (it.t_end - t_begin + kTcSlabTokens - 1) / kTcSlabTokens;
-  it.final_out = L <= p.partition_size;
+  it.final_out = L <= ps;
   return true;
 }
 
@@ -340,7 +339,8 @@ __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
   __syncthreads();
 
   finish_item<T, D, NW, S::OROW, S::RING_BYTES>(smem, p, (size_t)it.s * p.num_q_heads + it.hq0, it.gcount,
-                                                it.final_out, it.part);
+                                                it.final_out, ws_row_slot(p, it.s, it.hq0) + it.part,
+                                                seq_partition_slots(p, it.s));
 }
 
 // ------------------------------------------------------------------ launch
@@ -351,7 +351,7 @@ static cudaError_t launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const
   auto kernel = decode_tc_kernel<T, D, NW, NS>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const long long items = (long long)p.num_seqs * p.num_kv_heads * p.head_groups * p.pmax;
+  const long long items = decode_grid_size(p);
   if (items == 0) return cudaSuccess;
   return launch_dependent(kernel, dim3((unsigned)items), dim3(S::THREADS), S::SMEM_BYTES, stream, tk, tv, p);
 }

@@ -27,6 +27,10 @@ struct DecodeParams {
   int32_t num_blocks;
   int32_t partition_size;     // tokens per partition (multiple of B)
   int32_t pmax;               // partitions per sequence in the grid
+  // Sequences tail_seq0 .. num_seqs - 1 (the last in the grid's order) are cut into partitions of tail_ps
+  // tokens, tail_pmax per sequence in the grid, so that the grid ends on short items (tail_seq0 =
+  // num_seqs: none).  Their partials follow the others' in the workspace, tail_pmax slots a row.
+  int32_t tail_seq0, tail_ps, tail_pmax;
   float scale_log2;           // scale * log2(e)
   const float* alibi;         // nullable [Hq]: score_i += slope_h * (i - (L - 1))
   int32_t test_expire_first_wait;  // test hook: each ring's first slab is never requested (0 in normal use)
@@ -37,6 +41,41 @@ struct DecodeParams {
   void* k_cache_out;
   void* v_cache_out;
 };
+
+// Partition size of sequence s.
+__host__ __device__ inline int seq_partition_size(const DecodeParams& p, int s) {
+  return s >= p.tail_seq0 ? p.tail_ps : p.partition_size;
+}
+// Partition slots per row of sequence s in the workspace.
+__host__ __device__ inline int seq_partition_slots(const DecodeParams& p, int s) {
+  return s >= p.tail_seq0 ? p.tail_pmax : p.pmax;
+}
+// Workspace slot of partition 0 of row (sequence s, query head h); the row's partitions follow it.
+__host__ __device__ inline size_t ws_row_slot(const DecodeParams& p, int s, int h) {
+  if (s < p.tail_seq0) return ((size_t)s * p.num_q_heads + h) * p.pmax;
+  return (size_t)p.tail_seq0 * p.num_q_heads * p.pmax + ((size_t)(s - p.tail_seq0) * p.num_q_heads + h) * p.tail_pmax;
+}
+// CTAs of a decode launch: one per (sequence, kv head, head group, partition slot).
+__host__ __device__ inline long long decode_grid_size(const DecodeParams& p) {
+  const long long per_seq = (long long)p.num_kv_heads * p.head_groups;
+  return (long long)p.tail_seq0 * per_seq * p.pmax + (long long)(p.num_seqs - p.tail_seq0) * per_seq * p.tail_pmax;
+}
+// The work item of CTA id: sequence, kv-head group slot hh (kv head * head_groups + group) and partition.
+// The host keeps the grid within int32, so the divisions are 32-bit.
+__host__ __device__ inline void decode_item_ids(const DecodeParams& p, int id, int& s, int& hh, int& part) {
+  const int per_seq = p.num_kv_heads * p.head_groups;
+  const int grid_a = p.tail_seq0 * per_seq * p.pmax;
+  if (id < grid_a) {
+    part = id % p.pmax;
+    hh = (id / p.pmax) % per_seq;
+    s = id / (p.pmax * per_seq);
+  } else {
+    const int j = id - grid_a;
+    part = j % p.tail_pmax;
+    hh = (j / p.tail_pmax) % per_seq;
+    s = p.tail_seq0 + j / (p.tail_pmax * per_seq);
+  }
+}
 
 // Kernel launchers (return the cudaGetLastError of the launch).
 cudaError_t launch_decode_tc(int dtype, int head_size, int block_size, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -68,10 +68,14 @@ __global__ void __launch_bounds__(kMergeThreads, 5) merge_kernel(const DecodePar
   const int sub = warp % WPR;
   const long long row = (long long)blockIdx.x * ROWS + warp / WPR;
   int nparts = 0;
+  size_t slot0 = 0;  // the row's first partition slot in the workspace
   if (row < (long long)p.num_seqs * p.num_q_heads) {  // seq_lens is an input of the step, not a decode output
-    int L = p.seq_lens[row / p.num_q_heads];
+    const int s = (int)(row / p.num_q_heads);
+    int L = p.seq_lens[s];
     L = max(0, min(L, p.max_blocks * p.block_size));
-    nparts = (L + p.partition_size - 1) / p.partition_size;
+    const int ps = seq_partition_size(p, s);
+    nparts = (L + ps - 1) / ps;
+    slot0 = ws_row_slot(p, s, (int)(row % p.num_q_heads));
   }
   griddep_wait();  // the decode grid has finished; its partials are visible
 
@@ -80,8 +84,8 @@ __global__ void __launch_bounds__(kMergeThreads, 5) merge_kernel(const DecodePar
   for (int e = 0; e < V; ++e) acc[e] = 0.f;
   float lsum = 0.f;
   if (nparts > 1) {  // a single partition was written out by the decode kernel
-    const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + (size_t)row * p.pmax;  // (m_p, l_p)
-    const float* os = p.ws_o + (size_t)row * p.pmax * D + lane * V;
+    const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + slot0;  // (m_p, l_p)
+    const float* os = p.ws_o + slot0 * D + lane * V;
     // One round trip: this warp's first kMergePreload partial outputs and lane i's pair (m_i, l_i).
     float pre[kMergePreload][V];
 #pragma unroll
@@ -139,6 +143,7 @@ __global__ void __launch_bounds__(kMergeThreads, 5) merge_kernel(const DecodePar
 template <typename T, int D>
 static cudaError_t launch_merge_t(const DecodeParams& p, cudaStream_t stream) {
   const long long rows = (long long)p.num_seqs * p.num_q_heads;
+  // warps per row from the main partitions (rows of tail sequences, with up to twice as many, loop over the rest)
   const int wpr = p.pmax <= 4 ? 1 : p.pmax <= 8 ? 2 : p.pmax <= 16 ? 4 : 8;
   const long long per_cta = (kMergeThreads / 32) / wpr;
   const dim3 grid((unsigned)((rows + per_cta - 1) / per_cta)), block(kMergeThreads);
