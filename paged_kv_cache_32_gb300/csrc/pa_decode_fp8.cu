@@ -326,7 +326,8 @@ __global__ void __launch_bounds__(Fp8Shape<D, NW, NS>::THREADS)
                       const float v_scale) {
   using S = Fp8Shape<D, NW, NS>;
   griddep_launch_dependents();  // the partition merge may be scheduled behind this grid's last CTAs
-  griddep_wait();               // launched as a dependent: the previous kernel's writes are visible from here
+  // seq_lens, block_tables, q and the ALiBi slopes are read before griddepcontrol.wait: no kernel of this
+  // library writes them, so their loads overlap the end of the kernel before this one on the stream
   Fp8Item it;
   if (!fp8_item(p, blockIdx.x, it)) return;
 
@@ -338,29 +339,6 @@ __global__ void __launch_bounds__(Fp8Shape<D, NW, NS>::THREADS)
   uint8_t* ring = smem + warp * S::RING_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF) + warp * NS;
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + S::FLAG_OFF);
-  if (threadIdx.x == 0) {
-    abort_flag[0] = 0;
-  }
-  if (lane == 0) {
-    for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
-    fence_barrier_init();
-  }
-  // pa_decode_append: the warp whose slab holds position L - 1 starts copying the new token's fp16 rows
-  // (lanes 0..15 the key, 16..31 the value, 16 bytes each) into the stage
-  uint8_t* stage_rows = smem + S::STAGE_OFF;
-  {
-    const int apos = it.L - 1;
-    if (p.new_k != nullptr && apos >= it.j0 && apos < it.t_end && ((apos - it.j0) / S::SB) % NW == warp) {
-      constexpr int CH = D * 2 / 16;
-      const size_t row = (size_t)it.s * p.num_kv_heads + it.hkv;
-      const void* src = reinterpret_cast<const uint4*>(lane >= CH ? p.new_v : p.new_k) + row * CH + lane % CH;
-      const uint32_t dst = smem_u32(stage_rows + 16 * lane);
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n\tcp.async.commit_group;" ::"r"(dst), "l"(src)
-                   : "memory");
-    }
-  }
-  __syncthreads();
-
   const int n_my = it.nslabs > warp ? (it.nslabs - warp + NW - 1) / NW : 0;
   const int B = p.block_size;
   // B a multiple of 32: a slab (32 tokens from a multiple of 32; partitions start on block boundaries)
@@ -397,6 +375,32 @@ __global__ void __launch_bounds__(Fp8Shape<D, NW, NS>::THREADS)
     if (2 * c + 1 < it.gcount) bias_b = __ldg(p.alibi + it.hq0 + 2 * c + 1) * kLog2e;
   }
   const float sl2 = p.scale_log2 * k_scale;  // scores of the stored codes, in log2 units
+
+  if (threadIdx.x == 0) {
+    abort_flag[0] = 0;
+    tma_prefetch_descriptor(whole_slabs ? &tmap_k32 : &tmap_k);
+  }
+  if (lane == 0) {
+    for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  griddep_wait();  // launched as a dependent: the previous kernel's writes (cache, output) are visible from here
+  // pa_decode_append: the warp whose slab holds position L - 1 starts copying the new token's fp16 rows
+  // (lanes 0..15 the key, 16..31 the value, 16 bytes each) into the stage
+  uint8_t* stage_rows = smem + S::STAGE_OFF;
+  {
+    const int apos = it.L - 1;
+    if (p.new_k != nullptr && apos >= it.j0 && apos < it.t_end && ((apos - it.j0) / S::SB) % NW == warp) {
+      constexpr int CH = D * 2 / 16;
+      const size_t row = (size_t)it.s * p.num_kv_heads + it.hkv;
+      const void* src = reinterpret_cast<const uint4*>(lane >= CH ? p.new_v : p.new_k) + row * CH + lane % CH;
+      const uint32_t dst = smem_u32(stage_rows + 16 * lane);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n\tcp.async.commit_group;" ::"r"(dst), "l"(src)
+                   : "memory");
+    }
+  }
 
   uint32_t valid_mask = 0;
   auto issue = [&](int k) {  // the whole warp, k increasing

@@ -161,7 +161,8 @@ __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
                      const DecodeParams p) {
   using S = Shape<D, NW, NS>;
   griddep_launch_dependents();  // the partition merge may be scheduled behind this grid's last CTAs
-  griddep_wait();               // launched as a dependent: the previous kernel's writes are visible from here
+  // seq_lens, block_tables, q and the ALiBi slopes are read before griddepcontrol.wait: no kernel of this
+  // library writes them, so their loads overlap the end of the kernel before this one on the stream
   Item it;
   if (!decode_item(p, blockIdx.x, it)) return;  // partition past the end of its sequence
 
@@ -174,28 +175,6 @@ __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
   uint8_t* ring = smem + warp * S::RING_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF) + warp * NS;
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + S::FLAG_OFF);
-  if (threadIdx.x == 0) abort_flag[0] = 0;
-  // the appended token's rows: the warp whose slab holds position L - 1 starts copying them now,
-  // so that they are in shared memory when that slab is processed
-  uint8_t* stage_rows = smem + S::STAGE_OFF;
-  {
-    constexpr int CH = D * 2 / 16;
-    const int apos = it.L - 1;
-    if (p.new_k != nullptr && apos >= it.j0 * S::SB && apos < it.t_end && ((apos / S::SB - it.j0) % NW) == warp &&
-        lane < 2 * CH) {
-      const size_t row = (size_t)it.s * p.num_kv_heads + it.hkv;
-      const void* src = reinterpret_cast<const uint4*>(lane >= CH ? p.new_v : p.new_k) + row * CH + lane % CH;
-      const uint32_t dst = (uint32_t)__cvta_generic_to_shared(stage_rows + 16 * lane);
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n\tcp.async.commit_group;" ::"r"(dst), "l"(src)
-                   : "memory");
-    }
-  }
-  if (lane == 0) {
-    for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
-    fence_barrier_init();
-  }
-  __syncthreads();
-
   // ---- this warp's slabs: j = warp + k * NW, k < n_my
   const int n_my = it.nslabs > warp ? (it.nslabs - warp + NW - 1) / NW : 0;
   const int B = p.block_size;
@@ -233,6 +212,34 @@ __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
     constexpr float kLog2e = 1.4426950408889634f;
     if (2 * q4 < it.gcount) bias_a = __ldg(p.alibi + it.hq0 + 2 * q4) * kLog2e;
     if (2 * q4 + 1 < it.gcount) bias_b = __ldg(p.alibi + it.hq0 + 2 * q4 + 1) * kLog2e;
+  }
+
+  if (threadIdx.x == 0) {
+    abort_flag[0] = 0;
+    tma_prefetch_descriptor(&tmap_k);
+    tma_prefetch_descriptor(&tmap_v);
+  }
+  if (lane == 0) {
+    for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  griddep_wait();  // launched as a dependent: the previous kernel's writes (cache, output) are visible from here
+  // the appended token's rows: the warp whose slab holds position L - 1 starts copying them now,
+  // so that they are in shared memory when that slab is processed
+  uint8_t* stage_rows = smem + S::STAGE_OFF;
+  {
+    constexpr int CH = D * 2 / 16;
+    const int apos = it.L - 1;
+    if (p.new_k != nullptr && apos >= it.j0 * S::SB && apos < it.t_end && ((apos / S::SB - it.j0) % NW) == warp &&
+        lane < 2 * CH) {
+      const size_t row = (size_t)it.s * p.num_kv_heads + it.hkv;
+      const void* src = reinterpret_cast<const uint4*>(lane >= CH ? p.new_v : p.new_k) + row * CH + lane % CH;
+      const uint32_t dst = (uint32_t)__cvta_generic_to_shared(stage_rows + 16 * lane);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n\tcp.async.commit_group;" ::"r"(dst), "l"(src)
+                   : "memory");
+    }
   }
 
   uint32_t valid_mask = 0;  // bit `stage`: the slab in that buffer was loaded
