@@ -224,9 +224,9 @@ int32_t pa_decode_partition_size(int32_t max_blocks_per_seq, const pa_cache_desc
 /* Bytes of workspace pa_decode needs: (head_size + 2) * 4 bytes (fp32 partial output,
  * maximum and sum) per row (sequence, query head) and partition slot, each part padded
  * to 256 bytes.  A row has P_max = ceil(max_blocks_per_seq * block_size / partition)
- * slots; on the fp16/bf16/FP8 kernels, when 2 <= P_max <= 8, the last num_seqs / 16
- * sequences (the grid's last items) are split into partitions of half the size and
- * their rows have 2 P_max slots.  0 when no sequence can span two partitions.  Returns
+ * slots; on the fp16/bf16/FP8 kernels, when 2 <= P_max <= 8, the last num_seqs / 12
+ * (fp16/bf16) or num_seqs / 24 (FP8) sequences (the grid's last items) are split into
+ * partitions of half the size and their rows have 2 P_max slots.  0 when no sequence can span two partitions.  Returns
  * 0 for invalid arguments as well (pa_decode then reports the argument error). */
 size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
                                 const pa_cache_desc* cache, int32_t partition_size);
@@ -315,10 +315,10 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pairs, int
  *   - Which sizes fit: the workspace is about num_seqs * num_q_heads * P_max *
  *     (head_size + 2) * 4 bytes (pa_decode_workspace_size gives it exactly).
  *     At the default 1024-token partition, 64 sequences x 32 heads of up to
- *     2048 tokens need 2.3 MB and 128 x 32 heads of up to 1280 tokens 4.5 MB;
+ *     2048 tokens need 2.3 MB and 128 x 32 heads of up to 1280 tokens 4.6 MB;
  *     8 sequences x 32 heads of 32768 tokens in 512-token partitions need
- *     8.5 MB.  128 sequences x 64 query heads of up to 4096 tokens need 18.1 MB,
- *     over the limit: pass partition_size 2048 (9.1 MB) for them.  Sequences
+ *     8.5 MB.  128 sequences x 64 query heads of up to 4096 tokens need 18.4 MB,
+ *     over the limit: pass partition_size 2048 (9.2 MB) for them.  Sequences
  *     that fit one partition need none.
  *   - The first call on a device, whatever its sizes, looks up the array's
  *     device address with that device current and caches it.  Under CUDA's lazy

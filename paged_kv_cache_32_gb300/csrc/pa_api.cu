@@ -65,20 +65,22 @@ int32_t num_partitions(int32_t max_blocks_per_seq, int32_t block_size, int32_t p
   return max_len <= part ? 1 : (int32_t)((max_len + part - 1) / part);
 }
 
-// The last sixteenth of the sequences, the last items of the grid, are cut into partitions of half the
-// size, so that the grid ends on shorter items.  Only for calls with a few partitions a sequence (longer
-// splits are uniform already) on the tensor-core kernels, and when the half partition still holds whole
-// blocks and whole 32-token slabs.  Measured against an eighth and a quarter of the sequences, and quarter
-// partitions: a sixteenth in halves was the best common choice for the GQA and FP8 steps.
+// The last twelfth of the sequences (fp16/bf16 caches) or twenty-fourth (FP8), the last items of the grid,
+// are cut into partitions of half the size, so that the grid ends on shorter items.  Only for calls with a
+// few partitions a sequence (longer splits are uniform already) on the tensor-core kernels, and when the
+// half partition still holds whole blocks and whole 32-token slabs.  Measured against other shares (an
+// eighth to a twenty-fourth) and quarter partitions on the GQA and FP8 steps: the 16-bit kernel, whose
+// items take longer, gains most from a longer tail of short items.
 struct TailPlan {
   int32_t seq0, ps, pmax;  // first tail sequence (num_seqs: none), its partition size, partition slots a row
 };
 constexpr int32_t kTailMaxPartitions = 8;
-constexpr int32_t kTailShare = 16;  // 1 / kTailShare of the sequences
-constexpr int32_t kTailCut = 2;    // partitions cut into kTailCut
+constexpr int32_t kTailShare16 = 12;  // 1 / kTailShare16 of the sequences over fp16/bf16 caches
+constexpr int32_t kTailShareFp8 = 24; // 1 / kTailShareFp8 over FP8 caches
+constexpr int32_t kTailCut = 2;       // partitions cut into kTailCut
 TailPlan tail_plan(int32_t num_seqs, int32_t pmax, int32_t part, const pa_cache_desc* c) {
   const TailPlan none = {num_seqs, part, pmax};
-  const int32_t n = num_seqs / kTailShare, ps = part / kTailCut;
+  const int32_t n = num_seqs / (c->dtype == PA_FP8_E4M3 ? kTailShareFp8 : kTailShare16), ps = part / kTailCut;
   if (c->dtype == PA_F32 || pmax < 2 || pmax > kTailMaxPartitions || n == 0) return none;
   if (part % kTailCut != 0 || ps % c->block_size != 0 || ps % 32 != 0) return none;
   return {num_seqs - n, ps, kTailCut * pmax};
