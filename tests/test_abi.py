@@ -98,6 +98,33 @@ def test_partition_and_workspace_sizes(lib):
     assert pa.pa_decode_workspace_size(8, 32, 16, d, 0) == 0
 
 
+def test_workspace_size_with_half_partition_tail(lib):
+    """The documented rule: with 2 <= P_max <= 8 on the 16-bit and FP8 caches, the last num_seqs // 12
+    (fp16/bf16) or num_seqs // 24 (FP8) sequences take partitions of half the size and 2 P_max slots a row,
+    when the half partition holds whole blocks and whole 32-token slabs; the outputs' part is padded to 256
+    bytes, then (m, l) pairs follow."""
+    def size(slots, d=128):
+        return -(-slots * d * 4 // 256) * 256 + slots * 2 * 4
+
+    def slots(n, hq, pmax, tail_n, cut=2):
+        return ((n - tail_n) * pmax + tail_n * cut * pmax) * hq
+
+    bf16 = desc(nb=16384, bs=32, hkv=8, d=128, dtype=pa.PA_BF16)
+    fp8 = desc(nb=16384, bs=32, hkv=8, d=128, dtype=pa.PA_FP8_E4M3)
+    f32 = desc(nb=16384, bs=32, hkv=8, d=128, dtype=pa.PA_F32)
+    # 128 sequences x 64 query heads of up to 4096 tokens, 1024-token partitions: P_max = 4
+    assert pa.pa_decode_workspace_size(128, 64, 128, bf16, 0) == size(slots(128, 64, 4, 128 // 12))
+    assert pa.pa_decode_workspace_size(128, 64, 128, fp8, 0) == size(slots(128, 64, 4, 128 // 24))
+    assert pa.pa_decode_workspace_size(128, 64, 128, f32, 0) == size(slots(128, 64, 4, 0))
+    # P_max = 16 (256-token partitions): uniform
+    assert pa.pa_decode_workspace_size(128, 64, 128, bf16, 256) == size(slots(128, 64, 16, 0))
+    # fewer than twelve sequences: no tail
+    assert pa.pa_decode_workspace_size(11, 64, 128, bf16, 0) == size(slots(11, 64, 4, 0))
+    # a half partition of 128 tokens is not a whole 256-token block: uniform
+    big_blocks = desc(nb=4096, bs=256, hkv=8, d=128, dtype=pa.PA_BF16)
+    assert pa.pa_decode_workspace_size(128, 64, 4, big_blocks, 256) == size(slots(128, 64, 4, 0))
+
+
 def call_prefill(lib, d, out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, sl=FAKE, qs=FAKE, n=2, tq=64, hq=4, m=4, mql=32,
                  scale=0.1):
     return lib.pa_prefill(out, q, k, v, bt, sl, qs, n, tq, hq, m, mql, ctypes.byref(d), scale, None, None)
