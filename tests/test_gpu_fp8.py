@@ -259,6 +259,29 @@ def test_fp8_full_workload(name):
     print(name, "max abs err", err)
 
 
+def test_fp8_decode_append_full_workload():
+    """The benchmarked MHA FP8 step at full size: one pa_decode_append call, whose CTAs quantise and
+    attend each sequence's new token, with the last sequences of the grid in half-size partitions.  Both
+    pools equal the oracle's quantising append bit for bit, every output meets the oracle, and the output
+    equals pa_reshape_and_cache_fp8 followed by pa_decode bit for bit."""
+    import torch
+    w = W.WORKLOADS["mha_fp8"]()
+    fused = Fp8Step(w, w.info["k_scale"], w.info["v_scale"])
+    fused.pa.pa_decode_append(fused.out, fused.q, fused.k, fused.v, fused.nk, fused.nv, fused.tables, fused.lens,
+                              w.scale, partition_size=w.partition_size, err_flag=fused.err, desc=fused.desc,
+                              k_scale=fused.ks, v_scale=fused.vs)
+    torch.cuda.synchronize()
+    assert int(fused.err.item()) == 0
+    k, v = fused.host_after_append()
+    assert np.array_equal(fused.k.cpu().numpy(), k) and np.array_equal(fused.v.cpu().numpy(), v)
+    assert_close(out_f64(fused.out), fused.oracle(k, v), "mha_fp8 fused")
+    two = Fp8Step(w, w.info["k_scale"], w.info["v_scale"])
+    two.append()
+    two.decode()
+    assert int(two.err.item()) == 0
+    assert torch.equal(fused.out.view(torch.int16), two.out.view(torch.int16))
+
+
 # ---------------------------------------------------------------- the decode step with its quantising append fused in
 APPEND_FP8 = [  # Hq, Hkv, B, lens (the last token of each sequence is the step's new token)
     (32, 32, 16, [1, 2, 15, 16, 17, 31, 32, 33, 700, 2048, 0]),  # B 16: a slab's halves in two blocks
