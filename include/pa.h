@@ -141,13 +141,13 @@ enum {
  *   Launches: the decode kernel, then (when a sequence spans two partitions) the
  *   merge kernel, both with programmatic stream serialization.  Their CTAs may be
  *   scheduled while the kernel before them on `stream` finishes.  They read
- *   seq_lens, block_tables, q and alibi_slopes at once, and execute
- *   griddepcontrol.wait before they read anything else (the caches, key/value,
- *   the workspace) or write anything, so stream order holds as for a plain
- *   launch provided that those four inputs are not written by a kernel that
- *   lets its dependents start early (no kernel of this library writes them;
- *   copies and kernels launched without programmatic serialization complete
- *   first).  Stream capture records the dependencies as programmatic edges.
+ *   seq_lens and block_tables at once, and execute griddepcontrol.wait before
+ *   they read anything else (q, the caches, key/value, the workspace) or write
+ *   anything, so stream order holds as for a plain launch provided that those
+ *   two inputs are not written by a kernel that lets its dependents start
+ *   early (no kernel of this library writes them; copies, and kernels that do
+ *   not execute griddepcontrol.launch_dependents, complete first).  Stream
+ *   capture records the dependencies as programmatic edges.
  */
 int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
               const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,

@@ -326,8 +326,9 @@ __global__ void __launch_bounds__(Fp8Shape<D, NW, NS>::THREADS)
                       const float v_scale) {
   using S = Fp8Shape<D, NW, NS>;
   griddep_launch_dependents();  // the partition merge may be scheduled behind this grid's last CTAs
-  // seq_lens, block_tables, q and the ALiBi slopes are read before griddepcontrol.wait: no kernel of this
-  // library writes them, so their loads overlap the end of the kernel before this one on the stream
+  // seq_lens and block_tables are read before griddepcontrol.wait: no kernel of this library writes them.
+  // q and the ALiBi slopes, which a GEMM before this kernel may produce, are read after it; the CTA's q
+  // rows are only prefetched into L2 before it (a later load of them sees the final data).
   Fp8Item it;
   if (!fp8_item(p, blockIdx.x, it)) return;
 
@@ -355,6 +356,20 @@ __global__ void __launch_bounds__(Fp8Shape<D, NW, NS>::THREADS)
   int pb_batch = 0;
   int pb_reg0 = fetch(lane, 0), pb_reg1 = fetch(lane, 1);
 
+  if (warp == 0)
+    prefetch_l2(reinterpret_cast<const __half*>(p.q) + ((size_t)it.s * p.num_q_heads + it.hq0) * D,
+                it.gcount * D * (int)sizeof(__half), lane);
+  if (threadIdx.x == 0) {
+    abort_flag[0] = 0;
+    tma_prefetch_descriptor(whole_slabs ? &tmap_k32 : &tmap_k);
+  }
+  if (lane == 0) {
+    for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  griddep_wait();  // launched as a dependent: the previous kernel's writes (cache, output) are visible from here
   // ---- query fragments (B operand of S^T = K Q^T): head g; k-step j covers dimensions
   //      16j .. 16j+15 in the order of the key fragments: slots (2c, 2c+1 | 2c+8, 2c+9) <- 4c .. 4c+3
   uint32_t qf[D / 16][2];
@@ -376,17 +391,6 @@ __global__ void __launch_bounds__(Fp8Shape<D, NW, NS>::THREADS)
   }
   const float sl2 = p.scale_log2 * k_scale;  // scores of the stored codes, in log2 units
 
-  if (threadIdx.x == 0) {
-    abort_flag[0] = 0;
-    tma_prefetch_descriptor(whole_slabs ? &tmap_k32 : &tmap_k);
-  }
-  if (lane == 0) {
-    for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
-    fence_barrier_init();
-  }
-  __syncthreads();
-
-  griddep_wait();  // launched as a dependent: the previous kernel's writes (cache, output) are visible from here
   // pa_decode_append: the warp whose slab holds position L - 1 starts copying the new token's fp16 rows
   // (lanes 0..15 the key, 16..31 the value, 16 bytes each) into the stage
   uint8_t* stage_rows = smem + S::STAGE_OFF;

@@ -161,8 +161,9 @@ __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
                      const DecodeParams p) {
   using S = Shape<D, NW, NS>;
   griddep_launch_dependents();  // the partition merge may be scheduled behind this grid's last CTAs
-  // seq_lens, block_tables, q and the ALiBi slopes are read before griddepcontrol.wait: no kernel of this
-  // library writes them, so their loads overlap the end of the kernel before this one on the stream
+  // seq_lens and block_tables are read before griddepcontrol.wait: no kernel of this library writes them.
+  // q and the ALiBi slopes, which a GEMM before this kernel may produce, are read after it; the CTA's q
+  // rows are only prefetched into L2 before it (a later load of them sees the final data).
   Item it;
   if (!decode_item(p, blockIdx.x, it)) return;  // partition past the end of its sequence
 
@@ -193,6 +194,21 @@ __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
   int pb_batch = 0, pb_reg, pb_reg2;
   fetch(lane, pb_reg, pb_reg2);
 
+  if (warp == 0)
+    prefetch_l2(reinterpret_cast<const T*>(p.q) + ((size_t)it.s * p.num_q_heads + it.hq0) * D,
+                it.gcount * D * (int)sizeof(T), lane);
+  if (threadIdx.x == 0) {
+    abort_flag[0] = 0;
+    tma_prefetch_descriptor(&tmap_k);
+    tma_prefetch_descriptor(&tmap_v);
+  }
+  if (lane == 0) {
+    for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  griddep_wait();  // launched as a dependent: the previous kernel's writes (cache, output) are visible from here
   // ---- query fragments (B operand of S^T = K Q^T): head g, dims 16j + 2q4 (+8)
   uint32_t qf[S::KSTEPS][2];
   {
@@ -214,18 +230,6 @@ __global__ void __launch_bounds__(Shape<D, NW, NS>::THREADS)
     if (2 * q4 + 1 < it.gcount) bias_b = __ldg(p.alibi + it.hq0 + 2 * q4 + 1) * kLog2e;
   }
 
-  if (threadIdx.x == 0) {
-    abort_flag[0] = 0;
-    tma_prefetch_descriptor(&tmap_k);
-    tma_prefetch_descriptor(&tmap_v);
-  }
-  if (lane == 0) {
-    for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
-    fence_barrier_init();
-  }
-  __syncthreads();
-
-  griddep_wait();  // launched as a dependent: the previous kernel's writes (cache, output) are visible from here
   // the appended token's rows: the warp whose slab holds position L - 1 starts copying them now,
   // so that they are in shared memory when that slab is processed
   uint8_t* stage_rows = smem + S::STAGE_OFF;

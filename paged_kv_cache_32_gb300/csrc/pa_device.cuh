@@ -190,6 +190,13 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---------------------------------------------------------------- errors
+// Brings the lines of [base, base + bytes) into L2, one 128-byte line per lane and step.  L2 is the
+// device's point of coherence, so a later load sees whatever was written after the prefetch.
+__device__ __forceinline__ void prefetch_l2(const void* base, int bytes, int lane) {
+  for (int off = lane * 128; off < bytes; off += 32 * 128)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char*>(base) + off));
+}
+
 __device__ __forceinline__ void report_error(int32_t* flag, int32_t code) {
   if (flag != nullptr) atomicCAS(flag, 0, code);
 }
