@@ -226,7 +226,8 @@ int32_t pa_decode_partition_size(int32_t max_blocks_per_seq, const pa_cache_desc
  * to 256 bytes.  A row has P_max = ceil(max_blocks_per_seq * block_size / partition)
  * slots; on the fp16/bf16/FP8 kernels, when 2 <= P_max <= 8, the last num_seqs / 12
  * (fp16/bf16) or num_seqs / 24 (FP8) sequences (the grid's last items) are split into
- * partitions of half the size and their rows have 2 P_max slots.  0 when no sequence can span two partitions.  Returns
+ * partitions of half the size, if that half is a multiple of block_size and of 32,
+ * and their rows have 2 P_max slots.  0 when no sequence can span two partitions.  Returns
  * 0 for invalid arguments as well (pa_decode then reports the argument error). */
 size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
                                 const pa_cache_desc* cache, int32_t partition_size);
